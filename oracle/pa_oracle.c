@@ -1,0 +1,321 @@
+/*
+ * pa_oracle.c -- plain fp64 CPU oracle for one decode step of paged attention.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark load this file. The CUDA library never includes, links
+ * or calls it, and it includes nothing from the CUDA library.
+ *
+ * What it computes, and where the definition comes from:
+ *
+ *  append   Each new token's K and V row is copied, bit for bit, into its slot
+ *           of the paged pool. A slot is block * block_size + offset, the flat
+ *           form of the paged indexing in "MLSys Engineer -- Inference Systems
+ *           Q&A", Q1 "How does PagedAttention work?" (the kernel rewrite). The
+ *           decode step appends before it attends: "LLM inference and
+ *           serving", "Code from memory", the naive incremental decoder (the
+ *           cache append, then softmax over every row seen so far).
+ *
+ *  gather   Row i of a sequence's K (and V) lives in physical block
+ *           block_table[i / block_size] at offset i % block_size (same Q1).
+ *           The oracle rebuilds the sequence's contiguous K and V this way.
+ *
+ *  attend   Textbook single-query attention per query head, in fp64, from the
+ *           values stored in the cache dtype: S_i = scale * <q, K_i>,
+ *           w_i = exp(S_i - max S), out = sum_i (w_i / sum w) V_i (the naive
+ *           decoder above, with the running-max subtraction of Q4 "How would
+ *           you write a fused attention kernel?" used only for stability).
+ *           Grouped-query attention: query head qh reads KV head
+ *           qh / (num_heads / num_kv_heads) ("LLM inference and serving", Q7
+ *           "What are MQA and GQA"; consecutive grouping is this library's
+ *           reading of "each shared by H/H_kv query heads").
+ *
+ *  split    pao_decode_partitions / pao_combine_partitions restate the same
+ *           attention as per-partition (max, sum, unnormalised output)
+ *           triples merged by rescaling with exp(m_p - M), the rescale rule of
+ *           Q4's online softmax. They exist to pin the split-K identity.
+ *
+ * Layouts (row-major, element type = cache dtype):
+ *   q, out         [num_seqs][num_heads][head_dim]     (out is fp64 here)
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim]
+ *   k/v cache      [num_blocks][num_kv_heads][block_size][head_dim]
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs], counting the token appended this step
+ * dtype: 0 = fp32, 1 = bf16 (raw 16-bit patterns). Context length 0 gives a
+ * zero output row (a reading: the pages say nothing about empty sequences).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PAO_OK 0
+#define PAO_BAD_ARG (-1)
+#define PAO_BAD_BLOCK (-2)
+#define PAO_BAD_LEN (-3)
+#define PAO_NO_MEMORY (-4)
+
+static double load_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == 0) return (double)((const float*)base)[idx];
+    /* bf16: the 16 stored bits are the high half of an IEEE binary32. */
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static int elem_bytes_of(int dtype) { return dtype == 0 ? 4 : 2; }
+
+/* Copy every new K/V row into its slot. Negative slots are skipped (padding);
+ * a slot past the pool is skipped and counted. Returns that count. */
+int pao_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+               void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+               int head_dim, int block_size, int num_blocks, int dtype) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (dtype != 0 && dtype != 1))
+        return PAO_BAD_ARG;
+    const size_t row = (size_t)head_dim * (size_t)elem_bytes_of(dtype);
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    int bad = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) { ++bad; continue; }
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)t * num_kv_heads + h) * row;
+            const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * row;
+            memcpy((char*)k_cache + dst, (const char*)k_new + src, row);
+            memcpy((char*)v_cache + dst, (const char*)v_new + src, row);
+        }
+    }
+    return bad;
+}
+
+/* Rebuild the contiguous K and V rows 0..n-1 of (seq, kv_head) as fp64. */
+static int gather(const void* k_cache, const void* v_cache, const int32_t* table, int n,
+                  int kv_head, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, int dtype, double* Kc, double* Vc) {
+    for (int i = 0; i < n; ++i) {
+        const int32_t blk = table[i / block_size];
+        if (blk < 0 || blk >= num_blocks) return PAO_BAD_BLOCK;
+        const int off = i % block_size;
+        const size_t base =
+            (((size_t)blk * num_kv_heads + kv_head) * block_size + off) * (size_t)head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+            Kc[(size_t)i * head_dim + d] = load_elem(k_cache, base + d, dtype);
+            Vc[(size_t)i * head_dim + d] = load_elem(v_cache, base + d, dtype);
+        }
+    }
+    return PAO_OK;
+}
+
+/* Softmax weights of one query against n contiguous keys: w_i = exp(S_i - M) / Z. */
+static void softmax_weights(const double* qv, const double* Kc, int n, int head_dim,
+                            double scale, double* w) {
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d) dot += qv[d] * Kc[(size_t)i * head_dim + d];
+        w[i] = scale * dot;
+        if (w[i] > M) M = w[i];
+    }
+    double Z = 0.0;
+    for (int i = 0; i < n; ++i) {
+        w[i] = exp(w[i] - M);
+        Z += w[i];
+    }
+    for (int i = 0; i < n; ++i) w[i] /= Z;
+}
+
+static int check_shapes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                        int block_size, int num_blocks, int max_blocks_per_seq, int dtype) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
+        (dtype != 0 && dtype != 1) || num_heads % num_kv_heads != 0)
+        return PAO_BAD_ARG;
+    return PAO_OK;
+}
+
+/* Full decode attention. out: fp64 [num_seqs][num_heads][head_dim].
+ * num_threads <= 0 lets OpenMP (when compiled in) choose. */
+int pao_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, const int32_t* context_lens, double scale,
+               double* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, int max_blocks_per_seq, int dtype,
+               int num_threads) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, dtype);
+    if (rc != PAO_OK) return rc;
+    const int G = num_heads / num_kv_heads;
+    const int units = num_seqs * num_kv_heads;
+    int err = PAO_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#else
+    const int nt = 1;
+    (void)num_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int u = 0; u < units; ++u) {
+        const int s = u / num_kv_heads, h = u % num_kv_heads;
+        const int n = context_lens[s];
+        if (n < 0 || (long)n > (long)max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            err = PAO_BAD_LEN;
+            continue;
+        }
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* w = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!Kc || !Vc || !w || !qv) {
+#pragma omp atomic write
+            err = PAO_NO_MEMORY;
+            free(Kc); free(Vc); free(w); free(qv);
+            continue;
+        }
+        int grc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq, n, h,
+                         num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+        if (grc != PAO_OK) {
+#pragma omp atomic write
+            err = grc;
+        }
+        for (int g = 0; g < G; ++g) {
+            const int qh = h * G + g;
+            double* o = out + ((size_t)s * num_heads + qh) * head_dim;
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (n == 0 || grc != PAO_OK) continue;
+            for (int d = 0; d < head_dim; ++d)
+                qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);
+            softmax_weights(qv, Kc, n, head_dim, scale, w);
+            for (int i = 0; i < n; ++i)
+                for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
+        }
+        free(Kc); free(Vc); free(w); free(qv);
+    }
+    return err;
+}
+
+/* The normalised softmax weights of one (seq, query head): w[0..n-1]. */
+int pao_attention_weights(const void* q, const void* k_cache, const int32_t* block_tables,
+                          const int32_t* context_lens, double scale, int seq, int head,
+                          double* w, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, int dtype) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, dtype);
+    if (rc != PAO_OK) return rc;
+    if (seq < 0 || seq >= num_seqs || head < 0 || head >= num_heads) return PAO_BAD_ARG;
+    const int G = num_heads / num_kv_heads, h = head / G;
+    const int n = context_lens[seq];
+    if (n <= 0 || (long)n > (long)max_blocks_per_seq * block_size) return PAO_BAD_LEN;
+    double* Kc = (double*)malloc(sizeof(double) * (size_t)n * head_dim);
+    double* Vc = (double*)malloc(sizeof(double) * (size_t)n * head_dim);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    if (!Kc || !Vc || !qv) { free(Kc); free(Vc); free(qv); return PAO_NO_MEMORY; }
+    /* V is gathered along with K and ignored: one gather routine for both. */
+    rc = gather(k_cache, k_cache, block_tables + (size_t)seq * max_blocks_per_seq, n, h,
+                num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+    if (rc == PAO_OK) {
+        for (int d = 0; d < head_dim; ++d)
+            qv[d] = load_elem(q, ((size_t)seq * num_heads + head) * head_dim + d, dtype);
+        softmax_weights(qv, Kc, n, head_dim, scale, w);
+    }
+    free(Kc); free(Vc); free(qv);
+    return rc;
+}
+
+/* Per-partition state of the split form. Partition p of a sequence covers tokens
+ * [p*P, min(n, (p+1)*P)). For each (seq, head, p) it stores
+ *   m = max_i S_i,  l = sum_i exp(S_i - m),  o[d] = sum_i exp(S_i - m) V_i[d]
+ * into m/l [num_seqs][num_heads][max_parts] and o [..][max_parts][head_dim].
+ * Partitions past the sequence get m = -inf, l = 0, o = 0. */
+int pao_decode_partitions(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          double scale, int partition_size, int max_parts, double* m,
+                          double* l, double* o, int num_seqs, int num_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, int dtype) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, dtype);
+    if (rc != PAO_OK) return rc;
+    if (partition_size <= 0 || max_parts < 0) return PAO_BAD_ARG;
+    const int G = num_heads / num_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int n = context_lens[s];
+        if (n < 0 || (long)n > (long)max_blocks_per_seq * block_size) return PAO_BAD_LEN;
+        if ((long)n > (long)partition_size * max_parts) return PAO_BAD_ARG;
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        double* S = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        if (!Kc || !Vc || !qv || !S) { free(Kc); free(Vc); free(qv); free(S); return PAO_NO_MEMORY; }
+        for (int h = 0; h < num_kv_heads && rc == PAO_OK; ++h) {
+            rc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq, n, h,
+                        num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+            if (rc != PAO_OK) break;
+            for (int g = 0; g < G; ++g) {
+                const int qh = h * G + g;
+                for (int d = 0; d < head_dim; ++d)
+                    qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);
+                for (int i = 0; i < n; ++i) {
+                    double dot = 0.0;
+                    for (int d = 0; d < head_dim; ++d) dot += qv[d] * Kc[(size_t)i * head_dim + d];
+                    S[i] = scale * dot;
+                }
+                for (int p = 0; p < max_parts; ++p) {
+                    const size_t mi = ((size_t)s * num_heads + qh) * max_parts + p;
+                    double* op = o + mi * head_dim;
+                    double mp = -INFINITY, lp = 0.0;
+                    for (int d = 0; d < head_dim; ++d) op[d] = 0.0;
+                    const int lo = p * partition_size;
+                    const int hi = lo + partition_size < n ? lo + partition_size : n;
+                    for (int i = lo; i < hi; ++i)
+                        if (S[i] > mp) mp = S[i];
+                    for (int i = lo; i < hi; ++i) {
+                        const double e = exp(S[i] - mp);
+                        lp += e;
+                        for (int d = 0; d < head_dim; ++d) op[d] += e * Vc[(size_t)i * head_dim + d];
+                    }
+                    m[mi] = mp;
+                    l[mi] = lp;
+                }
+            }
+        }
+        free(Kc); free(Vc); free(qv); free(S);
+        if (rc != PAO_OK) return rc;
+    }
+    return PAO_OK;
+}
+
+/* Merge per-partition triples: M = max_p m_p, c_p = exp(m_p - M),
+ * out = (sum_p c_p o_p) / (sum_p c_p l_p). parts[s] partitions are used for
+ * sequence s; a sequence with none gets zeros. */
+int pao_combine_partitions(const double* m, const double* l, const double* o,
+                           const int32_t* parts, int max_parts, double* out, int num_seqs,
+                           int num_heads, int head_dim) {
+    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_parts < 0) return PAO_BAD_ARG;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (parts[s] < 0 || parts[s] > max_parts) return PAO_BAD_ARG;
+        for (int qh = 0; qh < num_heads; ++qh) {
+            const size_t base = ((size_t)s * num_heads + qh) * max_parts;
+            double* y = out + ((size_t)s * num_heads + qh) * head_dim;
+            for (int d = 0; d < head_dim; ++d) y[d] = 0.0;
+            if (parts[s] == 0) continue;
+            double M = -INFINITY;
+            for (int p = 0; p < parts[s]; ++p)
+                if (m[base + p] > M) M = m[base + p];
+            double L = 0.0;
+            for (int p = 0; p < parts[s]; ++p) {
+                const double c = exp(m[base + p] - M);
+                L += c * l[base + p];
+                for (int d = 0; d < head_dim; ++d) y[d] += c * o[(base + p) * head_dim + d];
+            }
+            for (int d = 0; d < head_dim; ++d) y[d] /= L;
+        }
+    }
+    return PAO_OK;
+}

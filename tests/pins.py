@@ -1,0 +1,331 @@
+"""Pins of the fp64 oracle: checks against facts the pages and the mathematics
+fix, not against the oracle itself. Each pin is a plain function that raises
+AssertionError on failure, so that test_oracle_pins.py runs them against the
+oracle and test_oracle_mutants.py runs them against copies of the oracle with a
+planted mistake (at least one pin must catch every such mistake).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import softmax
+
+import oracle
+from oracle import brute
+from paged_kv_cache_29_gb300 import workloads as wl
+from paged_kv_cache_29_gb300.block_manager import BlockManager
+
+
+def _f64(step, a):
+    return wl.as_f32(a, step.cache_dtype).astype(np.float64)
+
+
+def _after_append(step):
+    k = step.k_cache.copy()
+    v = step.v_cache.copy()
+    oracle.append(step.k_new, step.v_new, step.slot_mapping, k, v)
+    return k, v
+
+
+def _decode(step, k, v, **kw):
+    return oracle.decode(step.q, k, v, step.block_tables, step.context_lens, step.scale, **kw)
+
+
+def small_step(lens=(5, 17, 33, 64), hq=4, hkv=2, d=16, dtype="f32", bs=16, seed=11,
+               num_blocks=None):
+    return wl.build_step("pin", list(lens), hq, hkv, d, cache_dtype=dtype, block_size=bs,
+                         seed=seed, num_blocks=num_blocks)
+
+
+# ---- P1: an independent pure-Python implementation on tiny inputs ------------
+
+def pin_brute_force():
+    for dtype, hq, hkv, bs, d in [("f32", 4, 2, 16, 8), ("bf16", 6, 3, 4, 8),
+                                  ("f32", 2, 2, 1, 4), ("bf16", 8, 1, 16, 8)]:
+        step = small_step((1, 7, 16, 23), hq, hkv, d, dtype, bs, seed=3)
+        k, v = _after_append(step)
+        got = _decode(step, k, v)
+        kb, vb = _f64(step, step.k_cache).tolist(), _f64(step, step.v_cache).tolist()
+        brute.append(_f64(step, step.k_new).tolist(), _f64(step, step.v_new).tolist(),
+                     step.slot_mapping.tolist(), kb, vb, bs)
+        want = np.array(brute.decode(_f64(step, step.q).tolist(), kb, vb,
+                                     step.block_tables.tolist(), step.context_lens.tolist(),
+                                     step.scale, bs))
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+# ---- P2: paged == contiguous, the contiguous side through a library softmax --
+
+def pin_paged_equals_contiguous():
+    rng = np.random.default_rng(5)
+    hq, hkv, d, bs = 6, 2, 12, 4
+    G = hq // hkv
+    lens = [1, 4, 9, 30]
+    nb = 40
+    perm = rng.permutation(nb)
+    pool_k = rng.standard_normal((nb, hkv, bs, d))
+    pool_v = rng.standard_normal((nb, hkv, bs, d))
+    q = rng.standard_normal((len(lens), hq, d))
+    scale = 0.37
+    tables = np.full((len(lens), 8), -1, dtype=np.int32)
+    contig = []
+    nxt = 0
+    for s, n in enumerate(lens):
+        nblk = -(-n // bs)
+        tables[s, :nblk] = perm[nxt:nxt + nblk]
+        nxt += nblk
+        K = rng.standard_normal((n, hkv, d))
+        V = rng.standard_normal((n, hkv, d))
+        idx = np.arange(n)
+        pool_k[tables[s, idx // bs], :, idx % bs, :] = K     # scatter into the pool
+        pool_v[tables[s, idx // bs], :, idx % bs, :] = V
+        contig.append((K, V))
+    got = oracle.decode(q.astype(np.float32), pool_k.astype(np.float32),
+                        pool_v.astype(np.float32), tables, np.array(lens, np.int32), scale)
+    for s, (K, V) in enumerate(contig):
+        K32 = K.astype(np.float32).astype(np.float64)
+        V32 = V.astype(np.float32).astype(np.float64)
+        for qh in range(hq):
+            qv = q[s, qh].astype(np.float32).astype(np.float64)
+            w = softmax(scale * (K32[:, qh // G, :] @ qv))
+            np.testing.assert_allclose(got[s, qh], w @ V32[:, qh // G, :], rtol=0, atol=1e-12)
+
+
+# ---- P3: permuting physical blocks is invisible -------------------------------
+
+def pin_block_permutation():
+    step = small_step(dtype="bf16", seed=21)
+    k, v = _after_append(step)
+    base = _decode(step, k, v)
+    perm = np.random.default_rng(1).permutation(step.num_blocks)
+    k2, v2 = np.empty_like(k), np.empty_like(v)
+    k2[perm] = k
+    v2[perm] = v
+    bt2 = np.where(step.block_tables >= 0, perm[np.maximum(step.block_tables, 0)], -1)
+    got = oracle.decode(step.q, k2, v2, bt2.astype(np.int32), step.context_lens, step.scale)
+    assert np.array_equal(got, base), "block permutation changed the result"
+
+
+# ---- P4: block size 1 and 16 give the same result ----------------------------
+
+def pin_block_size_invariance():
+    step = small_step(dtype="f32", seed=8)
+    k, v = _after_append(step)
+    base = _decode(step, k, v)
+    bs = step.block_size
+    B = step.num_seqs
+    total = int(step.context_lens.sum())
+    order = np.random.default_rng(2).permutation(total + 3)
+    k1 = np.random.default_rng(3).standard_normal(
+        (total + 3, step.num_kv_heads, 1, step.head_dim)).astype(np.float32)
+    v1 = k1.copy()
+    bt1 = np.full((B, int(step.context_lens.max())), -1, dtype=np.int32)
+    nxt = 0
+    for s in range(B):
+        for i in range(int(step.context_lens[s])):
+            blk = order[nxt]
+            nxt += 1
+            src = step.block_tables[s, i // bs]
+            k1[blk, :, 0, :] = k[src, :, i % bs, :]
+            v1[blk, :, 0, :] = v[src, :, i % bs, :]
+            bt1[s, i] = blk
+    got = oracle.decode(step.q, k1, v1, bt1, step.context_lens, step.scale)
+    assert np.array_equal(got, base), "block size 1 and 16 disagree"
+
+
+# ---- P5: weights sum to one; the output is a convex combination ---------------
+
+def pin_softmax_weights_and_hull():
+    step = small_step(dtype="bf16", seed=4, hq=4, hkv=1)
+    k, v = _after_append(step)
+    out = _decode(step, k, v)
+    for s in range(step.num_seqs):
+        n = int(step.context_lens[s])
+        rows = np.array([_f64(step, v[step.block_tables[s, i // 16], 0, i % 16])
+                         for i in range(n)])
+        for qh in range(step.num_heads):
+            w = oracle.attention_weights(step.q, k, step.block_tables, step.context_lens,
+                                         step.scale, s, qh)
+            assert w.shape == (n,) and np.all(w >= 0)
+            assert abs(w.sum() - 1.0) < 1e-12
+            np.testing.assert_allclose(out[s, qh], w @ rows, rtol=0, atol=1e-12)
+            assert np.all(out[s, qh] <= rows.max(axis=0) + 1e-12)
+            assert np.all(out[s, qh] >= rows.min(axis=0) - 1e-12)
+
+
+# ---- P7: copy-on-write sharing gives the result of private copies ------------
+
+def pin_copy_on_write():
+    bs, hkv, hq, d = 16, 2, 4, 8
+    rng = np.random.default_rng(9)
+    nb = 24
+    mgr = BlockManager(nb, bs, free_order=rng.permutation(nb), prefix_caching=False)
+    mgr.admit("p", list(range(40)))              # last block holds 8 of 16 slots
+    mgr.fork("p", "c")
+    k = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    v = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    q = rng.standard_normal((2, hq, d)).astype(np.float32)
+
+    def tables():
+        t = [mgr.block_table("p"), mgr.block_table("c")]
+        out = np.full((2, 4), -1, np.int32)
+        for s, row in enumerate(t):
+            out[s, :len(row)] = row
+        return out
+
+    lens = np.array([40, 40], np.int32)
+    before = oracle.decode(q, k, v, tables(), lens, 0.3)
+    res_c = mgr.append("c", 99)                  # child writes into the shared block
+    assert res_c.copy_on_write is not None, "a shared partial block must be copied first"
+    src, dst = res_c.copy_on_write
+    k[dst], v[dst] = k[src], v[src]
+    new_k = rng.standard_normal((2, hkv, d)).astype(np.float32)
+    new_v = rng.standard_normal((2, hkv, d)).astype(np.float32)
+    oracle.append(new_k[1:], new_v[1:], np.array([res_c.slot], np.int64), k, v)
+    mid = oracle.decode(q, k, v, tables(), np.array([40, 41], np.int32), 0.3)
+    np.testing.assert_array_equal(mid[0], before[0])      # the parent never sees the write
+    res_p = mgr.append("p", 77)                  # now the parent appends its own token
+    assert res_p.copy_on_write is None and res_p.slot != res_c.slot
+    oracle.append(new_k[:1], new_v[:1], np.array([res_p.slot], np.int64), k, v)
+    lens2 = np.array([41, 41], np.int32)
+    shared = oracle.decode(q, k, v, tables(), lens2, 0.3)
+    # Same contents with every block private to its sequence.
+    t = tables()
+    kp = np.zeros((8, hkv, bs, d), np.float32)
+    vp = np.zeros_like(kp)
+    priv = np.full_like(t, -1)
+    nxt = 0
+    for s in range(2):
+        for j in range(-(-int(lens2[s]) // bs)):
+            kp[nxt], vp[nxt] = k[t[s, j]], v[t[s, j]]
+            priv[s, j] = nxt
+            nxt += 1
+    private = oracle.decode(q, kp, vp, priv, lens2, 0.3)
+    np.testing.assert_array_equal(private, shared)
+    # and the private layout holds each sequence's own new row
+    for s, slot_owner in ((0, new_k[0]), (1, new_k[1])):
+        blk = priv[s, 40 // bs]
+        np.testing.assert_array_equal(kp[blk, :, 40 % bs, :], slot_owner)
+
+
+# ---- P8: closed forms ---------------------------------------------------------
+
+def pin_closed_forms():
+    rng = np.random.default_rng(12)
+    hkv, hq, d, bs = 2, 4, 16, 16
+    nb = 8
+    k = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    v = rng.standard_normal((nb, hkv, bs, d)).astype(np.float32)
+    q = rng.standard_normal((4, hq, d)).astype(np.float32)
+    bt = np.array([[3, -1], [5, 1], [6, 2], [7, 4]], np.int32)
+    # one row: the output is that V row exactly
+    out = oracle.decode(q, k, v, bt, np.array([1, 0, 0, 0], np.int32), 0.125)
+    assert np.array_equal(out[0], v[3, np.arange(hq) // 2, 0, :].astype(np.float64))
+    assert np.all(out[1:] == 0.0), "empty sequences give zero rows"
+    # equal keys: uniform weights, the output is the mean of the V rows
+    k2 = k.copy()
+    k2[5] = k2[5, :, :1, :]
+    k2[1] = k2[5, :, :1, :]
+    out = oracle.decode(q, k2, v, bt, np.array([0, 20, 0, 0], np.int32), 0.125)
+    rows = np.concatenate([v[5], v[1, :, :4]], axis=1).astype(np.float64)   # [hkv][20][d]
+    for qh in range(hq):
+        np.testing.assert_allclose(out[1, qh], rows[qh // 2].mean(axis=0), rtol=0, atol=1e-12)
+    # q = 0: uniform weights as well
+    out = oracle.decode(np.zeros_like(q), k, v, bt, np.array([0, 0, 29, 0], np.int32), 0.125)
+    rows = np.concatenate([v[6], v[2, :, :13]], axis=1).astype(np.float64)
+    for qh in range(hq):
+        np.testing.assert_allclose(out[2, qh], rows[qh // 2].mean(axis=0), rtol=0, atol=1e-12)
+    # one key far ahead of the rest: the output is that key's V row. Both query
+    # heads of a group get the same q so that one key can lead for both.
+    q3 = q.copy()
+    q3[3, 1], q3[3, 3] = q3[3, 0], q3[3, 2]
+    k3 = k.copy()
+    for h in range(hkv):
+        k3[4, h, 9, :] = 1000.0 * np.sign(q3[3, 2 * h])
+    out = oracle.decode(q3, k3, v, bt, np.array([0, 0, 0, 26], np.int32), 1.0)
+    for qh in range(hq):
+        np.testing.assert_array_equal(out[3, qh], v[4, qh // 2, 9].astype(np.float64))
+
+
+# ---- P9: the split form merges back to the single pass ------------------------
+
+def pin_split_invariance():
+    step = small_step((1, 16, 17, 100, 257), hq=4, hkv=2, d=16, dtype="bf16", seed=31)
+    k, v = _after_append(step)
+    base = _decode(step, k, v)
+    for P in (1, 2, 3, 7, 16, 64, 512):
+        m, l, o, parts = oracle.decode_partitions(step.q, k, v, step.block_tables,
+                                                  step.context_lens, step.scale, P)
+        got = oracle.combine_partitions(m, l, o, parts)
+        np.testing.assert_allclose(got, base, rtol=0, atol=1e-12)
+        assert np.all(parts == -(-step.context_lens // P))
+
+
+# ---- GQA: G query heads on one KV head == the same KV head repeated G times ----
+
+def pin_gqa_grouping():
+    step = small_step(hq=8, hkv=2, d=8, dtype="f32", seed=17)
+    k, v = _after_append(step)
+    grouped = _decode(step, k, v)
+    G = step.num_heads // step.num_kv_heads
+    k_rep = np.repeat(k, G, axis=1)              # KV head h -> query heads h*G .. h*G+G-1
+    v_rep = np.repeat(v, G, axis=1)
+    mha = oracle.decode(step.q, k_rep, v_rep, step.block_tables, step.context_lens,
+                        step.scale)
+    assert np.array_equal(grouped, mha)
+
+
+# ---- append: bit copy into the slot, checked by numpy fancy indexing ----------
+
+def pin_append_slots():
+    step = small_step(dtype="bf16", d=8, seed=6, bs=4)
+    slots = step.slot_mapping.copy()
+    slots[1] = -1                                 # padding token: skipped
+    k, v = step.k_cache.copy(), step.v_cache.copy()
+    bad = oracle.append(step.k_new, step.v_new, slots, k, v)
+    assert bad == 0
+    ek, ev = step.k_cache.copy(), step.v_cache.copy()
+    for t, slot in enumerate(slots):
+        if slot >= 0:
+            ek[slot // 4, :, slot % 4, :] = step.k_new[t]
+            ev[slot // 4, :, slot % 4, :] = step.v_new[t]
+    assert np.array_equal(k, ek) and np.array_equal(v, ev)
+    over = np.array([step.num_blocks * 4, 0], np.int64)
+    assert oracle.append(step.k_new[:2], step.v_new[:2], over, k, v) == 1
+
+
+# ---- incremental decoding: the cache grows by one row a step ------------------
+
+def pin_incremental_decoder():
+    rng = np.random.default_rng(40)
+    d, bs, nb = 16, 4, 8
+    mgr = BlockManager(nb, bs, free_order=rng.permutation(nb), prefix_caching=False)
+    prompt = 4
+    k = np.zeros((nb, 1, bs, d), np.float32)
+    v = np.zeros_like(k)
+    rows_k, rows_v = [], []
+    mgr.admit("s", [])
+    for step in range(prompt + 6):
+        kn = rng.standard_normal((1, 1, d)).astype(np.float32)
+        vn = rng.standard_normal((1, 1, d)).astype(np.float32)
+        res = mgr.append("s", step)
+        oracle.append(kn, vn, np.array([res.slot], np.int64), k, v)
+        rows_k.append(kn[0, 0].astype(np.float64))
+        rows_v.append(vn[0, 0].astype(np.float64))
+        n = mgr.num_tokens("s")
+        assert n == step + 1
+        qv = rng.standard_normal((1, 1, d)).astype(np.float32)
+        bt = np.full((1, 3), -1, np.int32)
+        table = mgr.block_table("s")
+        bt[0, :len(table)] = table
+        out = oracle.decode(qv, k, v, bt, np.array([n], np.int32), 1 / math.sqrt(d))
+        w = softmax(np.array(rows_k) @ qv[0, 0].astype(np.float64) / math.sqrt(d))
+        np.testing.assert_allclose(out[0, 0], w @ np.array(rows_v), rtol=0, atol=1e-12)
+    assert mgr.num_tokens("s") == 10 == prompt + 6
+
+
+ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
+            pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
+            pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
+            pin_incremental_decoder]
