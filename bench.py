@@ -1,0 +1,494 @@
+"""Benchmark of one paged-attention decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b_gqa]
+                    [--kernel auto|mma|simt|generic] [--impl native|reference]
+
+A step is the whole hot path over one batch: pa_reshape_and_cache (append the
+new K/V rows) then pa_decode (attention through the block tables, with the
+split-K merge when a sequence spans several 512-row partitions). Inputs are
+the seeded synthetic workloads of paged_kv_cache_29_gb300.workloads, resident
+in HBM before timing. Between timed steps a 256 MiB buffer is written to flush
+L2 (the attended K/V bytes are also larger than L2). Timing uses CUDA events on
+the launching stream; clocks are sampled with nvidia-smi during the timed
+region.
+
+One JSON line is printed by rank 0. `value` is the step's algorithmic bytes
+(K/V rows attended, q read, out written, block-table entries and context
+lengths used, the append's reads and writes) over the step time, in GB/s.
+`roofline` covers the attention call (decode + merge kernels) against the
+measured HBM copy bandwidth. `e2e` repeats the measurement through the same
+public API with the step's per-step inputs copied from pinned host memory and
+the output copied back inside the timed region (the KV pool stays resident:
+it is the cache). `cpu_baseline` times the fp64 oracle on a bounded sample of
+the same workload on the host's cores.
+
+--impl reference times the oracle itself (the CPU baseline) in the same JSON
+format. Under torchrun every rank runs its own batch (weak scaling, no
+collective on the data path); only the barrier and the max-over-ranks of the
+timings cross ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_29_gb300 import accounting  # noqa: E402
+from paged_kv_cache_29_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention: achieved KV GB/s (% of GB300 HBM peak) and seqs/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_8b_gqa_ncu.md")
+CSRC = os.path.join(ROOT, "paged_kv_cache_29_gb300", "csrc")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_hbm_gbs() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, kernel: str) -> float | None:
+    """DRAM bytes per launch of the attention call from the committed ncu
+    summary, if it was taken on the current kernel sources and this workload."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for line in lines:
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    if vals.get("workload") != workload or vals.get("kernel") != kernel:
+        return None
+    try:
+        return float(vals["dram_bytes_per_call"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the oracle as it stands, on a bounded sample)
+# ---------------------------------------------------------------------------
+
+def sample_step(step: wl.DecodeStep, seqs: list[int]) -> wl.DecodeStep:
+    idx = np.array(seqs, dtype=np.int64)
+    return wl.DecodeStep(**{**step.__dict__, "q": step.q[idx], "k_new": step.k_new[idx],
+                            "v_new": step.v_new[idx], "slot_mapping": step.slot_mapping[idx],
+                            "block_tables": step.block_tables[idx],
+                            "context_lens": step.context_lens[idx]})
+
+
+def oracle_sample_plan(step: wl.DecodeStep, target_s: float, threads: int):
+    """Pick a sample of sequences that keeps the oracle busy about target_s
+    seconds; the rate is probed on one short sequence first."""
+    import oracle
+    order = list(np.argsort(step.context_lens, kind="stable"))
+    probe = sample_step(step, [order[len(order) // 2]])
+    t0 = time.perf_counter()
+    oracle.decode(probe.q, step.k_cache, step.v_cache, probe.block_tables, probe.context_lens,
+                  step.scale, num_threads=1)
+    per_token = (time.perf_counter() - t0) / max(int(probe.context_lens.sum()), 1)
+    budget_tokens = target_s * max(threads, 1) / max(per_token, 1e-12)
+    chosen, tokens = [], 0
+    rng = np.random.default_rng(123)
+    for s in rng.permutation(step.num_seqs):
+        n = int(step.context_lens[s])
+        if chosen and tokens + n > budget_tokens:
+            continue
+        chosen.append(int(s))
+        tokens += n
+        if tokens >= budget_tokens:
+            break
+    return sorted(chosen)
+
+
+def time_oracle(step: wl.DecodeStep, seqs: list[int], threads: int) -> tuple[float, int]:
+    """Seconds for one oracle decode over the sampled sequences, and its bytes."""
+    import oracle
+    sub = sample_step(step, seqs)
+    t0 = time.perf_counter()
+    oracle.decode(sub.q, step.k_cache, step.v_cache, sub.block_tables, sub.context_lens,
+                  step.scale, num_threads=threads)
+    dt = time.perf_counter() - t0
+    b = accounting.step_bytes(sub.context_lens, step.num_heads, step.num_kv_heads,
+                              step.head_dim, step.elem_bytes, step.block_size)
+    return dt, b.decode
+
+
+def cpu_baseline(step: wl.DecodeStep, target_s: float = 12.0) -> dict:
+    """The oracle over a bounded sample, repeated until about target_s seconds
+    of host time have passed; reports the mean rate."""
+    threads = os.cpu_count() or 1
+    seqs = oracle_sample_plan(step, target_s, threads)
+    total_s, total_bytes, reps = 0.0, 0, 0
+    while reps == 0 or (total_s < target_s and reps < 1000):
+        dt, nbytes = time_oracle(step, seqs, threads)
+        total_s += dt
+        total_bytes += nbytes
+        reps += 1
+    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"fp64 C oracle (OpenMP, {threads} threads) attention over {len(seqs)} of "
+                       f"{step.num_seqs} sequences ({int(step.context_lens[seqs].sum())} of "
+                       f"{int(step.context_lens.sum())} rows) of {step.name}, {reps} passes in "
+                       f"{total_s:.1f} s; GB/s of the sample's algorithmic attention bytes"),
+            "seconds": round(total_s, 3)}
+
+
+# ---------------------------------------------------------------------------
+# the native (CUDA) arm
+# ---------------------------------------------------------------------------
+
+def run_native(args) -> dict | None:
+    import torch
+    import paged_kv_cache_29_gb300 as pa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    step = wl.make(args.workload, seed=wl.WORKLOAD_SEEDS[args.workload] + 1000 * rank)
+    bytes_ = accounting.step_bytes_for(step)
+    cd = step.cache_dtype
+
+    def up(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if cd == "bf16" and a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    q, k_new, v_new = up(step.q), up(step.k_new), up(step.v_new)
+    k_cache, v_cache = up(step.k_cache), up(step.v_cache)
+    slots, tables, lens = up(step.slot_mapping), up(step.block_tables), up(step.context_lens)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    mcl = step.max_context_len
+    ws_bytes = pa.pa_decode_workspace_size(step.num_seqs, step.num_heads, step.head_dim, mcl)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
+
+    def do_step():
+        pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
+                                stream=stream)
+        pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                     workspace=workspace, error_word=err, stream=stream, kernel=args.kernel)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        do_step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(K):
+            flush.fill_(i & 0xff)
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
+                                    stream=stream)
+            e1.record(stream)
+            pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                         workspace=workspace, error_word=err, stream=stream, kernel=args.kernel)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
+    append_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    total_ms = sum(step_ms)
+    decode_avg = sum(decode_ms) / K
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
+
+    # ---- end to end through the public API with host buffers --------------
+    pin = {name: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+           for name, a in (("q", step.q), ("k_new", step.k_new), ("v_new", step.v_new),
+                           ("slots", step.slot_mapping), ("tables", step.block_tables),
+                           ("lens", step.context_lens))}
+    if cd == "bf16":
+        for name in ("q", "k_new", "v_new"):
+            pin[name] = pin[name].view(torch.bfloat16)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dsts = {"q": q, "k_new": k_new, "v_new": v_new, "slots": slots, "tables": tables,
+            "lens": lens}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for name, t in pin.items():
+            dsts[name].copy_(t, non_blocking=True)
+        do_step()
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, e2e_total, decode_avg], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total, decode_avg = t.tolist()
+        nb = torch.tensor([float(bytes_.total), float(step.num_seqs)], device=dev,
+                          dtype=torch.float64)
+        dist.all_reduce(nb)
+        all_bytes, all_seqs = nb.tolist()
+    else:
+        all_bytes, all_seqs = float(bytes_.total), float(step.num_seqs)
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_hbm_gbs()
+    ms_per_step = total_ms / K
+    value = all_bytes / (ms_per_step * 1e-3) / 1e9
+    decode_gbs = bytes_.decode / (decode_avg * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload, args.kernel)
+    kernel_name = {"auto": "auto", "mma": "mma", "simt": "simt", "generic": "generic"}[args.kernel]
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cd,
+        "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
+        "config": {
+            "workload": args.workload,
+            "num_seqs": step.num_seqs, "num_heads": step.num_heads,
+            "num_kv_heads": step.num_kv_heads, "head_dim": step.head_dim,
+            "block_size": step.block_size, "cache_dtype": cd,
+            "total_context_rows": int(step.context_lens.sum()),
+            "max_context_len": mcl, "partition_size": 512, "kernel": kernel_name,
+            "l2": "256 MiB buffer written between timed steps; attended K/V also exceed L2",
+            "parallelism": f"replicas x{world} (independent batches per GPU)",
+        },
+        "seqs_per_s": round(all_seqs / (ms_per_step * 1e-3), 1),
+        "kv_gbs": round(bytes_.kv * world / (ms_per_step * 1e-3) / 1e9, 2),
+        "pct_of_measured_hbm": round(100 * value / peak / world, 2),
+        "pct_of_nominal_8tbs": round(100 * value / NOMINAL_HBM_GBS / world, 2),
+        "step_breakdown_ms": {"append": round(sum(append_ms) / K, 5),
+                              "decode_call": round(decode_avg, 5)},
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode call (decode_tma_kernel + combine_kernel)",
+            "achieved": round(decode_gbs, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(decode_gbs / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_call": bytes_.decode,
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+        },
+        "e2e": {
+            "value": round(all_bytes / (e2e_total / K * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_total / K, 5),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if step.meta.get("unique_blocks") and bytes_.kv_unique != bytes_.kv:
+        res["kv_unique_gbs"] = round(bytes_.kv_unique / (ms_per_step * 1e-3) / 1e9, 2)
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(step, args.cpu_seconds)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the oracle, timed as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args) -> dict | None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    step = wl.make(args.workload)
+    threads = os.cpu_count() or 1
+    per_step_s = max(1.0, min(args.cpu_seconds, 120.0 / max(args.steps + args.warmup, 1)))
+    seqs = oracle_sample_plan(step, per_step_s, threads)
+    for _ in range(args.warmup):
+        time_oracle(step, seqs, threads)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = time_oracle(step, seqs, threads)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"fp64 C oracle (OpenMP, {threads} threads) attention over {len(seqs)} of "
+              f"{step.num_seqs} sequences ({int(step.context_lens[seqs].sum())} rows) of "
+              f"{step.name} per step")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
+        "config": {"workload": args.workload, "num_seqs": len(seqs),
+                   "sampled_from": step.num_seqs, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description="paged decode attention benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="8b_gqa", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt", "generic"])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target oracle time of the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, _, _ = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    res = run_reference(args) if args.impl == "reference" else run_native(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "native":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

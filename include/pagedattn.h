@@ -1,0 +1,165 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode library.
+ *
+ * One decode step of paged attention is two calls on one CUDA stream:
+ *
+ *   pa_reshape_and_cache  writes each sequence's new K and V row into its slot
+ *                         of the paged pool (the cache append of the naive
+ *                         incremental decoder in "LLM inference and serving",
+ *                         "Code from memory");
+ *   pa_decode             single-query attention for every sequence, reading K
+ *                         and V through the sequence's block table
+ *                         ("MLSys Engineer -- Inference Systems Q&A", Q1 "How
+ *                         does PagedAttention work?": row i of a sequence is
+ *                         row i % block_size of physical block
+ *                         block_table[i / block_size]).
+ *
+ * Data layouts (row-major; "T" is the cache dtype, fp32 or bf16):
+ *   k_cache, v_cache  T [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k_new, v_new      T [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping      int64 [num_tokens]; slot = block * block_size + offset,
+ *                     a negative slot means "no append for this token"
+ *   q, out            T [num_seqs][num_heads][head_dim]
+ *   block_tables      int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                     ceil(context_len / block_size) are never read
+ *   context_lens      int32 [num_seqs]; the number of rows attended, counting
+ *                     the row appended this step (0 gives a zero output row)
+ * Query head qh uses KV head qh / (num_heads / num_kv_heads): consecutive
+ * groups of query heads share one KV head ("LLM inference and serving", Q7
+ * "What are MQA and GQA").
+ *
+ * Ownership and synchronisation: every pointer is a device pointer owned by
+ * the caller. The library allocates no memory and keeps no state between
+ * calls beyond cached driver entry points and kernel attributes. Calls only
+ * enqueue work on `stream` (NULL = legacy default stream) and return without
+ * waiting for it.
+ *
+ * Errors: invalid arguments are rejected on the host before anything is
+ * enqueued, with a pa_status and no side effects. Problems only visible on
+ * the device (a block-table entry outside the pool, a slot past the pool, a
+ * context length past the block table, a wait that hit its time limit) are
+ * OR-ed into *error_word (an int32 in device memory, may be NULL) as
+ * PA_DEVERR_* bits; the affected sequence or token is skipped and nothing
+ * outside the caller's buffers is touched. The kernels never trap.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer, ... */
+    PA_ERR_UNSUPPORTED = 2,  /* a valid shape this build has no kernel for */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
+    PA_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_DEVICE_BOUNDS = 5 /* returned by pa_check_error_word: PA_DEVERR_* set */
+} pa_status;
+
+typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 } pa_dtype;
+
+/* Bits the kernels OR into *error_word. */
+#define PA_DEVERR_BLOCK_ID 0x1  /* a block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT 0x2      /* a slot >= num_blocks * block_size */
+#define PA_DEVERR_CONTEXT 0x4   /* context_len < 0, or > max_context_len, or past the table */
+#define PA_DEVERR_TIMEOUT 0x8   /* a shared-memory barrier wait gave up after its limit */
+
+/*
+ * Append one K and one V row per token into the paged pool:
+ *   k_cache[s / bs][h][s % bs][:] = k_new[t][h][:]   (same for V), s = slot_mapping[t]
+ * for every t with s >= 0 and every KV head h. A bit copy: no rounding.
+ * Tokens with s >= num_blocks * block_size are skipped and flagged
+ * PA_DEVERR_SLOT. Two tokens with the same slot race (last writer wins).
+ * head_dim * sizeof(T) must be a multiple of 16 and every buffer 16-byte
+ * aligned. Returns PA_OK or an error; never blocks.
+ */
+pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               int num_tokens, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, pa_dtype dtype,
+                               int32_t* error_word, struct CUstream_st* stream);
+
+/*
+ * Decode attention for num_seqs sequences:
+ *   out[s][qh][:] = sum_i softmax_i(scale * <q[s][qh], K_i>) * V_i[:]
+ * over the context_lens[s] rows of sequence s (K_i, V_i gathered through
+ * block_tables[s]), accumulated in fp32, stored in the cache dtype with
+ * round-to-nearest-even.
+ *
+ * Long sequences are split into fixed partitions of 512 rows whose partial
+ * results (running max, sum and unnormalised output, the online-softmax state
+ * of Q4 "How would you write a fused attention kernel?") are merged by a
+ * second kernel. Partition boundaries depend only on the sequence's own
+ * length, so a sequence's result does not depend on the rest of the batch.
+ *
+ * max_context_len: an upper bound on every context_lens[s] (sizes the grid
+ *   and the workspace); must not exceed max_blocks_per_seq * block_size.
+ * workspace: device scratch of at least
+ *   pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len)
+ *   bytes, 16-byte aligned; may be NULL when that size is 0 (every sequence
+ *   fits one partition). Its contents on entry do not matter.
+ * Supported: fp32 and bf16; any block_size >= 1; head_dim 1..256; any
+ * num_heads that is a multiple of num_kv_heads. The fastest kernels need
+ * block_size a multiple of 16, head_dim 64 or 128 and at most 8 query heads
+ * per KV head; other shapes run a plain kernel that loads through the block
+ * table directly.
+ */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int max_blocks_per_seq,
+                    int max_context_len, pa_dtype dtype, void* workspace,
+                    size_t workspace_bytes, int32_t* error_word, struct CUstream_st* stream);
+
+/* Bytes of workspace pa_decode needs for these sizes (0 if no sequence can
+ * span more than one partition). */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+/* Kernel choice for pa_decode_ex (for measurement and tests; pa_decode uses
+ * PA_KERNEL_AUTO). PA_KERNEL_MMA needs bf16. */
+typedef enum pa_kernel {
+    PA_KERNEL_AUTO = 0,
+    PA_KERNEL_SIMT = 1,    /* TMA tile ring, CUDA-core dot products */
+    PA_KERNEL_MMA = 2,     /* TMA tile ring, per-tile bf16 tensor-core MMA */
+    PA_KERNEL_GENERIC = 3  /* direct loads through the block table */
+} pa_kernel;
+
+typedef struct pa_decode_options {
+    int kernel;          /* a pa_kernel value */
+    int partition_size;  /* rows per split-K partition: a multiple of 16, 16..4096; 0 = 512 */
+} pa_decode_options;
+
+/* pa_decode with explicit options (NULL = defaults). The workspace must be
+ * sized with pa_decode_workspace_size_ex for the same partition size. */
+pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, float scale,
+                       void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_seq,
+                       int max_context_len, pa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, int32_t* error_word,
+                       const pa_decode_options* options, struct CUstream_st* stream);
+
+size_t pa_decode_workspace_size_ex(int num_seqs, int num_heads, int head_dim,
+                                   int max_context_len, int partition_size);
+
+/* Human-readable name of a status. Never NULL. */
+const char* pa_status_string(pa_status status);
+
+/* PA_OK if error_word (host copy) is 0, else PA_ERR_DEVICE_BOUNDS. */
+pa_status pa_check_error_word(int32_t error_word_value);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

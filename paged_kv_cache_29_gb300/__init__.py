@@ -3,5 +3,23 @@
 The compute path is a C-ABI CUDA library (``include/pagedattn.h``) built for
 sm_103a; this package holds its thin Python binding plus the host-side pieces
 that feed it: the block manager, byte accounting and the seeded workloads.
+
+    from paged_kv_cache_29_gb300 import pa_reshape_and_cache, pa_decode
 """
-__all__ = ["block_manager", "workloads", "accounting"]
+from ._binding import (  # noqa: F401
+    KERNELS,
+    PA_DEVERR_BLOCK_ID,
+    PA_DEVERR_CONTEXT,
+    PA_DEVERR_SLOT,
+    PA_DEVERR_TIMEOUT,
+    PagedAttentionError,
+    pa_decode,
+    pa_decode_workspace_size,
+    pa_reshape_and_cache,
+    pa_status_string,
+    pa_version,
+)
+
+__all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size", "pa_status_string",
+           "pa_version", "PagedAttentionError", "KERNELS", "block_manager", "workloads",
+           "accounting"]

@@ -1,0 +1,198 @@
+"""ctypes binding of libpagedattn.so (include/pagedattn.h).
+
+Argument marshalling only: every function takes torch tensors (or plain
+integers), checks that they are CUDA tensors of the expected dtype and shape,
+passes their device pointers and the current torch stream to the C entry point
+of the same name, and raises PagedAttentionError on a non-OK status. There is
+no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpagedattn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "pagedattn.h")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_WORKSPACE = 3
+PA_ERR_CUDA = 4
+PA_ERR_DEVICE_BOUNDS = 5
+
+PA_DEVERR_BLOCK_ID = 0x1
+PA_DEVERR_SLOT = 0x2
+PA_DEVERR_CONTEXT = 0x4
+PA_DEVERR_TIMEOUT = 0x8
+
+KERNELS = {"auto": 0, "simt": 1, "mma": 2, "generic": 3}
+DEFAULT_PARTITION = 512
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {pa_status_string(status)} (status {status})")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("partition_size", ctypes.c_int)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_29_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+        L.pa_reshape_and_cache.restype = I
+        L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
+        L.pa_decode.restype = I
+        L.pa_decode_ex.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
+                                   ctypes.POINTER(_Options), P]
+        L.pa_decode_ex.restype = I
+        L.pa_decode_workspace_size.argtypes = [I, I, I, I]
+        L.pa_decode_workspace_size.restype = S
+        L.pa_decode_workspace_size_ex.argtypes = [I, I, I, I, I]
+        L.pa_decode_workspace_size_ex.restype = S
+        L.pa_status_string.argtypes = [I]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_check_error_word.argtypes = [ctypes.c_int32]
+        L.pa_check_error_word.restype = I
+        L.pa_version.argtypes = []
+        L.pa_version.restype = I
+        _lib = L
+        return L
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/pagedattn.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def pa_status_string(status: int) -> str:
+    try:
+        return lib().pa_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def pa_version() -> int:
+    return lib().pa_version()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"cache dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check_cuda(name, t, dtype=None, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+
+
+def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, error_word=None,
+                         stream=None) -> None:
+    """Append new K/V rows ([T][Hkv][D]) into their slots of the paged pools
+    ([NB][Hkv][bs][D]). slot_mapping: int64 [T], negative = skip."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("k_new", k_new, k_cache.dtype, 3)
+    _check_cuda("v_new", v_new, k_cache.dtype, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != (nb, hkv, bs, d) or tuple(k_new.shape[1:]) != (hkv, d) \
+            or k_new.shape != v_new.shape or slot_mapping.shape[0] != k_new.shape[0]:
+        raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    rc = lib().pa_reshape_and_cache(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                    _ptr(k_cache), _ptr(v_cache), int(k_new.shape[0]), hkv, d,
+                                    bs, nb, _dtype_code(k_cache), _ptr(error_word),
+                                    _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_reshape_and_cache")
+
+
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
+                             max_context_len: int, partition_size: int = 0) -> int:
+    return int(lib().pa_decode_workspace_size_ex(num_seqs, num_heads, head_dim,
+                                                 max_context_len, partition_size))
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
+              workspace=None, error_word=None, stream=None, kernel: str = "auto",
+              partition_size: int = 0) -> None:
+    """Decode attention for every sequence, written into ``out`` ([B][Hq][D]).
+
+    max_context_len bounds context_lens (host value; sizes grid and workspace).
+    workspace: a CUDA tensor of at least pa_decode_workspace_size(...) bytes,
+    required when max_context_len exceeds one partition."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("q", q, k_cache.dtype, 3)
+    _check_cuda("out", out, k_cache.dtype, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    ws_bytes = 0
+    if workspace is not None:
+        _check_cuda("workspace", workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    opts = _Options(KERNELS[kernel], int(partition_size))
+    rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d, bs, nb,
+                            int(block_tables.shape[1]), int(max_context_len),
+                            _dtype_code(k_cache), _ptr(workspace), ws_bytes, _ptr(error_word),
+                            ctypes.byref(opts), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_decode")

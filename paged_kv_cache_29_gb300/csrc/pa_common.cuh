@@ -1,0 +1,148 @@
+// pa_common.cuh -- small device helpers shared by the paged-attention kernels:
+// mbarrier and TMA wrappers written as inline PTX for sm_103a, bounded waits,
+// the device error word, and bf16 packing.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// ---- device error word ------------------------------------------------------
+__device__ __forceinline__ void raise_error(int32_t* error_word, uint32_t bits) {
+    if (error_word != nullptr) atomicOr(reinterpret_cast<unsigned int*>(error_word), bits);
+}
+
+// ---- shared-memory addresses ------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the phase with the given parity has completed. Gives up after
+// kWaitLimitNs of wall time (or an iteration cap, whichever comes first) and
+// returns false; the caller records PA_DEVERR_TIMEOUT and winds down. A copy
+// that was issued always lands long before either limit.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kWaitMaxIters = 1u << 26;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < kWaitMaxIters; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// ---- TMA --------------------------------------------------------------------
+// 2D tiled bulk-tensor load global -> shared, completion counted in bytes on
+// an mbarrier. x (innermost coordinate, elements) must be 16-byte aligned.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// Named barrier among `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---- numeric helpers -----------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <typename T>
+struct ElemTraits;
+
+template <>
+struct ElemTraits<float> {
+    static constexpr int kBytes = 4;
+    static constexpr int kPerChunk = 4;   // elements per 16-byte chunk
+    __device__ static __forceinline__ void unpack(const uint4& c, float* f) {
+        f[0] = __uint_as_float(c.x);
+        f[1] = __uint_as_float(c.y);
+        f[2] = __uint_as_float(c.z);
+        f[3] = __uint_as_float(c.w);
+    }
+    __device__ static __forceinline__ float load(const float* p) { return *p; }
+    __device__ static __forceinline__ void store(float* p, float v) { *p = v; }
+};
+
+template <>
+struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kPerChunk = 8;
+    __device__ static __forceinline__ void unpack(const uint4& c, float* f) {
+        f[0] = bf16_lo(c.x); f[1] = bf16_hi(c.x);
+        f[2] = bf16_lo(c.y); f[3] = bf16_hi(c.y);
+        f[4] = bf16_lo(c.z); f[5] = bf16_hi(c.z);
+        f[6] = bf16_lo(c.w); f[7] = bf16_hi(c.w);
+    }
+    __device__ static __forceinline__ float load(const __nv_bfloat16* p) {
+        return __bfloat162float(*p);
+    }
+    __device__ static __forceinline__ void store(__nv_bfloat16* p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+}  // namespace pa

@@ -1,0 +1,258 @@
+// pa_decode_generic.cu -- the plain decode kernel (any block size, head dim up
+// to 256, any group size) and the split-K combine kernel.
+//
+// Generic kernel: one CTA per (sequence, KV head, partition). It reads the
+// partition's rows straight from the pool through the block table (row i is
+// row i % block_size of block block_tables[s][i / block_size], "MLSys
+// Engineer -- Inference Systems Q&A", Q1), computes all scores of the
+// partition into shared memory, takes the softmax over them in base 2 and
+// accumulates P.V in fp32. It exists for shapes the tile-ring kernels do not
+// cover (block sizes that are not a multiple of 16, other head dims); it is
+// not tuned.
+//
+// Combine kernel: for a sequence split into partitions p = 0..P-1 with states
+// (m_p, l_p, o_p) -- running max (base 2), sum of exp2(s - m_p), unnormalised
+// output -- the result is sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with
+// M = max_p m_p: the rescale rule of the online softmax in Q4 "How would you
+// write a fused attention kernel?", applied once per partition, in ascending
+// partition order.
+#include <cfloat>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kGenericThreads = 128;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kGenericThreads)
+decode_generic_kernel(const DecodeParams p, int group) {
+    using E = ElemTraits<T>;
+    extern __shared__ float sm[];
+    const int D = p.head_dim;
+    const int P = p.partition_size;
+    float* qf = sm;                           // [group][D]
+    float* sc = qf + group * D;               // [group][P]
+    float* red = sc + group * P;              // [group][2]: max, sum
+    int32_t* ids = reinterpret_cast<int32_t*>(red + 2 * group);   // partition's block ids
+    __shared__ int bad;
+
+    const int bh = p.num_seqs * p.num_kv_heads;
+    const int part = blockIdx.x / bh;
+    const int rem = blockIdx.x - part * bh;
+    const int s = rem / p.num_kv_heads;
+    const int h = rem - s * p.num_kv_heads;
+    const int n = __ldg(p.context_lens + s);
+    if (n < 0 || n > p.context_cap) {
+        if (threadIdx.x == 0 && part == 0 && h == 0) raise_error(p.error_word, PA_DEVERR_CONTEXT);
+        return;
+    }
+    const int lo = part * P;
+    const size_t row0 = static_cast<size_t>(s) * p.num_heads + static_cast<size_t>(h) * group;
+    if (n == 0) {
+        if (part == 0)
+            for (int i = threadIdx.x; i < group * D; i += blockDim.x)
+                E::store(static_cast<T*>(p.out) + row0 * D + i, 0.f);
+        return;
+    }
+    if (lo >= n) return;
+    const int hi = min(n, lo + P);
+    const int len = hi - lo;
+    const int nparts = (n + P - 1) / P;
+    const int bs = p.block_size;
+    const int b0 = lo / bs;
+    const int nblk = (hi - 1) / bs - b0 + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+        const int id = __ldg(p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq + b0 + j);
+        if (id < 0 || id >= p.num_blocks) bad = 1;
+        ids[j] = id;
+    }
+    const T* q = static_cast<const T*>(p.q) + row0 * D;
+    for (int i = threadIdx.x; i < group * D; i += blockDim.x) qf[i] = E::load(q + i) * p.scale_log2;
+    __syncthreads();
+    if (bad) {
+        if (threadIdx.x == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
+        return;
+    }
+    const T* kc = static_cast<const T*>(p.k_cache);
+    const T* vc = static_cast<const T*>(p.v_cache);
+    auto row_of = [&](int i) -> size_t {
+        const int tok = lo + i;
+        const size_t blk = static_cast<size_t>(ids[tok / bs - b0]);
+        return ((blk * p.num_kv_heads + h) * bs + (tok % bs)) * static_cast<size_t>(D);
+    };
+
+    // scores, base 2: one warp per row, lanes over head dims
+    for (int i = warp; i < len; i += nwarps) {
+        const T* krow = kc + row_of(i);
+        for (int g = 0; g < group; ++g) {
+            float acc = 0.f;
+            for (int d = lane; d < D; d += 32) acc = fmaf(qf[g * D + d], E::load(krow + d), acc);
+            acc = warp_sum(acc);
+            if (lane == 0) sc[g * P + i] = acc;
+        }
+    }
+    __syncthreads();
+    // softmax per query head: one warp per head
+    for (int g = warp; g < group; g += nwarps) {
+        float mx = -INFINITY;
+        for (int i = lane; i < len; i += 32) mx = fmaxf(mx, sc[g * P + i]);
+        mx = warp_max(mx);
+        float sum = 0.f;
+        for (int i = lane; i < len; i += 32) {
+            const float e = fast_exp2(sc[g * P + i] - mx);
+            sc[g * P + i] = e;
+            sum += e;
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+            red[2 * g] = mx;
+            red[2 * g + 1] = sum;
+        }
+    }
+    __syncthreads();
+    // P.V: threads over (head, dim)
+    for (int idx = threadIdx.x; idx < group * D; idx += blockDim.x) {
+        const int g = idx / D, d = idx - g * D;
+        float acc = 0.f;
+        for (int i = 0; i < len; ++i) acc = fmaf(sc[g * P + i], E::load(vc + row_of(i) + d), acc);
+        const size_t row = row0 + g;
+        if (nparts == 1) {
+            E::store(static_cast<T*>(p.out) + row * D + d, acc / red[2 * g + 1]);
+        } else {
+            const size_t slot = row * p.max_parts + part;
+            p.part_o[slot * D + d] = acc;
+            if (d == 0) {
+                p.part_ml[2 * slot] = red[2 * g];
+                p.part_ml[2 * slot + 1] = red[2 * g + 1];
+            }
+        }
+    }
+}
+
+constexpr int kCombineThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeParams p) {
+    extern __shared__ float wts[];            // [max_parts] rescale weights
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float total;
+    const int qh = blockIdx.x;
+    const int s = blockIdx.y;
+    const int n = __ldg(p.context_lens + s);
+    const int P = p.partition_size;
+    if (n <= P || n > p.context_cap) return;   // one partition (written directly) or flagged
+    const int np = (n + P - 1) / P;
+    const size_t row = static_cast<size_t>(s) * p.num_heads + qh;
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row * p.max_parts;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < np; i += blockDim.x) mx = fmaxf(mx, ml[i].x);
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        const float2 v = ml[i];
+        const float c = fast_exp2(v.x - M);
+        wts[i] = c;
+        sum = fmaf(c, v.y, sum);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
+        total = L;
+    }
+    __syncthreads();
+    const float inv_l = 1.f / total;
+    const int D = p.head_dim;
+    const float* o = p.part_o + row * p.max_parts * static_cast<size_t>(D);
+    T* out = static_cast<T*>(p.out) + row * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        for (int i = 0; i < np; ++i) acc = fmaf(wts[i], o[static_cast<size_t>(i) * D + d], acc);
+        ElemTraits<T>::store(out + d, acc * inv_l);
+    }
+}
+
+}  // namespace
+
+size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block_size) {
+    const size_t floats = static_cast<size_t>(group) * head_dim +
+                          static_cast<size_t>(group) * partition_size + 2 * static_cast<size_t>(group);
+    const size_t ids = static_cast<size_t>(partition_size) / block_size + 2;
+    return 4 * (floats + ids);
+}
+
+cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
+    const int group = p.num_heads / p.num_kv_heads;
+    const size_t smem = generic_smem_bytes(group, p.head_dim, p.partition_size, p.block_size);
+    const long long grid = static_cast<long long>(p.max_parts) * p.num_seqs * p.num_kv_heads;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    cudaError_t err;
+    if (dtype == PA_DTYPE_BF16) {
+        err = cudaFuncSetAttribute(decode_generic_kernel<__nv_bfloat16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        decode_generic_kernel<__nv_bfloat16>
+            <<<static_cast<unsigned>(grid), kGenericThreads, smem, stream>>>(p, group);
+    } else {
+        err = cudaFuncSetAttribute(decode_generic_kernel<float>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        decode_generic_kernel<float>
+            <<<static_cast<unsigned>(grid), kGenericThreads, smem, stream>>>(p, group);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
+    if (p.max_parts <= 1 || p.num_seqs == 0) return cudaSuccess;
+    const dim3 grid(p.num_heads, p.num_seqs);
+    const size_t smem = static_cast<size_t>(p.max_parts) * sizeof(float);
+    cudaError_t err;
+    if (dtype == PA_DTYPE_BF16) {
+        err = cudaFuncSetAttribute(combine_kernel<__nv_bfloat16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        combine_kernel<__nv_bfloat16><<<grid, kCombineThreads, smem, stream>>>(p);
+    } else {
+        err = cudaFuncSetAttribute(combine_kernel<float>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        combine_kernel<float><<<grid, kCombineThreads, smem, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pa

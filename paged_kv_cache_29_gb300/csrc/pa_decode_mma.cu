@@ -1,0 +1,40 @@
+// pa_decode_mma.cu -- instances of the tile-ring decode kernel with the
+// tensor-core tile math (bf16 caches; head dim 64 or 128; 1, 2, 4 or 8 query
+// heads per KV head).
+#include "pa_decode_tma.cuh"
+
+namespace pa {
+
+namespace {
+constexpr int kWarps = 4;     // consumer warps per CTA
+constexpr int kStages = 6;    // ring depth: 6 x (K + V) tiles = 48 KiB at head dim 128
+
+template <int D, int G>
+cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                cudaStream_t stream) {
+    return launch_tma_instance<MmaMath<D, G>, D, G, kWarps, kStages>(tk, tv, p, stream);
+}
+
+template <int D>
+cudaError_t by_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                     cudaStream_t stream) {
+    switch (p.num_heads / p.num_kv_heads) {
+        case 1: return run<D, 1>(tk, tv, p, stream);
+        case 2: return run<D, 2>(tk, tv, p, stream);
+        case 4: return run<D, 4>(tk, tv, p, stream);
+        case 8: return run<D, 8>(tk, tv, p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+}  // namespace
+
+cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, cudaStream_t stream) {
+    switch (p.head_dim) {
+        case 64: return by_group<64>(tk, tv, p, stream);
+        case 128: return by_group<128>(tk, tv, p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,61 @@
+// pa_internal.h -- parameters and launchers shared between the host API and
+// the kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// Everything a decode kernel needs besides the tensor maps.
+struct DecodeParams {
+    const void* q;                 // [B][Hq][D], cache dtype
+    void* out;                     // [B][Hq][D], cache dtype
+    const void* k_cache;           // raw pool pointers (the generic kernel reads them directly)
+    const void* v_cache;
+    const int32_t* block_tables;   // [B][max_blocks_per_seq]
+    const int32_t* context_lens;   // [B]
+    float* part_o;                 // [B][Hq][max_parts][D] unnormalised partial outputs
+    float* part_ml;                // [B][Hq][max_parts][2] (running max in log2 units, sum)
+    int32_t* error_word;           // nullable
+    float scale_log2;              // scale * log2(e): scores are kept in base 2
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    int num_blocks;
+    int max_blocks_per_seq;
+    int context_cap;               // min(max_context_len, max_blocks_per_seq * block_size)
+    int partition_size;
+    int max_parts;                 // ceil(max_context_len / partition_size), >= 1
+};
+
+// Launch result: cudaSuccess or the launch error.
+cudaError_t launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                          int row_bytes, int block_size, int num_blocks, int32_t* error_word,
+                          cudaStream_t stream);
+
+// TMA-ring kernels. Return cudaErrorNotSupported for shapes without an instance.
+cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
+bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group);
+
+// Direct-load kernel for any block size and head dim <= 256.
+cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
+size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block_size);
+
+// Merge of partition partials for sequences longer than one partition.
+cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
+
+constexpr int kMaxHeadDim = 256;
+constexpr int kDefaultPartition = 512;
+
+}  // namespace pa

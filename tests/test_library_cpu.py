@@ -1,0 +1,102 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+the header declares, and rejects bad arguments on the host before touching
+CUDA."""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_29_gb300 import _binding as pa
+from paged_kv_cache_29_gb300 import build as build_mod
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return pa.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = pa.declared_functions()
+    assert {"pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size",
+            "pa_status_string"} <= set(names)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    for code in range(6):
+        assert pa.pa_status_string(code)
+    assert pa.pa_status_string(99) == "unknown status"
+    assert pa.pa_version() >= 10000
+    assert lib.pa_check_error_word(0) == pa.PA_OK
+    assert lib.pa_check_error_word(pa.PA_DEVERR_SLOT) == pa.PA_ERR_DEVICE_BOUNDS
+
+
+def _decode(lib, **kw):
+    args = dict(q=None, k=None, v=None, bt=None, cl=None, scale=0.1, out=None, B=4, Hq=8,
+                Hkv=2, D=128, bs=16, NB=10, mb=4, mcl=64, dtype=1, ws=None, wsb=0, err=None)
+    args.update(kw)
+    return lib.pa_decode(*args.values(), None)
+
+
+FAKE = 1 << 20   # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), pa.PA_ERR_INVALID_ARG),                     # heads not a multiple
+    (dict(q=None), pa.PA_ERR_INVALID_ARG),                           # null pointers
+    (dict(dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(mcl=65), pa.PA_ERR_INVALID_ARG),                          # past max_blocks * bs
+    (dict(B=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(D=512), pa.PA_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, status):
+    ptrs = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, out=FAKE)
+    if "q" in kw:
+        ptrs["q"] = None
+        kw = {}
+    assert _decode(lib, **ptrs, **kw) == status
+
+
+def test_decode_rejects_misaligned_and_missing_workspace(lib):
+    ptrs = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, out=FAKE)
+    assert _decode(lib, **{**ptrs, "q": FAKE + 8}) == pa.PA_ERR_INVALID_ARG
+    # 600 rows need two partitions of 512: workspace required
+    assert _decode(lib, **ptrs, mcl=600, mb=40) == pa.PA_ERR_WORKSPACE
+    need = lib.pa_decode_workspace_size(4, 8, 128, 600)
+    assert need == 4 * 8 * 2 * 130 * 4
+    assert _decode(lib, **ptrs, mcl=600, mb=40, ws=FAKE, wsb=need - 4) == pa.PA_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _decode(lib, B=0) == pa.PA_OK
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, 2, 128, 16, 8, 1, None,
+                                    None) == pa.PA_OK
+
+
+def test_append_rejects_bad_arguments(lib):
+    P = FAKE
+    assert lib.pa_reshape_and_cache(P, P, P, P, P, 4, 2, 128, 0, 8, 1, None, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(P, P, P, P, P, 4, 2, 3, 16, 8, 1, None, None) == \
+        pa.PA_ERR_UNSUPPORTED                                         # 6-byte rows
+    assert lib.pa_reshape_and_cache(None, P, P, P, P, 4, 2, 128, 16, 8, 1, None, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(P + 4, P, P, P, P, 4, 2, 128, 16, 8, 1, None, None) == \
+        pa.PA_ERR_INVALID_ARG
+
+
+def test_workspace_size_formula(lib):
+    assert lib.pa_decode_workspace_size(8, 32, 128, 512) == 0
+    assert lib.pa_decode_workspace_size(8, 32, 128, 100_000) == 8 * 32 * 196 * 130 * 4
+    assert lib.pa_decode_workspace_size_ex(2, 4, 64, 100, 16) == 2 * 4 * 7 * 66 * 4
+
+
+def test_python_binding_has_no_cpu_fallback():
+    """The binding refuses CPU tensors instead of computing anything itself."""
+    import torch
+    x = torch.zeros(1, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pa.pa_reshape_and_cache(x, x, torch.zeros(1, dtype=torch.int64),
+                                torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16),
+                                torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16))
