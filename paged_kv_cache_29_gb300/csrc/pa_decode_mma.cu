@@ -7,7 +7,7 @@ namespace pa {
 
 namespace {
 constexpr int kWarps = 4;     // consumer warps per CTA
-constexpr int kStages = 6;    // ring depth: 6 x (K + V) tiles = 48 KiB at head dim 128
+constexpr int kStages = 8;    // ring depth, a multiple of kWarps: 8 x (K + V) tiles = 64 KiB at d=128
 
 template <int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,

@@ -8,10 +8,12 @@ namespace pa {
 namespace {
 constexpr int kWarps = 4;
 
-// Ring depth by tile size: about 48 KiB of K and V tiles in flight per CTA.
+// Ring depth by tile size: about 48 KiB of K and V tiles per CTA, rounded
+// down to a multiple of the consumer warps (at least one stage per warp).
 template <typename T, int D>
 constexpr int stages_for() {
-    return (48 * 1024) / TileGeom<T, D>::kStageBytes < 3 ? 3 : (48 * 1024) / TileGeom<T, D>::kStageBytes;
+    constexpr int fit = (48 * 1024) / TileGeom<T, D>::kStageBytes;
+    return fit < kWarps ? kWarps : (fit / kWarps) * kWarps;
 }
 
 template <typename T, int D, int G>

@@ -117,8 +117,10 @@ struct MmaMath {
     __device__ __forceinline__ void init(const DecodeParams& p, int s, int h, int lane) {
         gid = lane >> 2;
         t4 = lane & 3;
+        // Lanes of padded heads (gid >= G) keep a valid row pointer and load nothing.
+        const int head = h * G + (gid < G ? gid : G - 1);
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_heads + h * G + gid) * D);
+            static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_heads + head) * D);
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             qb[kk][0] = gid < G ? __ldg(qrow + 8 * kk + t4) : 0u;
@@ -399,10 +401,17 @@ __device__ __forceinline__ void write_zero_rows(const DecodeParams& p, int s, in
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) ElemTraits<T>::store(out + i, 0.f);
 }
 
+// Stage ownership: tile t lives in stage t % STAGES and is consumed by warp
+// t % W. With STAGES a multiple of W every stage belongs to one warp, which
+// waits on its uses in order, so a waiter is never more than one phase ahead
+// of the barrier it polls. (A parity wait cannot tell phase u from phase u+2:
+// if a stage were shared between warps, a fast warp could see the stage's
+// previous phase as its own and consume a tile that has not landed.)
 template <class Math, int D, int G, int W, int STAGES>
 __global__ void __launch_bounds__((W + 1) * 32)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+    static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
     using Smem = DecodeSmem<W, STAGES, Geom, G, D>;
