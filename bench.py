@@ -100,6 +100,17 @@ def profiled_traffic(workload: str, kernel: str) -> float | None:
         return None
 
 
+def _quick_step_seconds(do_step, flush) -> float:
+    """Wall time of one step (for sizing the clock soak)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        do_step()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) / 5
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
 
@@ -115,7 +126,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -264,7 +275,9 @@ def run_native(args) -> dict | None:
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
+    # append, plan, decode (the split-K merge runs inside the decode kernel;
+    # a separate merge kernel follows only the generic decode kernel)
+    launches_per_step = 3 if args.kernel != "generic" else 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
 
     def do_step():
         pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
@@ -280,29 +293,48 @@ def run_native(args) -> dict | None:
         raise RuntimeError(f"device error word {int(err.item()):#x} during warm-up")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # Clock soak: about a second of back-to-back steps under the clock sampler,
+    # so the clocks reported describe this load, then the timed region.
+    soak_steps = 0
+    if args.clock_soak_s > 0:
+        soak_steps = max(1, int(args.clock_soak_s / max(1e-4, _quick_step_seconds(do_step, flush))))
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        for _ in range(soak_steps):
+            do_step()
+        # Timed region A: whole steps (append + attention), events around each
+        # step only, so the launches of a step run back to back as in use.
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
         for i in range(K):
             flush.fill_(i & 0xff)
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
-                                    stream=stream)
-            e1.record(stream)
-            pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
-                         workspace=workspace, error_word=err, stream=stream, kernel=args.kernel)
-            e2.record(stream)
+            ev[i][0].record(stream)
+            do_step()
+            ev[i][1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
-    append_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
+    # Timed region B: the same steps with events around the attention call,
+    # for the roofline of the dominant kernel (decode + merge).
+    evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xff)
+        e0, e1, e2 = evb[i]
+        e0.record(stream)
+        pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
+                                stream=stream)
+        e1.record(stream)
+        pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                     workspace=workspace, error_word=err, stream=stream, kernel=args.kernel)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    decode_ms = [b.elapsed_time(c) for _, b, c in evb]
+    append_ms = [a.elapsed_time(b) for a, b, _ in evb]
     decode_avg = sum(decode_ms) / K
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
@@ -392,7 +424,7 @@ def run_native(args) -> dict | None:
                               "decode_call": round(decode_avg, 5)},
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode call (decode_tma_kernel + combine_kernel)",
+            "kernel": "pa_decode call (plan_kernel + decode_stream_kernel with fused split-K merge)",
             "achieved": round(decode_gbs, 2),
             "peak": peak,
             "unit": "GB/s",
@@ -409,6 +441,7 @@ def run_native(args) -> dict | None:
             "d2h_bytes_per_step": d2h,
         },
         "gpu_launches": launches_per_step * K,
+        "gpu_launches_note": "timed region A; region B repeats the same launches",
         "clocks": clocks.summary(),
     }
     if step.meta.get("unique_blocks") and bytes_.kv_unique != bytes_.kv:
@@ -476,6 +509,9 @@ def main() -> None:
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle time of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-soak-s", type=float, default=1.0,
+                    help="seconds of untimed back-to-back steps under the clock sampler "
+                         "before the timed region (0 = none)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -96,15 +96,18 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
  * Long sequences are split into fixed partitions of 512 rows whose partial
  * results (running max, sum and unnormalised output, the online-softmax state
  * of Q4 "How would you write a fused attention kernel?") are merged by a
- * second kernel. Partition boundaries depend only on the sequence's own
- * length, so a sequence's result does not depend on the rest of the batch.
+ * second kernel. Partition boundaries and the merge order depend only on the
+ * sequence's own length, so a sequence's result does not depend on the rest
+ * of the batch.
  *
- * max_context_len: an upper bound on every context_lens[s] (sizes the grid
- *   and the workspace); must not exceed max_blocks_per_seq * block_size.
+ * max_context_len: an upper bound on every context_lens[s] (sizes the work
+ *   list and the workspace); must not exceed max_blocks_per_seq * block_size.
  * workspace: device scratch of at least
  *   pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len)
- *   bytes, 16-byte aligned; may be NULL when that size is 0 (every sequence
- *   fits one partition). Its contents on entry do not matter.
+ *   bytes, 16-byte aligned (non-zero for any non-empty batch: it holds the
+ *   call's work list, and the partition partials when a sequence can span
+ *   more than one partition). Its contents on entry do not matter; calls that
+ *   share one workspace must not overlap on the GPU.
  * Supported: fp32 and bf16; any block_size >= 1; head_dim 1..256; any
  * num_heads that is a multiple of num_kv_heads. The fastest kernels need
  * block_size a multiple of 16, head_dim 64 or 128 and at most 8 query heads
@@ -118,8 +121,8 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     int max_context_len, pa_dtype dtype, void* workspace,
                     size_t workspace_bytes, int32_t* error_word, struct CUstream_st* stream);
 
-/* Bytes of workspace pa_decode needs for these sizes (0 if no sequence can
- * span more than one partition). */
+/* Bytes of workspace pa_decode needs for these sizes (0 only for an empty
+ * batch). */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
 
 /* Kernel choice for pa_decode_ex (for measurement and tests; pa_decode uses

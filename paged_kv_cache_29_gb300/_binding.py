@@ -167,9 +167,10 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
               partition_size: int = 0) -> None:
     """Decode attention for every sequence, written into ``out`` ([B][Hq][D]).
 
-    max_context_len bounds context_lens (host value; sizes grid and workspace).
-    workspace: a CUDA tensor of at least pa_decode_workspace_size(...) bytes,
-    required when max_context_len exceeds one partition."""
+    max_context_len bounds context_lens (host value; sizes the work list and
+    the workspace). workspace: a CUDA tensor of at least
+    pa_decode_workspace_size(...) bytes; when None, one is allocated from
+    torch's caching allocator for this call."""
     import torch
     _check_cuda("k_cache", k_cache, ndim=4)
     _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
@@ -184,10 +185,13 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
-    ws_bytes = 0
-    if workspace is not None:
-        _check_cuda("workspace", workspace)
-        ws_bytes = workspace.numel() * workspace.element_size()
+    if workspace is None:
+        # The C library allocates nothing; the binding takes the scratch from
+        # torch's allocator for callers that do not manage their own.
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len), int(partition_size))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
     opts = _Options(KERNELS[kernel], int(partition_size))
     rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d, bs, nb,

@@ -38,21 +38,27 @@ int elem_bytes(pa_dtype d) { return d == PA_DTYPE_F32 ? 4 : 2; }
 
 bool valid_dtype(pa_dtype d) { return d == PA_DTYPE_F32 || d == PA_DTYPE_BF16; }
 
-// The pool viewed as a 2D tensor [rows][head_dim], rows = blocks * kv_heads *
-// block_size; boxes of 16 rows x 128 bytes with the 128-byte swizzle.
+// The pool viewed as a 3D tensor for TMA: x = element within a 128-byte
+// column half of a row, y = row (rows = blocks * kv_heads * block_size, stride
+// one row), z = which 128-byte half (stride 128 bytes). One box {128 B, 16
+// rows, all halves} is one 16-row tile of one (block, KV head), landing in
+// shared memory as [half][row][128 B] with the 128-byte swizzle.
 pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dtype, int head_dim,
                         long long rows) {
     EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr) return PA_ERR_CUDA;
     const int es = elem_bytes(dtype);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * es};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 16u};
-    const cuuint32_t estr[2] = {1u, 1u};
+    const int row_bytes = head_dim * es;
+    const int halves = row_bytes / 128;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / es), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(halves)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), 128};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 16u, static_cast<cuuint32_t>(halves)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(map,
                           dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          2, const_cast<void*>(base), dims, strides, box, estr,
+                          3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -60,13 +66,36 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dtype, int 
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// Workspace layout (per launch of at most kPlanMaxSeqs sequences, reused by
+// consecutive launches of one call):
+//   [0, 256)              work-item count
+//   items                 int4 per (sequence, KV head, partition): num_heads
+//                         bounds num_kv_heads
+//   part_ml, part_o       partition partials, only when a sequence can span
+//                         more than one partition
+struct WorkspaceLayout {
+    size_t items_off, ml_off, o_off, total;
+};
+
+WorkspaceLayout layout_for(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                           int partition_size) {
+    WorkspaceLayout w{0, 0, 0, 0};
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || partition_size <= 0 ||
+        max_context_len < 0)
+        return w;
+    const long long seqs = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
+    const long long parts = max_context_len > 0 ? ceil_div(max_context_len, partition_size) : 1;
+    const size_t units = static_cast<size_t>(seqs) * num_heads * parts;
+    w.items_off = 256;
+    w.ml_off = w.items_off + 16 * units;
+    w.o_off = w.ml_off + (parts > 1 ? 8 * units : 0);
+    w.total = w.o_off + (parts > 1 ? 4 * units * static_cast<size_t>(head_dim) : 0);
+    return w;
+}
+
 size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int max_context_len,
                            int partition_size) {
-    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || partition_size <= 0 ||
-        max_context_len <= partition_size)
-        return 0;
-    const long long parts = ceil_div(max_context_len, partition_size);
-    return static_cast<size_t>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float);
+    return layout_for(num_seqs, num_heads, head_dim, max_context_len, partition_size).total;
 }
 
 }  // namespace
@@ -155,12 +184,11 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
 
     const int group = num_heads / num_kv_heads;
     const long long max_parts = max_context_len > 0 ? ceil_div(max_context_len, partition) : 1;
-    const long long grid = max_parts * num_seqs * num_kv_heads;
-    if (grid > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if (max_parts > 1 && num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    const long long chunk = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
+    if (max_parts * chunk * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
 
-    const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, max_context_len, partition);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    const WorkspaceLayout lay = layout_for(num_seqs, num_heads, head_dim, max_context_len, partition);
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
         return PA_ERR_WORKSPACE;
 
     const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
@@ -182,46 +210,66 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
         pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem)
         return PA_ERR_UNSUPPORTED;
 
-    DecodeParams p{};
-    p.q = q;
-    p.out = out;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    const size_t ml_floats = static_cast<size_t>(num_seqs) * num_heads * max_parts * 2;
-    p.part_ml = need ? static_cast<float*>(workspace) : nullptr;
-    p.part_o = need ? static_cast<float*>(workspace) + ml_floats : nullptr;
-    p.error_word = error_word;
-    p.scale_log2 = scale * kLog2e;
-    p.num_seqs = num_seqs;
-    p.num_heads = num_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.head_dim = head_dim;
-    p.block_size = block_size;
-    p.num_blocks = num_blocks;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.context_cap = max_context_len;
-    p.partition_size = partition;
-    p.max_parts = static_cast<int>(max_parts);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams base{};
+    base.k_cache = k_cache;
+    base.v_cache = v_cache;
+    base.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ml_off) : nullptr;
+    base.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.o_off) : nullptr;
+    base.sched = reinterpret_cast<int*>(ws);
+    base.items = reinterpret_cast<int4*>(ws + lay.items_off);
+    base.error_word = error_word;
+    base.scale_log2 = scale * kLog2e;
+    base.num_heads = num_heads;
+    base.num_kv_heads = num_kv_heads;
+    base.head_dim = head_dim;
+    base.block_size = block_size;
+    base.num_blocks = num_blocks;
+    base.max_blocks_per_seq = max_blocks_per_seq;
+    base.context_cap = max_context_len;
+    base.partition_size = partition;
+    base.max_parts = static_cast<int>(max_parts);
 
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t err;
-    if (kernel == PA_KERNEL_GENERIC) {
-        err = pa::launch_decode_generic(p, dtype, st);
-    } else {
-        CUtensorMap tk, tv;
+    CUtensorMap tk, tv;
+    int sm_count = 0;
+    if (kernel != PA_KERNEL_GENERIC) {
         pa_status ps = make_pool_map(&tk, k_cache, dtype, head_dim, rows);
         if (ps == PA_OK) ps = make_pool_map(&tv, v_cache, dtype, head_dim, rows);
         if (ps != PA_OK) return ps;
-        err = kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, st)
-                                      : pa::launch_decode_simt(tk, tv, p, dtype, st);
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sm_count <= 0)
+            return PA_ERR_CUDA;
     }
-    if (err == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
-    if (err != cudaSuccess) return PA_ERR_CUDA;
-    if (max_parts > 1) {
-        err = pa::launch_combine(p, dtype, st);
+    const size_t es = static_cast<size_t>(elem_bytes(dtype));
+    // Batches above kPlanMaxSeqs sequences run as consecutive launches over
+    // slices of the batch; they reuse the workspace in stream order.
+    for (int s0 = 0; s0 < num_seqs; s0 += pa::kPlanMaxSeqs) {
+        const int bs_n = num_seqs - s0 < pa::kPlanMaxSeqs ? num_seqs - s0 : pa::kPlanMaxSeqs;
+        DecodeParams p = base;
+        const size_t qoff = static_cast<size_t>(s0) * num_heads * head_dim * es;
+        p.q = static_cast<const uint8_t*>(q) + qoff;
+        p.out = static_cast<uint8_t*>(out) + qoff;
+        p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
+        p.context_lens = context_lens + s0;
+        p.num_seqs = bs_n;
+        cudaError_t err;
+        if (kernel == PA_KERNEL_GENERIC) {
+            err = pa::launch_decode_generic(p, dtype, st);
+        } else {
+            err = pa::launch_plan(p, dtype, st);
+            if (err == cudaSuccess)
+                err = kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
+                                              : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
+        }
+        if (err == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
         if (err != cudaSuccess) return PA_ERR_CUDA;
+        if (max_parts > 1) {
+            err = pa::launch_combine(p, dtype, st);
+            if (err != cudaSuccess) return PA_ERR_CUDA;
+        }
     }
     return PA_OK;
 }

@@ -21,6 +21,9 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
               const int64_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
               uint4* __restrict__ v_cache, long long total_chunks, int chunks_per_row,
               int num_kv_heads, int block_size, long long num_slots, int32_t* error_word) {
+    // A decode call launched next on the stream may start its set-up now; it
+    // waits for this grid to finish before reading the cache.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
          i < total_chunks; i += stride) {

@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodePa
     extern __shared__ float wts[];            // [max_parts] rescale weights
     __shared__ float red[kCombineThreads / 32];
     __shared__ float total;
+    // Launched as a programmatic dependent of the decode kernel: wait for its
+    // partials before reading anything.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int qh = blockIdx.x;
     const int s = blockIdx.y;
     const int n = __ldg(p.context_lens + s);
@@ -238,20 +241,28 @@ cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStr
 
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
     if (p.max_parts <= 1 || p.num_seqs == 0) return cudaSuccess;
-    const dim3 grid(p.num_heads, p.num_seqs);
     const size_t smem = static_cast<size_t>(p.max_parts) * sizeof(float);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_heads, p.num_seqs);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t err;
     if (dtype == PA_DTYPE_BF16) {
         err = cudaFuncSetAttribute(combine_kernel<__nv_bfloat16>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (err != cudaSuccess) return err;
-        combine_kernel<__nv_bfloat16><<<grid, kCombineThreads, smem, stream>>>(p);
+        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
     } else {
         err = cudaFuncSetAttribute(combine_kernel<float>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (err != cudaSuccess) return err;
-        combine_kernel<float><<<grid, kCombineThreads, smem, stream>>>(p);
+        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
     }
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

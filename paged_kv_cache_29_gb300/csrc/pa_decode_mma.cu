@@ -1,38 +1,39 @@
 // pa_decode_mma.cu -- instances of the tile-ring decode kernel with the
 // tensor-core tile math (bf16 caches; head dim 64 or 128; 1, 2, 4 or 8 query
 // heads per KV head).
-#include "pa_decode_tma.cuh"
+#include "pa_decode_stream.cuh"
 
 namespace pa {
 
 namespace {
 constexpr int kWarps = 4;     // consumer warps per CTA
-constexpr int kStages = 8;    // ring depth, a multiple of kWarps: 8 x (K + V) tiles = 64 KiB at d=128
+constexpr int kStages = 4;    // ring depth, a multiple of kWarps: 4 x (K + V) tiles = 32 KiB at d=128
 
 template <int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                cudaStream_t stream) {
-    return launch_tma_instance<MmaMath<D, G>, D, G, kWarps, kStages>(tk, tv, p, stream);
+                int sm_count, cudaStream_t stream) {
+    return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages>(tk, tv, p, sm_count,
+                                                                          stream);
 }
 
 template <int D>
 cudaError_t by_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                     cudaStream_t stream) {
+                     int sm_count, cudaStream_t stream) {
     switch (p.num_heads / p.num_kv_heads) {
-        case 1: return run<D, 1>(tk, tv, p, stream);
-        case 2: return run<D, 2>(tk, tv, p, stream);
-        case 4: return run<D, 4>(tk, tv, p, stream);
-        case 8: return run<D, 8>(tk, tv, p, stream);
+        case 1: return run<D, 1>(tk, tv, p, sm_count, stream);
+        case 2: return run<D, 2>(tk, tv, p, sm_count, stream);
+        case 4: return run<D, 4>(tk, tv, p, sm_count, stream);
+        case 8: return run<D, 8>(tk, tv, p, sm_count, stream);
         default: return cudaErrorNotSupported;
     }
 }
 }  // namespace
 
 cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecodeParams& p, cudaStream_t stream) {
+                              const DecodeParams& p, int sm_count, cudaStream_t stream) {
     switch (p.head_dim) {
-        case 64: return by_group<64>(tk, tv, p, stream);
-        case 128: return by_group<128>(tk, tv, p, stream);
+        case 64: return by_group<64>(tk, tv, p, sm_count, stream);
+        case 128: return by_group<128>(tk, tv, p, sm_count, stream);
         default: return cudaErrorNotSupported;
     }
 }

@@ -1,55 +1,54 @@
 // pa_decode_simt.cu -- instances of the tile-ring decode kernel with the
 // CUDA-core tile math (fp32 or bf16 caches; head dim 64 or 128; 1, 2, 4 or 8
 // query heads per KV head).
-#include "pa_decode_tma.cuh"
+#include "pa_decode_stream.cuh"
 
 namespace pa {
 
 namespace {
 constexpr int kWarps = 4;
 
-// Ring depth by tile size: about 48 KiB of K and V tiles per CTA, rounded
-// down to a multiple of the consumer warps (at least one stage per warp).
+// Ring depth: one stage per consumer warp (short rings, several CTAs per SM).
 template <typename T, int D>
 constexpr int stages_for() {
-    constexpr int fit = (48 * 1024) / TileGeom<T, D>::kStageBytes;
-    return fit < kWarps ? kWarps : (fit / kWarps) * kWarps;
+    return kWarps;
 }
 
 template <typename T, int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                cudaStream_t stream) {
-    return launch_tma_instance<SimtMath<T, D, G>, D, G, kWarps, stages_for<T, D>()>(tk, tv, p,
-                                                                                     stream);
+                int sm_count, cudaStream_t stream) {
+    return launch_stream_instance<SimtMath<T, D, G>, D, G, kWarps, stages_for<T, D>()>(
+        tk, tv, p, sm_count, stream);
 }
 
 template <typename T, int D>
 cudaError_t by_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                     cudaStream_t stream) {
+                     int sm_count, cudaStream_t stream) {
     switch (p.num_heads / p.num_kv_heads) {
-        case 1: return run<T, D, 1>(tk, tv, p, stream);
-        case 2: return run<T, D, 2>(tk, tv, p, stream);
-        case 4: return run<T, D, 4>(tk, tv, p, stream);
-        case 8: return run<T, D, 8>(tk, tv, p, stream);
+        case 1: return run<T, D, 1>(tk, tv, p, sm_count, stream);
+        case 2: return run<T, D, 2>(tk, tv, p, sm_count, stream);
+        case 4: return run<T, D, 4>(tk, tv, p, sm_count, stream);
+        case 8: return run<T, D, 8>(tk, tv, p, sm_count, stream);
         default: return cudaErrorNotSupported;
     }
 }
 
 template <typename T>
 cudaError_t by_dim(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                   cudaStream_t stream) {
+                   int sm_count, cudaStream_t stream) {
     switch (p.head_dim) {
-        case 64: return by_group<T, 64>(tk, tv, p, stream);
-        case 128: return by_group<T, 128>(tk, tv, p, stream);
+        case 64: return by_group<T, 64>(tk, tv, p, sm_count, stream);
+        case 128: return by_group<T, 128>(tk, tv, p, sm_count, stream);
         default: return cudaErrorNotSupported;
     }
 }
 }  // namespace
 
 cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
-    return dtype == PA_DTYPE_BF16 ? by_dim<__nv_bfloat16>(tk, tv, p, stream)
-                                  : by_dim<float>(tk, tv, p, stream);
+                               const DecodeParams& p, pa_dtype dtype, int sm_count,
+                               cudaStream_t stream) {
+    return dtype == PA_DTYPE_BF16 ? by_dim<__nv_bfloat16>(tk, tv, p, sm_count, stream)
+                                  : by_dim<float>(tk, tv, p, sm_count, stream);
 }
 
 bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group) {

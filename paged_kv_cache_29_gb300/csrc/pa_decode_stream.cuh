@@ -1,0 +1,343 @@
+// pa_decode_stream.cuh -- persistent paged decode attention with a TMA tile ring.
+//
+// Work item: one (sequence s, KV head h, partition p) of at most
+// partition_size rows. The plan kernel lists every item of the batch in the
+// workspace (full partitions first, then the partial last partitions, largest
+// first). A fixed set of CTAs (a few per SM) walks that list: CTA c takes
+// items c, 2C-1-c, 2C+c, ... (a snake, so that the per-CTA totals even out)
+// and streams all of their tiles through one ring without stopping between
+// items.
+//
+// Producer warp: for each item, loads its block ids (one coalesced load,
+// validated against the pool, prefetched one item ahead), then for every
+// 16-row tile issues 2D TMA loads of the K and V tile (16 rows x head_dim of
+// one physical block and KV head, contiguous in the
+// [block][kv_head][block_size][head_dim] pool) into the next ring stage. Row i
+// of a sequence is row (i % block_size) of block block_tables[s][i /
+// block_size]: the paged gather of "MLSys Engineer -- Inference Systems Q&A",
+// Q1.
+//
+// Consumer warps: the CTA's tiles are numbered in stream order; tile t lives
+// in stage t % STAGES and is consumed by warp t % W (STAGES is a multiple of
+// W, so every stage has one owner and parity waits stay within one phase).
+// At the end of an item every warp writes its online-softmax state to a
+// double-buffered merge area, the consumer warps meet at a named barrier, and
+// the merged result is written as the final output (one partition) or as the
+// item's partial (max, sum, unnormalised output) for the combine kernel.
+//
+// Sizing: a random 4 KB tile gather streams at about 6.6 TB/s on GB300 only
+// with four or more independent rings per SM (a ring's single producer waits
+// on its oldest stage); deeper rings in fewer CTAs stream slower. So the
+// kernel runs several small CTAs per SM, each with a short ring.
+//
+// Programmatic dependent launch: everything before griddepcontrol.wait (ring
+// and barrier set-up) may overlap the previous kernel on the stream; every
+// global read of the plan, the block tables, q and the KV pool comes after it.
+#pragma once
+
+#include "pa_tile_math.cuh"
+
+namespace pa {
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Block ids of one item: partitions of up to 4096 rows span at most
+// 4096 / 16 + 1 = 257 blocks when block_size is a multiple of 16.
+constexpr int kMaxItemBlocks = 260;
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_group_1() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// CTA c's j-th item in a snake over C CTAs.
+__device__ __forceinline__ int snake_item(int c, int j, int C) {
+    return j * C + ((j & 1) ? (C - 1 - c) : c);
+}
+
+template <int W, int STAGES, typename Geom, int G, int D>
+struct StreamSmem {
+    static constexpr int kRing = STAGES * Geom::kStageBytes;
+    static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
+    static constexpr int kMerge = 2 * W * kState * 4;   // double-buffered warp states
+    static constexpr int kBarriers = 2 * STAGES * 8;
+    static constexpr int kFlags = (STAGES + 2 * W + 8) * 4;
+    static constexpr int kIds = 2 * kMaxItemBlocks * 4;
+    static constexpr size_t kBytes = 1024 + kRing + kMerge + kBarriers + kFlags + kIds;
+};
+
+template <class Math, int D, int G, int W, int STAGES>
+__global__ void __launch_bounds__((W + 1) * 32)
+decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+    static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
+    using T = typename Math::T;
+    using Geom = typename Math::Geom;
+    using Smem = StreamSmem<W, STAGES, Geom, G, D>;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float* merge = reinterpret_cast<float*>(ring + Smem::kRing);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + Smem::kRing + Smem::kMerge);
+    uint64_t* empty = full + STAGES;
+    volatile int32_t* stage_bad = reinterpret_cast<volatile int32_t*>(empty + STAGES);
+    volatile int32_t* warp_bad = stage_bad + STAGES;          // [2][W]: per item parity
+    volatile int32_t* abort_flag = warp_bad + 2 * W;
+    int32_t* ids_buf = reinterpret_cast<int32_t*>(
+        reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(smem_addr(&full[i]), 1);
+            mbar_init(smem_addr(&empty[i]), 1);
+        }
+        abort_flag[0] = 0;
+        mbar_init_fence();
+    }
+    if (warp == W && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int total = __ldg(p.sched);
+    const int C = gridDim.x;
+    const int c = blockIdx.x;
+    const int P = p.partition_size;
+    const int bs = p.block_size;
+    const uint32_t ring_addr = smem_addr(ring);
+
+    if (warp == W) {
+        // ------------------------------ producer ------------------------------
+        // Item info and block ids are loaded one item ahead of their use.
+        auto load_item = [&](int j) -> int4 {
+            const int k = snake_item(c, j, C);
+            return k < total ? __ldg(p.items + k) : make_int4(-1, 0, 0, 0);
+        };
+        // Block ids of an item are copied into a double-buffered shared array
+        // with cp.async one item ahead of their use.
+        auto prefetch_ids = [&](const int4& it, int32_t* buf) {
+            if (it.x >= 0) {
+                const int lo = it.z * P;
+                const int hi = min(it.w, lo + P);
+                const int b0 = lo / bs;
+                const int nblk = (hi - 1) / bs - b0 + 1;
+                const int32_t* bt = p.block_tables + static_cast<size_t>(it.x) * p.max_blocks_per_seq + b0;
+                for (int i = lane; i < nblk; i += 32) cp_async_4(smem_addr(buf + i), bt + i);
+            }
+            cp_async_commit();
+        };
+        int4 cur = load_item(0);
+        int4 nxt = load_item(1);
+        prefetch_ids(cur, ids_buf);
+        int t = 0;              // stream tile counter
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; cur.x >= 0 && ok; ++j) {
+            const int4 nxt2 = load_item(j + 2);     // used two items from now
+            int32_t* ids = ids_buf + (j & 1) * kMaxItemBlocks;
+            prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
+            cp_async_wait_group_1();                // this item's ids have landed
+            __syncwarp();
+            const int b0 = (cur.z * P) / bs;
+            const int nblk = (min(cur.w, cur.z * P + P) - 1) / bs - b0 + 1;
+            bool bad_lane = false;
+            for (int i = lane; i < nblk; i += 32) bad_lane |= (ids[i] < 0) | (ids[i] >= p.num_blocks);
+            const int cur_bad = __any_sync(0xffffffffu, bad_lane) ? 1 : 0;
+            const int lo = cur.z * P;
+            const int hi = min(cur.w, lo + P);
+            const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
+            if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
+            for (int tt = 0; tt < ntiles; ++tt, ++t) {
+                const int tok = lo + kTileRows * tt;
+                const int stage = t % STAGES;
+                const uint32_t fb = smem_addr(&full[stage]);
+                if (lane == 0) {
+                    if (t >= STAGES && !mbar_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
+                        ok = false;
+                    } else if (abort_flag[0]) {
+                        ok = false;
+                    } else {
+                        stage_bad[stage] = cur_bad;
+                        if (cur_bad)
+                            mbar_arrive(fb);          // no data: consumers skip the tile
+                        else
+                            mbar_arrive_expect_tx(fb, Geom::kStageBytes);
+                        issued = t + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                // Lane 0 copies the K tile, lane 1 the V tile: one 3D box each
+                // (all 128-byte column halves of 16 rows), issued after lane
+                // 0's expect_tx (ordered by the shuffle above).
+                if (!cur_bad && lane < 2) {
+                    const int id = ids[tok / bs - b0];
+                    const int row = (id * p.num_kv_heads + cur.y) * bs + (tok % bs);
+                    const uint32_t dst = ring_addr + stage * Geom::kStageBytes +
+                                         (lane ? Geom::kTileBytes : 0);
+                    tma_load_3d(dst, lane ? static_cast<const void*>(&tmap_v)
+                                          : static_cast<const void*>(&tmap_k),
+                                fb, 0, row, 0);
+                }
+            }
+            cur = nxt;
+            nxt = nxt2;
+        }
+        cp_async_wait_all();
+        if (lane == 0) {
+            if (!ok) {
+                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                abort_flag[0] = 1;
+            }
+            // Copies still in flight must land before the CTA's shared memory
+            // is released: wait (bounded) for the last issued stages.
+            for (int u = issued > STAGES ? issued - STAGES : 0; u < issued; ++u)
+                (void)mbar_wait(smem_addr(&full[u % STAGES]), (u / STAGES) & 1);
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    // The next item's description and q are loaded one item ahead, so that an
+    // item boundary costs no global-memory round trip.
+    Math math;
+    math.setup(lane);
+    auto item_at = [&](int j) -> int4 {
+        const int k = snake_item(c, j, C);
+        return k < total ? __ldg(p.items + k) : make_int4(-1, 0, 0, 0);
+    };
+    int4 it = item_at(0);
+    int4 it_next = item_at(1);
+    typename Math::QRegs q_next;
+    if (it.x >= 0) math.load_q(p, it.x, it.y, q_next);
+    int t0 = 0;                 // stream index of the current item's first tile
+    bool aborted = false;
+    for (int j = 0; it.x >= 0; ++j) {
+        const int s = it.x, h = it.y, part = it.z, n = it.w;
+        const int lo = part * P;
+        const int hi = min(n, lo + P);
+        const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
+        math.begin(p, q_next);
+        const int4 it_after = item_at(j + 2);
+        if (it_next.x >= 0) math.load_q(p, it_next.x, it_next.y, q_next);
+        bool bad = false;
+        if (!aborted) {
+            const int first = t0 + ((warp - t0 % W) + W) % W;   // this warp's first tile of the item
+            for (int t = first; t < t0 + ntiles; t += W) {
+                const int stage = t % STAGES;
+                const bool got = mbar_wait(smem_addr(&full[stage]), (t / STAGES) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    aborted = true;
+                    break;
+                }
+                if (stage_bad[stage]) {
+                    bad = true;
+                } else {
+                    const int valid = min(kTileRows, hi - (lo + kTileRows * (t - t0)));
+                    const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
+                    math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
+            }
+        }
+        it = it_next;
+        it_next = it_after;
+        t0 += ntiles;
+        float* buf = merge + (j & 1) * (W * Smem::kState);
+        math.write_state(buf + warp * Smem::kState, lane);
+        if (lane == 0) {
+            warp_bad[(j & 1) * W + warp] = bad;
+            if (aborted) {
+                abort_flag[0] = 1;
+                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+            }
+        }
+        named_barrier(1, W * 32);
+        if (abort_flag[0]) break;           // read after the barrier: one decision for all warps
+        bool any_bad = false;
+#pragma unroll
+        for (int w = 0; w < W; ++w) any_bad |= warp_bad[(j & 1) * W + w] != 0;
+        if (any_bad) continue;              // flagged by the producer; output left unspecified
+        const int nparts = (n + P - 1) / P;
+        const int qh0 = h * G;
+        for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
+            const int g = idx / D;
+            const int d = idx - g * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; ++w) M = fmaxf(M, buf[w * Smem::kState + g]);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float* sw = buf + w * Smem::kState;
+                const float cw = fast_exp2(sw[g] - M);
+                L = fmaf(cw, sw[G + g], L);
+                O = fmaf(cw, sw[2 * G + g * D + d], O);
+            }
+            const size_t row = static_cast<size_t>(s) * p.num_heads + qh0 + g;
+            if (nparts == 1) {
+                ElemTraits<T>::store(static_cast<T*>(p.out) + row * D + d, O / L);
+            } else {
+                const size_t slot = row * p.max_parts + part;
+                p.part_o[slot * D + d] = O;
+                if (d == 0) {
+                    p.part_ml[2 * slot] = M;
+                    p.part_ml[2 * slot + 1] = L;
+                }
+            }
+        }
+    }
+}
+
+// Host-side launch of one persistent instance: as many CTAs as fit on
+// sm_count SMs, programmatic dependent launch on the stream.
+template <class Math, int D, int G, int W, int STAGES>
+cudaError_t launch_stream_instance(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const DecodeParams& p, int sm_count, cudaStream_t stream) {
+    using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D>;
+    auto kernel = decode_stream_kernel<Math, D, G, W, STAGES>;
+    const int smem = static_cast<int>(Smem::kBytes);
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (W + 1) * 32, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count * per_sm));
+    cfg.blockDim = dim3((W + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,29 +1,18 @@
-// pa_decode_tma.cuh -- paged decode attention with a TMA tile ring.
+// pa_tile_math.cuh -- the per-tile math of the paged decode kernels.
 //
-// Work item: one (sequence s, KV head h, partition) of at most partition_size
-// rows. One CTA per work item, W consumer warps plus one producer warp.
+// A tile is 16 consecutive rows of one sequence's K (and V) for one KV head:
+// 16 rows x head_dim of one physical block, staged in shared memory by TMA as
+// 128-byte-wide boxes with the 128-byte swizzle. A consumer warp folds tiles
+// into an online-softmax state per query head of its group (running max m,
+// running sum l, unnormalised output o, rescaled by 2^(m_old - m_new) when the
+// max grows: the online softmax of "MLSys Engineer -- Inference Systems Q&A",
+// Q4 "How would you write a fused attention kernel?"), accumulating in fp32.
+// Scores are kept in base 2: the score scale is scale * log2(e).
 //
-// Producer: stages the partition's block ids in shared memory, then streams
-// 16-row tiles of K and V (16 rows x head_dim of one physical block and KV
-// head, contiguous in the [block][kv_head][block_size][head_dim] pool) into a
-// ring of STAGES shared-memory stages with 2D TMA loads (128-byte swizzle, so
-// any 8 rows of one 16-byte column land in 8 different bank groups). Row i of
-// the sequence is row (i % block_size) of block block_tables[s][i / block_size]:
-// the paged gather of "MLSys Engineer -- Inference Systems Q&A", Q1.
-//
-// Consumers: warp w takes tiles w, w + W, ... and keeps its own online-softmax
-// state per query head of the group (running max m, running sum l, and an
-// unnormalised output o rescaled by exp(m_old - m_new) when the max grows, as
-// in Q4 "How would you write a fused attention kernel?"), with fp32
-// accumulation throughout. Scores are kept in base 2 (scale * log2 e folded
-// into the score scale). The math of one tile is a policy:
-//   MmaMath   bf16: S^T = K_tile . Q^T and O^T += V_tile^T . P^T as
-//             m16n8k16 tensor-core MMAs (tokens, then head-dim rows, as M;
-//             the G <= 8 query heads of the group as N);
+//   MmaMath   bf16: S^T = K_tile . Q^T and O^T += V_tile^T . P^T as m16n8k16
+//             tensor-core MMAs (tokens, then head-dim rows, as M; the G <= 8
+//             query heads of the group as N), softmax on the accumulators;
 //   SimtMath  fp32 or bf16: CUDA-core dot products and warp-shuffle sums.
-// At the end the W warp states are merged through shared memory and written
-// either as the final normalised output (one partition) or as a partition
-// partial (max, sum, unnormalised output) for the combine kernel.
 #pragma once
 
 #include <cfloat>
@@ -109,25 +98,41 @@ struct MmaMath {
     static constexpr int kSteps = D / 16;
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
 
-    uint32_t qb[kSteps][2];
+    // q of the group as the B operand of the QK MMA (heads >= G are zero).
+    struct QRegs {
+        uint32_t b[kSteps][2];
+    };
+
+    QRegs qb;
     float o[kSteps][4];
     float m[2], l[2];
     int gid, t4;
 
-    __device__ __forceinline__ void init(const DecodeParams& p, int s, int h, int lane) {
+    __device__ __forceinline__ void setup(int lane) {
         gid = lane >> 2;
         t4 = lane & 3;
+    }
+
+    // Load q of (sequence s, KV head h); may run one item ahead of begin().
+    __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, QRegs& r) const {
         // Lanes of padded heads (gid >= G) keep a valid row pointer and load nothing.
         const int head = h * G + (gid < G ? gid : G - 1);
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
             static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_heads + head) * D);
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
-            qb[kk][0] = gid < G ? __ldg(qrow + 8 * kk + t4) : 0u;
-            qb[kk][1] = gid < G ? __ldg(qrow + 8 * kk + 4 + t4) : 0u;
+            r.b[kk][0] = gid < G ? __ldg(qrow + 8 * kk + t4) : 0u;
+            r.b[kk][1] = gid < G ? __ldg(qrow + 8 * kk + 4 + t4) : 0u;
+        }
+    }
+
+    // Start an item: take its q and clear the softmax state.
+    __device__ __forceinline__ void begin(const DecodeParams&, const QRegs& r) {
+        qb = r;
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk)
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[kk][i] = 0.f;
-        }
         m[0] = m[1] = -INFINITY;
         l[0] = l[1] = 0.f;
     }
@@ -144,7 +149,7 @@ struct MmaMath {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(swizzled(kbase + (kk >> 2) * kBoxBytes, r, 2 * (kk & 3) + (mi >> 1)),
                         a0, a1, a2, a3);
-                mma_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                mma_16816(c, a0, a1, a2, a3, qb.b[kk][0], qb.b[kk][1]);
             }
         }
 #pragma unroll
@@ -262,25 +267,57 @@ struct SimtMath {
     static constexpr int kPasses = kTileRows / kRpp;
     static constexpr int kSub = kPasses < 8 ? kPasses : 8;  // passes per softmax sub-step
 
+    // This lane's chunk of q for every head of the group, scaled to base 2.
+    // It is prefetched one item ahead only when small; otherwise begin()
+    // loads it (the extra registers would spill).
+    static constexpr bool kPrefetch = G * kEpc <= 32;
+    struct QRegs {
+        float f[kPrefetch ? G : 1][kPrefetch ? kEpc : 1];
+        int s, h;
+    };
+
     float qf[G][kEpc];
     float o[G][kEpc];
     float m[G], l[G];
     int rr, ch;
 
-    __device__ __forceinline__ void init(const DecodeParams& p, int s, int h, int lane) {
+    __device__ __forceinline__ void setup(int lane) {
         rr = lane / kLpr;
         ch = lane % kLpr;
+    }
+
+    __device__ __forceinline__ void load_rows(const DecodeParams& p, int s, int h,
+                                              float (&dst)[G][kEpc]) const {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const T* qrow = static_cast<const T*>(p.q) +
                             (static_cast<size_t>(s) * p.num_heads + h * G + g) * D;
             const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow) + ch);
-            E::unpack(raw, qf[g]);
+            E::unpack(raw, dst[g]);
 #pragma unroll
-            for (int e = 0; e < kEpc; ++e) {
-                qf[g][e] *= p.scale_log2;
-                o[g][e] = 0.f;
-            }
+            for (int e = 0; e < kEpc; ++e) dst[g][e] *= p.scale_log2;
+        }
+    }
+
+    __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, QRegs& r) const {
+        r.s = s;
+        r.h = h;
+        if constexpr (kPrefetch) load_rows(p, s, h, r.f);
+    }
+
+    __device__ __forceinline__ void begin(const DecodeParams& p, const QRegs& r) {
+        if constexpr (kPrefetch) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < kEpc; ++e) qf[g][e] = r.f[g][e];
+        } else {
+            load_rows(p, r.s, r.h, qf);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int e = 0; e < kEpc; ++e) o[g][e] = 0.f;
             m[g] = -INFINITY;
             l[g] = 0.f;
         }
@@ -380,221 +417,5 @@ struct SimtMath {
         }
     }
 };
-
-// ---------------------------------------------------------------------------
-// The kernel.
-// ---------------------------------------------------------------------------
-template <int W, int STAGES, typename Geom, int G, int D>
-struct DecodeSmem {
-    static constexpr int kRing = STAGES * Geom::kStageBytes;
-    static constexpr int kState = 2 * G + G * D;
-    static_assert(W * kState * 4 <= kRing, "the merge scratch reuses the ring");
-    // align slack + ring + full/empty barriers + flags + block ids
-    static size_t bytes(int partition_size) {
-        return 1024 + kRing + 16 * STAGES + 4 * 4 + 4 * (partition_size / kTileRows + 2);
-    }
-};
-
-template <typename T>
-__device__ __forceinline__ void write_zero_rows(const DecodeParams& p, int s, int h, int G, int D) {
-    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.num_heads + h * G) * D;
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) ElemTraits<T>::store(out + i, 0.f);
-}
-
-// Stage ownership: tile t lives in stage t % STAGES and is consumed by warp
-// t % W. With STAGES a multiple of W every stage belongs to one warp, which
-// waits on its uses in order, so a waiter is never more than one phase ahead
-// of the barrier it polls. (A parity wait cannot tell phase u from phase u+2:
-// if a stage were shared between warps, a fast warp could see the stage's
-// previous phase as its own and consume a tile that has not landed.)
-template <class Math, int D, int G, int W, int STAGES>
-__global__ void __launch_bounds__((W + 1) * 32)
-decode_tma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-    static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
-    using T = typename Math::T;
-    using Geom = typename Math::Geom;
-    using Smem = DecodeSmem<W, STAGES, Geom, G, D>;
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + Smem::kRing);
-    uint64_t* empty = full + STAGES;
-    volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(empty + STAGES);
-    // flags[0]: bad block id seen; flags[1]: producer gave up; flags[2]: a consumer gave up
-    int32_t* s_blk = reinterpret_cast<int32_t*>(empty + STAGES) + 4;
-
-    const int bh = p.num_seqs * p.num_kv_heads;
-    const int part = blockIdx.x / bh;
-    const int rem = blockIdx.x - part * bh;
-    const int s = rem / p.num_kv_heads;
-    const int h = rem - s * p.num_kv_heads;
-    const int n = __ldg(p.context_lens + s);
-    if (n < 0 || n > p.context_cap) {
-        if (threadIdx.x == 0 && part == 0 && h == 0) raise_error(p.error_word, PA_DEVERR_CONTEXT);
-        return;
-    }
-    const int P = p.partition_size;
-    const int lo = part * P;
-    if (n == 0) {
-        if (part == 0) write_zero_rows<T>(p, s, h, G, D);
-        return;
-    }
-    if (lo >= n) return;
-    const int hi = min(n, lo + P);
-    const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
-    const int nparts = (n + P - 1) / P;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int bs = p.block_size;
-    const int b0 = lo / bs;
-    const int nblk = (hi - 1) / bs - b0 + 1;
-
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(smem_addr(&full[i]), 1);
-            mbar_init(smem_addr(&empty[i]), 1);
-        }
-        flags[1] = 0;
-        flags[2] = 0;
-        mbar_init_fence();
-    }
-    Math math;
-    if (warp == W) {
-        bool bad = false;
-        const int32_t* bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq + b0;
-        for (int j = lane; j < nblk; j += 32) {
-            const int id = __ldg(bt + j);
-            bad |= (id < 0) | (id >= p.num_blocks);
-            s_blk[j] = id;
-        }
-        bad = __any_sync(0xffffffffu, bad);
-        if (lane == 0) {
-            flags[0] = bad ? 1 : 0;
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
-    } else {
-        math.init(p, s, h, lane);
-    }
-    __syncthreads();
-    if (flags[0]) {
-        if (threadIdx.x == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
-        return;
-    }
-
-    const uint32_t ring_addr = smem_addr(ring);
-    if (warp == W) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            int issued = 0;
-            bool ok = true;
-            for (int t = 0; t < ntiles; ++t) {
-                const int stage = t % STAGES;
-                if (t >= STAGES && !mbar_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (flags[2]) break;
-                const int tok = lo + kTileRows * t;
-                const int id = s_blk[tok / bs - b0];
-                const int row = (id * p.num_kv_heads + h) * bs + (tok % bs);
-                const uint32_t fb = smem_addr(&full[stage]);
-                const uint32_t dst = ring_addr + stage * Geom::kStageBytes;
-                mbar_arrive_expect_tx(fb, Geom::kStageBytes);
-#pragma unroll
-                for (int b = 0; b < Geom::kBoxes; ++b)
-                    tma_load_2d(dst + b * kBoxBytes, &tmap_k, fb, b * Geom::kBoxElems, row);
-#pragma unroll
-                for (int b = 0; b < Geom::kBoxes; ++b)
-                    tma_load_2d(dst + Geom::kTileBytes + b * kBoxBytes, &tmap_v, fb,
-                                b * Geom::kBoxElems, row);
-                issued = t + 1;
-            }
-            if (!ok) {
-                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
-                flags[1] = 1;
-            }
-            // Copies still in flight must land before this CTA's shared memory
-            // can be released: wait (bounded) for the last issued stages.
-            for (int t = issued > STAGES ? issued - STAGES : 0; t < issued; ++t)
-                (void)mbar_wait(smem_addr(&full[t % STAGES]), (t / STAGES) & 1);
-        }
-        return;
-    }
-
-    // ---------------- consumers ----------------
-    bool ok = true;
-    for (int t = warp; t < ntiles; t += W) {
-        const int stage = t % STAGES;
-        const bool got = mbar_wait(smem_addr(&full[stage]), (t / STAGES) & 1);
-        if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-        }
-        const int valid = min(kTileRows, hi - (lo + kTileRows * t));
-        const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
-        math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
-    }
-    if (!ok && lane == 0) {
-        raise_error(p.error_word, PA_DEVERR_TIMEOUT);
-        flags[2] = 1;
-    }
-    named_barrier(1, W * 32);
-    if (flags[2]) return;   // copies may still land in the ring: no merge
-
-    float* state = reinterpret_cast<float*>(ring);
-    math.write_state(state + warp * Smem::kState, lane);
-    named_barrier(1, W * 32);
-
-    const int qh0 = h * G;
-    for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-        const int g = idx / D;
-        const int d = idx - g * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, state[w * Smem::kState + g]);
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-            const float* sw = state + w * Smem::kState;
-            const float cw = fast_exp2(sw[g] - M);
-            L = fmaf(cw, sw[G + g], L);
-            O = fmaf(cw, sw[2 * G + g * D + d], O);
-        }
-        const size_t row = static_cast<size_t>(s) * p.num_heads + qh0 + g;
-        if (nparts == 1) {
-            ElemTraits<T>::store(static_cast<T*>(p.out) + row * D + d, O / L);
-        } else {
-            const size_t slot = row * p.max_parts + part;
-            p.part_o[slot * D + d] = O;
-            if (d == 0) {
-                p.part_ml[2 * slot] = M;
-                p.part_ml[2 * slot + 1] = L;
-            }
-        }
-    }
-}
-
-// Host-side launch of one instance.
-template <class Math, int D, int G, int W, int STAGES>
-cudaError_t launch_tma_instance(const CUtensorMap& tk, const CUtensorMap& tv,
-                                const DecodeParams& p, cudaStream_t stream) {
-    using Smem = DecodeSmem<W, STAGES, typename Math::Geom, G, D>;
-    auto kernel = decode_tma_kernel<Math, D, G, W, STAGES>;
-    const size_t smem = Smem::bytes(p.partition_size);
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    const long long grid = static_cast<long long>(p.max_parts) * p.num_seqs * p.num_kv_heads;
-    if (grid <= 0) return cudaSuccess;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kernel<<<static_cast<unsigned>(grid), (W + 1) * 32, smem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
-}
 
 }  // namespace pa

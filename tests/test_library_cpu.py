@@ -58,14 +58,27 @@ def test_decode_rejects_bad_arguments(lib, kw, status):
     assert _decode(lib, **ptrs, **kw) == status
 
 
+def workspace_formula(B, hq, d, mcl, P=512):
+    """The documented workspace layout: a 256-byte header, one 16-byte work
+    item per (sequence, head, partition) for at most 4096 sequences, then
+    8 + 4 * d bytes of partials per (sequence, head, partition) when a sequence
+    can span more than one partition."""
+    if B <= 0:
+        return 0
+    parts = max(1, -(-mcl // P))
+    seqs = min(B, 4096)
+    units = seqs * hq * parts
+    return 256 + 16 * units + ((8 + 4 * d) * units if parts > 1 else 0)
+
+
 def test_decode_rejects_misaligned_and_missing_workspace(lib):
     ptrs = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, out=FAKE)
     assert _decode(lib, **{**ptrs, "q": FAKE + 8}) == pa.PA_ERR_INVALID_ARG
-    # 600 rows need two partitions of 512: workspace required
     assert _decode(lib, **ptrs, mcl=600, mb=40) == pa.PA_ERR_WORKSPACE
     need = lib.pa_decode_workspace_size(4, 8, 128, 600)
-    assert need == 4 * 8 * 2 * 130 * 4
+    assert need == workspace_formula(4, 8, 128, 600)
     assert _decode(lib, **ptrs, mcl=600, mb=40, ws=FAKE, wsb=need - 4) == pa.PA_ERR_WORKSPACE
+    assert _decode(lib, **ptrs, mcl=600, mb=40, ws=FAKE + 8, wsb=need) == pa.PA_ERR_WORKSPACE
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -87,9 +100,11 @@ def test_append_rejects_bad_arguments(lib):
 
 
 def test_workspace_size_formula(lib):
-    assert lib.pa_decode_workspace_size(8, 32, 128, 512) == 0
-    assert lib.pa_decode_workspace_size(8, 32, 128, 100_000) == 8 * 32 * 196 * 130 * 4
-    assert lib.pa_decode_workspace_size_ex(2, 4, 64, 100, 16) == 2 * 4 * 7 * 66 * 4
+    for args in [(8, 32, 128, 512), (8, 32, 128, 100_000), (128, 32, 128, 7811), (1, 1, 64, 0),
+                 (5000, 8, 64, 1000)]:
+        assert lib.pa_decode_workspace_size(*args) == workspace_formula(*args), args
+    assert lib.pa_decode_workspace_size(0, 32, 128, 512) == 0
+    assert lib.pa_decode_workspace_size_ex(2, 4, 64, 100, 16) == workspace_formula(2, 4, 64, 100, 16)
 
 
 def test_python_binding_has_no_cpu_fallback():
