@@ -3,6 +3,7 @@
 // the host and only enqueues work on the caller's stream.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -237,11 +238,16 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
         pa_status ps = make_pool_map(&tk, k_cache, dtype, head_dim, rows);
         if (ps == PA_OK) ps = make_pool_map(&tv, v_cache, dtype, head_dim, rows);
         if (ps != PA_OK) return ps;
+        static std::atomic<int> cached_sms[pa::kMaxDevices];
         int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            sm_count <= 0)
-            return PA_ERR_CUDA;
+        if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+        sm_count = dev < pa::kMaxDevices ? cached_sms[dev].load(std::memory_order_relaxed) : 0;
+        if (sm_count <= 0) {
+            if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sm_count <= 0)
+                return PA_ERR_CUDA;
+            if (dev < pa::kMaxDevices) cached_sms[dev].store(sm_count, std::memory_order_relaxed);
+        }
     }
     const size_t es = static_cast<size_t>(elem_bytes(dtype));
     // Batches above kPlanMaxSeqs sequences run as consecutive launches over

@@ -14,8 +14,8 @@
 // (m_p, l_p, o_p) -- running max (base 2), sum of exp2(s - m_p), unnormalised
 // output -- the result is sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with
 // M = max_p m_p: the rescale rule of the online softmax in Q4 "How would you
-// write a fused attention kernel?", applied once per partition, in ascending
-// partition order.
+// write a fused attention kernel?", applied per partition. The summation
+// order is fixed by the sequence's own partition count.
 #include <cfloat>
 
 #include "pa_common.cuh"
@@ -150,13 +150,26 @@ decode_generic_kernel(const DecodeParams p, int group) {
     }
 }
 
-constexpr int kCombineThreads = 128;
+constexpr int kCombineChunk = 32;          // partitions per warp per pass (one per lane)
+constexpr int kCombineMaxWarps = 16;
+constexpr int kCombineMaxElems = kMaxHeadDim / 32;   // output elements per lane
+constexpr int kCombineBatch = 8;           // partitions whose o rows are loaded before use
 
-template <typename T>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodeParams p) {
-    extern __shared__ float wts[];            // [max_parts] rescale weights
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ float total;
+// Warps used for a sequence of np partitions: warp w takes chunks w, w + nw,
+// ... of 32 consecutive partitions. Depends on np only, so a sequence's
+// summation order does not depend on the rest of the batch.
+__host__ __device__ __forceinline__ int combine_warps(int np) {
+    const int w = (np + kCombineChunk - 1) / kCombineChunk;
+    return w < kCombineMaxWarps ? w : kCombineMaxWarps;
+}
+
+// One CTA per (sequence, query head) of a sequence longer than one partition.
+// Each warp merges its chunks (lane q holds partition q's max and sum; the o
+// rows are loaded kCombineBatch partitions at a time), then the warp results
+// are merged in warp order.
+template <typename T, int E>
+__global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const DecodeParams p) {
+    extern __shared__ float sm[];                // [nw][2 + head_dim]
     // Launched as a programmatic dependent of the decode kernel: wait for its
     // partials before reading anything.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -166,44 +179,66 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const DecodePa
     const int P = p.partition_size;
     if (n <= P || n > p.context_cap) return;   // one partition (written directly) or flagged
     const int np = (n + P - 1) / P;
+    const int nw = combine_warps(np);
+    const int D = p.head_dim;
     const size_t row = static_cast<size_t>(s) * p.num_heads + qh;
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row * p.max_parts;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += blockDim.x) mx = fmaxf(mx, ml[i].x);
-    mx = warp_max(mx);
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    float M = red[0];
-#pragma unroll
-    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < np; i += blockDim.x) {
-        const float2 v = ml[i];
-        const float c = fast_exp2(v.x - M);
-        wts[i] = c;
-        sum = fmaf(c, v.y, sum);
-    }
-    sum = warp_sum(sum);
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
-        total = L;
-    }
-    __syncthreads();
-    const float inv_l = 1.f / total;
-    const int D = p.head_dim;
     const float* o = p.part_o + row * p.max_parts * static_cast<size_t>(D);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < nw) {
+        float M = -INFINITY, L = 0.f;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (int c0 = warp * kCombineChunk; c0 < np; c0 += nw * kCombineChunk) {
+            const int cnt = min(kCombineChunk, np - c0);
+            const float2 v = lane < cnt ? ml[c0 + lane] : make_float2(-INFINITY, 0.f);
+            const float Mc = fmaxf(M, warp_max(v.x));
+            const float w = lane < cnt ? fast_exp2(v.x - Mc) : 0.f;
+            const float rescale = fast_exp2(M - Mc);          // 0 on the first chunk
+            L = L * rescale + warp_sum(w * v.y);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] *= rescale;
+            M = Mc;
+            for (int i = 0; i < cnt; i += kCombineBatch) {
+                float ov[kCombineBatch][E];
+#pragma unroll
+                for (int k = 0; k < kCombineBatch; ++k)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int d = lane + 32 * e;
+                        ov[k][e] = (i + k < cnt && d < D)
+                                       ? o[static_cast<size_t>(c0 + i + k) * D + d] : 0.f;
+                    }
+#pragma unroll
+                for (int k = 0; k < kCombineBatch; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, (i + k) & 31);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, ov[k][e], acc[e]);
+                }
+            }
+        }
+        float* st = sm + warp * (D + 2);
+        if (lane == 0) {
+            st[0] = M;
+            st[1] = L;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane + 32 * e;
+            if (d < D) st[2 + d] = acc[e];
+        }
+    }
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, sm[w * (D + 2)]);
+    float L = 0.f;
+    for (int w = 0; w < nw; ++w) L = fmaf(fast_exp2(sm[w * (D + 2)] - M), sm[w * (D + 2) + 1], L);
     T* out = static_cast<T*>(p.out) + row * D;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float acc = 0.f;
-        for (int i = 0; i < np; ++i) acc = fmaf(wts[i], o[static_cast<size_t>(i) * D + d], acc);
-        ElemTraits<T>::store(out + d, acc * inv_l);
+        float a = 0.f;
+        for (int w = 0; w < nw; ++w) a = fmaf(fast_exp2(sm[w * (D + 2)] - M), sm[w * (D + 2) + 2 + d], a);
+        ElemTraits<T>::store(out + d, a / L);
     }
 }
 
@@ -241,10 +276,11 @@ cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStr
 
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
     if (p.max_parts <= 1 || p.num_seqs == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(p.max_parts) * sizeof(float);
+    const int warps = combine_warps(p.max_parts);   // enough for the longest sequence
+    const size_t smem = static_cast<size_t>(warps) * (p.head_dim + 2) * sizeof(float);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_heads, p.num_seqs);
-    cfg.blockDim = dim3(kCombineThreads);
+    cfg.blockDim = dim3(32 * warps);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -252,16 +288,16 @@ cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err;
-    if (dtype == PA_DTYPE_BF16) {
-        err = cudaFuncSetAttribute(combine_kernel<__nv_bfloat16>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
-    } else {
-        err = cudaFuncSetAttribute(combine_kernel<float>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
-    }
+    // Output elements per lane: exact for head dims 64 and 128, else the maximum.
+    auto pick = [&](auto tag) -> cudaError_t {
+        using T = decltype(tag);
+        // At most 16 warps x (256 + 2) floats: within the default shared-memory limit.
+        auto run = [&](auto kernel) -> cudaError_t { return cudaLaunchKernelEx(&cfg, kernel, p); };
+        if (p.head_dim == 128) return run(combine_kernel<T, 4>);
+        if (p.head_dim == 64) return run(combine_kernel<T, 2>);
+        return run(combine_kernel<T, kCombineMaxElems>);
+    };
+    cudaError_t err = dtype == PA_DTYPE_BF16 ? pick(__nv_bfloat16{}) : pick(float{});
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

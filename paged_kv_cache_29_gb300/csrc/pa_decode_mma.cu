@@ -8,12 +8,13 @@ namespace pa {
 namespace {
 constexpr int kWarps = 4;     // consumer warps per CTA
 constexpr int kStages = 4;    // ring depth, a multiple of kWarps: 4 x (K + V) tiles = 32 KiB at d=128
+constexpr int kMinCtasPerSm = 4;   // four rings per SM (register budget 96 per thread)
 
 template <int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                 int sm_count, cudaStream_t stream) {
-    return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages>(tk, tv, p, sm_count,
-                                                                          stream);
+    return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages, kMinCtasPerSm>(
+        tk, tv, p, sm_count, stream);
 }
 
 template <int D>

@@ -35,6 +35,8 @@
 // global read of the plan, the block tables, q and the KV pool comes after it.
 #pragma once
 
+#include <atomic>
+
 #include "pa_tile_math.cuh"
 
 namespace pa {
@@ -69,7 +71,7 @@ __device__ __forceinline__ int snake_item(int c, int j, int C) {
     return j * C + ((j & 1) ? (C - 1 - c) : c);
 }
 
-template <int W, int STAGES, typename Geom, int G, int D>
+template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes>
 struct StreamSmem {
     static constexpr int kRing = STAGES * Geom::kStageBytes;
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
@@ -77,17 +79,20 @@ struct StreamSmem {
     static constexpr int kBarriers = 2 * STAGES * 8;
     static constexpr int kFlags = (STAGES + 2 * W + 8) * 4;
     static constexpr int kIds = 2 * kMaxItemBlocks * 4;
-    static constexpr size_t kBytes = 1024 + kRing + kMerge + kBarriers + kFlags + kIds;
+    static constexpr size_t kQBuf = 2 * Math_kQBufBytes;
+    static constexpr size_t kBytes = 1024 + kRing + kMerge + kBarriers + kFlags + kIds + kQBuf;
 };
 
-template <class Math, int D, int G, int W, int STAGES>
-__global__ void __launch_bounds__((W + 1) * 32)
+// MIN_CTAS: resident CTAs per SM the register budget is sized for (see
+// "Sizing" above).
+template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
+__global__ void __launch_bounds__((W + 1) * 32, MIN_CTAS)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
-    using Smem = StreamSmem<W, STAGES, Geom, G, D>;
+    using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes>;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -100,6 +105,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     volatile int32_t* abort_flag = warp_bad + 2 * W;
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
         reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
+    uint8_t* qbuf = reinterpret_cast<uint8_t*>(ids_buf + 2 * kMaxItemBlocks);   // [2][kQBufBytes]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -168,8 +174,15 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int hi = min(cur.w, lo + P);
             const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
             if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
-            for (int tt = 0; tt < ntiles; ++tt, ++t) {
+            // The item's tiles are padded with data-less slots up to a multiple
+            // of W, so that every item starts at a stream index divisible by W
+            // and warp w always takes tiles w, w + W, ... of the item: the
+            // rounding of an item's result never depends on what the CTA
+            // streamed before it.
+            const int span = ((ntiles + W - 1) / W) * W;
+            for (int tt = 0; tt < span; ++tt, ++t) {
                 const int tok = lo + kTileRows * tt;
+                const bool data = tt < ntiles && !cur_bad;
                 const int stage = t % STAGES;
                 const uint32_t fb = smem_addr(&full[stage]);
                 if (lane == 0) {
@@ -179,10 +192,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         ok = false;
                     } else {
                         stage_bad[stage] = cur_bad;
-                        if (cur_bad)
-                            mbar_arrive(fb);          // no data: consumers skip the tile
-                        else
+                        if (data)
                             mbar_arrive_expect_tx(fb, Geom::kStageBytes);
+                        else
+                            mbar_arrive(fb);          // no data: consumers skip the slot
                         issued = t + 1;
                     }
                 }
@@ -191,7 +204,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // Lane 0 copies the K tile, lane 1 the V tile: one 3D box each
                 // (all 128-byte column halves of 16 rows), issued after lane
                 // 0's expect_tx (ordered by the shuffle above).
-                if (!cur_bad && lane < 2) {
+                if (data && lane < 2) {
                     const int id = ids[tok / bs - b0];
                     const int row = (id * p.num_kv_heads + cur.y) * bs + (tok % bs);
                     const uint32_t dst = ring_addr + stage * Geom::kStageBytes +
@@ -230,21 +243,39 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int4 it = item_at(0);
     int4 it_next = item_at(1);
     typename Math::QRegs q_next;
-    if (it.x >= 0) math.load_q(p, it.x, it.y, q_next);
-    int t0 = 0;                 // stream index of the current item's first tile
+    if constexpr (Math::kQInSmem) {
+        // q of item 0 now, then always one item ahead, copied by warp 0.
+        if (warp == 0 && it.x >= 0) {
+            math.stage_q(p, it.x, it.y, smem_addr(qbuf), lane);
+            cp_async_wait_all();
+        }
+        named_barrier(1, W * 32);
+    } else {
+        if (it.x >= 0) math.load_q(p, it.x, it.y, q_next);
+    }
+    int t0 = 0;                 // stream index of the current item's first tile (a multiple of W)
     bool aborted = false;
     for (int j = 0; it.x >= 0; ++j) {
         const int s = it.x, h = it.y, part = it.z, n = it.w;
         const int lo = part * P;
         const int hi = min(n, lo + P);
         const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
-        math.begin(p, q_next);
         const int4 it_after = item_at(j + 2);
-        if (it_next.x >= 0) math.load_q(p, it_next.x, it_next.y, q_next);
+        if constexpr (Math::kQInSmem) {
+            math.begin_staged(qbuf + (j & 1) * Math::kQBufBytes);
+            // The other buffer was last read when item j - 1 began, before the
+            // previous item's closing barrier.
+            if (warp == 0 && it_next.x >= 0)
+                math.stage_q(p, it_next.x, it_next.y, smem_addr(qbuf + ((j + 1) & 1) * Math::kQBufBytes),
+                             lane);
+        } else {
+            math.begin(p, q_next);
+            if (it_next.x >= 0) math.load_q(p, it_next.x, it_next.y, q_next);
+        }
+        const int span = ((ntiles + W - 1) / W) * W;   // padded as the producer pads
         bool bad = false;
         if (!aborted) {
-            const int first = t0 + ((warp - t0 % W) + W) % W;   // this warp's first tile of the item
-            for (int t = first; t < t0 + ntiles; t += W) {
+            for (int t = t0 + warp; t < t0 + span; t += W) {
                 const int stage = t % STAGES;
                 const bool got = mbar_wait(smem_addr(&full[stage]), (t / STAGES) & 1);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -253,7 +284,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 if (stage_bad[stage]) {
                     bad = true;
-                } else {
+                } else if (t - t0 < ntiles) {
                     const int valid = min(kTileRows, hi - (lo + kTileRows * (t - t0)));
                     const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
                     math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
@@ -264,9 +295,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         it = it_next;
         it_next = it_after;
-        t0 += ntiles;
+        t0 += span;
         float* buf = merge + (j & 1) * (W * Smem::kState);
         math.write_state(buf + warp * Smem::kState, lane);
+        if constexpr (Math::kQInSmem) {
+            if (warp == 0) cp_async_wait_all();   // next item's q is visible after the barrier
+        }
         if (lane == 0) {
             warp_bad[(j & 1) * W + warp] = bad;
             if (aborted) {
@@ -313,18 +347,27 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 // Host-side launch of one persistent instance: as many CTAs as fit on
 // sm_count SMs, programmatic dependent launch on the stream.
-template <class Math, int D, int G, int W, int STAGES>
+template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
 cudaError_t launch_stream_instance(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecodeParams& p, int sm_count, cudaStream_t stream) {
-    using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D>;
-    auto kernel = decode_stream_kernel<Math, D, G, W, STAGES>;
+    using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D, Math::kQBufBytes>;
+    auto kernel = decode_stream_kernel<Math, D, G, W, STAGES, MIN_CTAS>;
     const int smem = static_cast<int>(Smem::kBytes);
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The shared-memory attribute and the resulting CTAs per SM are set up
+    // once per device and instance.
+    static std::atomic<int> cached_per_sm[kMaxDevices];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (W + 1) * 32, smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    int per_sm = dev < kMaxDevices ? cached_per_sm[dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm == 0) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (W + 1) * 32, smem);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        if (dev < kMaxDevices) cached_per_sm[dev].store(per_sm, std::memory_order_relaxed);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count * per_sm));
     cfg.blockDim = dim3((W + 1) * 32);

@@ -65,6 +65,7 @@ size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
 
 constexpr int kMaxHeadDim = 256;
+constexpr int kMaxDevices = 64;      // devices whose per-kernel launch set-up is cached
 constexpr int kDefaultPartition = 512;
 
 }  // namespace pa

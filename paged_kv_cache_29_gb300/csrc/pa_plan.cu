@@ -13,6 +13,8 @@
 //
 // It also writes the zero output rows of empty sequences and flags context
 // lengths outside [0, max_context_len] (those sequences get no items).
+#include <atomic>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -20,7 +22,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 constexpr int kBuckets = 16;
 
 __device__ __forceinline__ void grid_dependency_wait_() {
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeParams p
     int* pf = lens + B;          // [B + 1] exclusive prefix of full partitions
     int* rank = pf + B + 1;      // [B] position among partial items
     __shared__ int count[kBuckets], cursor[kBuckets];
-    __shared__ int warp_sum[kPlanThreads / 32];
+    __shared__ int warp_sum[32];
     __shared__ int partials;
     const int P = p.partition_size;
     const int Hkv = p.num_kv_heads;
@@ -82,14 +84,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeParams p
     if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_sum[lane];
+        int w = lane < (kPlanThreads >> 5) ? warp_sum[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, wi, off);
             if (lane >= off) wi += v;
         }
-        warp_sum[lane] = wi - w;     // exclusive prefix of warp totals
+        if (lane < (kPlanThreads >> 5)) warp_sum[lane] = wi - w;   // exclusive prefix of warp totals
     }
     __syncthreads();
     int run = warp_sum[warp] + incl - local;
@@ -123,19 +125,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const DecodeParams p
 
     const int full_items = pf[B] * Hkv;
     if (tid == 0) p.sched[0] = full_items + partials * Hkv;
-    for (int k = tid; k < full_items; k += blockDim.x) {
-        const int unit = k / Hkv;
-        int lo = 0, hi = B - 1;              // last s with pf[s] <= unit
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pf[mid] <= unit) lo = mid; else hi = mid - 1;
+    // One warp per sequence writes its items: the full partitions at
+    // pf[s] * Hkv (partition-major, KV head fastest), the partial one at its
+    // bucket rank.
+    for (int s = warp; s < B; s += blockDim.x >> 5) {
+        const int n = lens[s];
+        if (n <= 0) continue;
+        const int nfull = n / P;
+        int4* dst = p.items + static_cast<size_t>(pf[s]) * Hkv;
+        for (int i = lane; i < nfull * Hkv; i += 32) dst[i] = make_int4(s, i % Hkv, i / Hkv, n);
+        if (rank[s] >= 0) {
+            int4* pdst = p.items + full_items + static_cast<size_t>(rank[s]) * Hkv;
+            for (int h = lane; h < Hkv; h += 32) pdst[h] = make_int4(s, h, nfull, n);
         }
-        p.items[k] = make_int4(lo, k - unit * Hkv, unit - pf[lo], lens[lo]);
-    }
-    for (int s = tid; s < B; s += blockDim.x) {
-        if (rank[s] < 0) continue;
-        const int base = full_items + rank[s] * Hkv;
-        for (int h = 0; h < Hkv; ++h) p.items[base + h] = make_int4(s, h, lens[s] / P, lens[s]);
     }
     // The next kernel's griddepcontrol.wait covers this grid only: wait for the
     // kernel before this one (the cache append) so that the chain stays whole.
@@ -158,16 +160,24 @@ cudaError_t launch_plan(const DecodeParams& p, pa_dtype dtype, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err;
-    if (dtype == PA_DTYPE_BF16) {
+    // The shared-memory attribute is set once per device, for the largest
+    // batch a launch takes.
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= kMaxDevices || !ready[dev].load(std::memory_order_relaxed)) {
+        const int max_smem = static_cast<int>(plan_smem_bytes(kPlanMaxSeqs));
         err = cudaFuncSetAttribute(plan_kernel<__nv_bfloat16>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, plan_kernel<__nv_bfloat16>, p);
-    } else {
-        err = cudaFuncSetAttribute(plan_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem);
-        if (err == cudaSuccess) err = cudaLaunchKernelEx(&cfg, plan_kernel<float>, p);
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(plan_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       max_smem);
+        if (err != cudaSuccess) return err;
+        if (dev < kMaxDevices) ready[dev].store(1, std::memory_order_relaxed);
     }
+    err = dtype == PA_DTYPE_BF16 ? cudaLaunchKernelEx(&cfg, plan_kernel<__nv_bfloat16>, p)
+                                 : cudaLaunchKernelEx(&cfg, plan_kernel<float>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

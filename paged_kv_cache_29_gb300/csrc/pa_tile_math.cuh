@@ -98,12 +98,15 @@ struct MmaMath {
     static constexpr int kSteps = D / 16;
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
 
-    // q of the group as the B operand of the QK MMA (heads >= G are zero).
-    struct QRegs {
-        uint32_t b[kSteps][2];
-    };
+    // q of the next item is staged in shared memory ([G][D] bf16 rows padded
+    // to D * 2 + 16 bytes, so that the fragment reads below hit 32 different
+    // banks) by one warp with cp.async, instead of being held in registers.
+    static constexpr bool kQInSmem = true;
+    static constexpr int kQRowBytes = D * 2 + 16;
+    static constexpr int kQBufBytes = ((G * kQRowBytes + 127) / 128) * 128;
+    struct QRegs {};
 
-    QRegs qb;
+    uint32_t qb[kSteps][2];
     float o[kSteps][4];
     float m[2], l[2];
     int gid, t4;
@@ -113,26 +116,33 @@ struct MmaMath {
         t4 = lane & 3;
     }
 
-    // Load q of (sequence s, KV head h); may run one item ahead of begin().
-    __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, QRegs& r) const {
-        // Lanes of padded heads (gid >= G) keep a valid row pointer and load nothing.
-        const int head = h * G + (gid < G ? gid : G - 1);
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.num_heads + head) * D);
-#pragma unroll
-        for (int kk = 0; kk < kSteps; ++kk) {
-            r.b[kk][0] = gid < G ? __ldg(qrow + 8 * kk + t4) : 0u;
-            r.b[kk][1] = gid < G ? __ldg(qrow + 8 * kk + 4 + t4) : 0u;
+    // One warp copies q of (sequence s, KV head h) into the staging buffer.
+    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, uint32_t qbuf,
+                                            int lane) const {
+        constexpr int kChunksPerRow = D * 2 / 16;
+        const uint8_t* q = reinterpret_cast<const uint8_t*>(static_cast<const T*>(p.q) +
+                                                            (static_cast<size_t>(s) * p.num_heads + h * G) * D);
+        for (int c = lane; c < G * kChunksPerRow; c += 32) {
+            const int g = c / kChunksPerRow, ch = c - g * kChunksPerRow;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             qbuf + static_cast<uint32_t>(g * kQRowBytes + ch * 16)),
+                         "l"(q + static_cast<size_t>(g) * D * 2 + ch * 16)
+                         : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
-    // Start an item: take its q and clear the softmax state.
-    __device__ __forceinline__ void begin(const DecodeParams&, const QRegs& r) {
-        qb = r;
+    // Start an item: read q's B fragments from the staging buffer and clear
+    // the softmax state.
+    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf) {
 #pragma unroll
-        for (int kk = 0; kk < kSteps; ++kk)
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const uint8_t* r = qbuf + gid * kQRowBytes + (16 * kk + 2 * t4) * 2;
+            qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(r) : 0u;
+            qb[kk][1] = gid < G ? *reinterpret_cast<const uint32_t*>(r + 16) : 0u;
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[kk][i] = 0.f;
+        }
         m[0] = m[1] = -INFINITY;
         l[0] = l[1] = 0.f;
     }
@@ -149,7 +159,7 @@ struct MmaMath {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(swizzled(kbase + (kk >> 2) * kBoxBytes, r, 2 * (kk & 3) + (mi >> 1)),
                         a0, a1, a2, a3);
-                mma_16816(c, a0, a1, a2, a3, qb.b[kk][0], qb.b[kk][1]);
+                mma_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
         }
 #pragma unroll
@@ -271,6 +281,8 @@ struct SimtMath {
     // It is prefetched one item ahead only when small; otherwise begin()
     // loads it (the extra registers would spill).
     static constexpr bool kPrefetch = G * kEpc <= 32;
+    static constexpr bool kQInSmem = false;
+    static constexpr int kQBufBytes = 0;
     struct QRegs {
         float f[kPrefetch ? G : 1][kPrefetch ? kEpc : 1];
         int s, h;

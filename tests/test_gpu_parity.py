@@ -104,9 +104,27 @@ def test_garbage_rows_do_not_leak():
             assert max_abs(out, ref) <= TOL[dtype], kernel
 
 
+def _run_subset(step, dev, idx, kernel):
+    """Decode only the sequences `idx` (in that order) against dev's appended pool."""
+    sub = DeviceStep(wl.DecodeStep(**{**step.__dict__, "q": step.q[idx],
+                                      "block_tables": step.block_tables[idx],
+                                      "context_lens": step.context_lens[idx]}))
+    sub.k_cache.copy_(dev.k_cache)
+    sub.v_cache.copy_(dev.v_cache)
+    sub.decode(kernel, max_context_len=int(step.context_lens[idx].max()))
+    torch.cuda.synchronize()
+    assert sub.error_word() == 0
+    return from_torch(sub.out)
+
+
 def test_batch_invariance_and_determinism():
-    """A sequence's output bits do not depend on the rest of the batch."""
-    step = ragged_step("bf16", 32, 8, 128, seed=9)
+    """A sequence's output bits do not depend on the rest of the batch: run
+    alone, inside a batch large enough that every persistent CTA processes
+    many items, and inside a permuted batch with a 40,000-row sequence."""
+    rng = np.random.default_rng(77)
+    lens = list(rng.integers(1, 3000, size=95)) + [40_000]
+    step = wl.build_step("invariance", lens, 32, 8, 128, seed=21)
+    B = step.num_seqs
     for kernel in ["mma", "simt", "generic"]:
         dev = DeviceStep(step)
         dev.run(kernel)
@@ -114,17 +132,12 @@ def test_batch_invariance_and_determinism():
         dev.decode(kernel)
         torch.cuda.synchronize()
         assert np.array_equal(from_torch(dev.out), batch_out), "not deterministic"
-        for s in [0, 3, 8, 11]:
-            single = DeviceStep(step)
-            single.k_cache.copy_(dev.k_cache)
-            single.v_cache.copy_(dev.v_cache)
-            single.q = dev.q[s:s + 1].contiguous()
-            single.out = torch.empty_like(single.q)
-            single.tables = dev.tables[s:s + 1].contiguous()
-            single.lens = dev.lens[s:s + 1].contiguous()
-            single.decode(kernel, max_context_len=int(step.context_lens[s]))
-            torch.cuda.synchronize()
-            assert np.array_equal(from_torch(single.out)[0], batch_out[s]), (kernel, s)
+        for s in [0, 7, 50, B - 1]:
+            single = _run_subset(step, dev, np.array([s]), kernel)
+            assert np.array_equal(single[0], batch_out[s]), (kernel, s)
+        perm = rng.permutation(B)
+        shuffled = _run_subset(step, dev, perm, kernel)
+        assert np.array_equal(shuffled, batch_out[perm]), kernel
 
 
 def test_block_permutation_is_invisible():
