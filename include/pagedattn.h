@@ -125,6 +125,42 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * batch). */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
 
+/*
+ * pa_decode_noalloc -- pa_decode without a workspace argument. The pages have
+ * no counterpart to this call: it exists for callers that cannot hand the
+ * library a scratch buffer. A host program that links only this library and
+ * the CUDA runtime may have no device allocator of its own to size one per
+ * batch shape; a server that reserves almost all device memory for the paged
+ * pool when it starts may have no room left to allocate per call, and a
+ * cudaMalloc/cudaFree pair per step would stall its decode loop, because
+ * cudaFree waits for the device to go idle.
+ *
+ * Same arguments, layouts and results as pa_decode (same kernels, same
+ * partitioning). The scratch is a device array of PA_NOALLOC_SCRATCH_BYTES
+ * inside the library, created by the CUDA runtime on each device where the
+ * library's modules are loaded; no call allocates device or host memory.
+ *   - Requests whose pa_decode_workspace_size(num_seqs, num_heads, head_dim,
+ *     max_context_len) exceeds PA_NOALLOC_SCRATCH_BYTES return
+ *     PA_ERR_WORKSPACE before anything is enqueued; use pa_decode with a
+ *     caller-provided workspace for those.
+ *   - The first call on a device looks up the scratch's address there (with
+ *     that device current) and caches it: make that first call before any
+ *     stream capture on that device.
+ *   - There is ONE scratch per device. Calls whose work may overlap on the
+ *     GPU (other streams, other host threads, or another pa_decode_noalloc
+ *     call on a stream not ordered after this one) race on it and give wrong
+ *     results. Calls on one stream are ordered and safe.
+ * Returns PA_ERR_CUDA if the scratch's address cannot be obtained.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            float scale, void* out, int num_seqs, int num_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                            int32_t* error_word, struct CUstream_st* stream);
+
 /* Kernel choice for pa_decode_ex (for measurement and tests; pa_decode uses
  * PA_KERNEL_AUTO). PA_KERNEL_MMA needs bf16. */
 typedef enum pa_kernel {

@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_ex.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
                                    ctypes.POINTER(_Options), P]
         L.pa_decode_ex.restype = I
+        L.pa_decode_noalloc.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, P]
+        L.pa_decode_noalloc.restype = I
         L.pa_decode_workspace_size.argtypes = [I, I, I, I]
         L.pa_decode_workspace_size.restype = S
         L.pa_decode_workspace_size_ex.argtypes = [I, I, I, I, I]
@@ -200,3 +202,39 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
                             ctypes.byref(opts), _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode")
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                      max_context_len, error_word=None, stream=None) -> None:
+    """pa_decode on the library's fixed device scratch: no workspace argument
+    and no allocation. Raises PagedAttentionError (PA_ERR_WORKSPACE) when the
+    call needs more than NOALLOC_SCRATCH_BYTES of scratch. Calls that may
+    overlap on the GPU share the one scratch and race."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("q", q, k_cache.dtype, 3)
+    _check_cuda("out", out, k_cache.dtype, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    rc = lib().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d, bs,
+                                 nb, int(block_tables.shape[1]), int(max_context_len),
+                                 _dtype_code(k_cache), _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        what = "pa_decode_noalloc"
+        if rc == PA_ERR_WORKSPACE:
+            what += (f" (needs {need} bytes of scratch, the fixed scratch holds "
+                     f"{NOALLOC_SCRATCH_BYTES}; pass a workspace to pa_decode instead)")
+        raise PagedAttentionError(rc, what)

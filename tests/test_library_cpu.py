@@ -115,3 +115,16 @@ def test_python_binding_has_no_cpu_fallback():
         pa.pa_reshape_and_cache(x, x, torch.zeros(1, dtype=torch.int64),
                                 torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16),
                                 torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16))
+
+
+def test_noalloc_rejects_oversize_requests_on_the_host(lib):
+    """pa_decode_noalloc refuses a call whose scratch need exceeds its fixed
+    scratch before any CUDA call, so this runs without a GPU."""
+    too_big = (128, 32, 128, 1 << 20)
+    assert lib.pa_decode_workspace_size(*too_big) > pa.NOALLOC_SCRATCH_BYTES
+    B, hq, d, mcl = too_big
+    rc = lib.pa_decode_noalloc(None, None, None, None, None, 0.1, None, B, hq, 8, d, 16, 1000,
+                               mcl // 16, mcl, 1, None, None)
+    assert rc == pa.PA_ERR_WORKSPACE
+    # The 8B GQA decode batch (128 sequences up to ~8K rows) fits.
+    assert lib.pa_decode_workspace_size(128, 32, 128, 8192) <= pa.NOALLOC_SCRATCH_BYTES
