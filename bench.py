@@ -435,7 +435,7 @@ def run_native(args) -> dict | None:
                   "is the same step launched through the Python binding",
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode call (plan_kernel + decode_stream_kernel with fused split-K merge)",
+            "kernel": "pa_decode call (plan_kernel, decode_stream_kernel, combine_kernel)",
             "achieved": round(decode_gbs, 2),
             "peak": peak,
             "unit": "GB/s",
