@@ -69,9 +69,10 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // Workspace layout (per launch of at most kPlanMaxSeqs sequences, reused by
 // consecutive launches of one call):
-//   [0, 256)              work-item count
-//   items                 int4 per (sequence, KV head, partition): num_heads
-//                         bounds num_kv_heads
+//   [0, 256)              reserved
+//   items                 int4 per (sequence, KV head, partition), written and
+//                         read by the decode kernel: num_heads bounds
+//                         num_kv_heads
 //   part_ml, part_o       partition partials, only when a sequence can span
 //                         more than one partition
 struct WorkspaceLayout {
@@ -186,7 +187,7 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     const int group = num_heads / num_kv_heads;
     const long long max_parts = max_context_len > 0 ? ceil_div(max_context_len, partition) : 1;
     const long long chunk = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
-    if (max_parts * chunk * num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (max_parts * chunk * num_kv_heads > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
 
     const WorkspaceLayout lay = layout_for(num_seqs, num_heads, head_dim, max_context_len, partition);
     if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
@@ -217,7 +218,6 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
     base.v_cache = v_cache;
     base.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ml_off) : nullptr;
     base.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.o_off) : nullptr;
-    base.sched = reinterpret_cast<int*>(ws);
     base.items = reinterpret_cast<int4*>(ws + lay.items_off);
     base.error_word = error_word;
     base.scale_log2 = scale * kLog2e;
@@ -265,10 +265,8 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
         if (kernel == PA_KERNEL_GENERIC) {
             err = pa::launch_decode_generic(p, dtype, st);
         } else {
-            err = pa::launch_plan(p, dtype, st);
-            if (err == cudaSuccess)
-                err = kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
-                                              : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
+            err = kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
+                                          : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
         }
         if (err == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
         if (err != cudaSuccess) return PA_ERR_CUDA;

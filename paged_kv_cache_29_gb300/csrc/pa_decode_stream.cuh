@@ -1,16 +1,15 @@
 // pa_decode_stream.cuh -- persistent paged decode attention with a TMA tile ring.
 //
 // Work item: one (sequence s, KV head h, partition p) of at most
-// partition_size rows. The plan kernel lists every item of the batch in the
-// workspace (full partitions first, then the partial last partitions, largest
-// first). A fixed set of CTAs (a few per SM) walks that list: CTA c takes
-// items c, 2C-1-c, 2C+c, ... (a snake, so that the per-CTA totals even out)
-// and streams all of their tiles through one ring without stopping between
-// items.
+// partition_size rows. A fixed set of CTAs (a few per SM) shares the items of
+// the launch; each CTA first computes and stores its own items (pa_plan.cuh:
+// full partitions first, then the partial last partitions, largest first,
+// dealt out in a snake) and then streams all of their tiles through one ring
+// without stopping between items.
 //
 // Producer warp: for each item, loads its block ids (one coalesced load,
 // validated against the pool, prefetched one item ahead), then for every
-// 16-row tile issues 2D TMA loads of the K and V tile (16 rows x head_dim of
+// 16-row tile issues 3D TMA loads of the K and V tile (16 rows x head_dim of
 // one physical block and KV head, contiguous in the
 // [block][kv_head][block_size][head_dim] pool) into the next ring stage. Row i
 // of a sequence is row (i % block_size) of block block_tables[s][i /
@@ -30,13 +29,15 @@
 // on its oldest stage); deeper rings in fewer CTAs stream slower. So the
 // kernel runs several small CTAs per SM, each with a short ring.
 //
-// Programmatic dependent launch: everything before griddepcontrol.wait (ring
-// and barrier set-up) may overlap the previous kernel on the stream; every
-// global read of the plan, the block tables, q and the KV pool comes after it.
+// Programmatic dependent launch: only ring and barrier set-up come before
+// griddepcontrol.wait; every global access (context lengths, the work list,
+// block tables, q, the KV pool, the output) comes after it, so a launch never
+// touches memory that the kernel before it on the stream still uses.
 #pragma once
 
 #include <atomic>
 
+#include "pa_plan.cuh"
 #include "pa_tile_math.cuh"
 
 namespace pa {
@@ -66,11 +67,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// CTA c's j-th item in a snake over C CTAs.
-__device__ __forceinline__ int snake_item(int c, int j, int C) {
-    return j * C + ((j & 1) ? (C - 1 - c) : c);
-}
-
 template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes>
 struct StreamSmem {
     static constexpr int kRing = STAGES * Geom::kStageBytes;
@@ -93,6 +89,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     using T = typename Math::T;
     using Geom = typename Math::Geom;
     using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes>;
+    static_assert(Smem::kMerge >= 4 * plan_scratch_ints((W + 1) * 32),
+                  "the plan's scratch lives in the merge area");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -126,9 +124,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     grid_dependency_wait();
     grid_launch_dependents();
 
-    const int total = __ldg(p.sched);
     const int C = gridDim.x;
     const int c = blockIdx.x;
+    // The CTA's work list; its scratch is the merge area, free until the first
+    // item ends. The items are read back with plain (coherent) loads.
+    const int total = plan_cta<T, (W + 1) * 32>(p, c, C, reinterpret_cast<int*>(merge));
+    __syncthreads();
     const int P = p.partition_size;
     const int bs = p.block_size;
     const uint32_t ring_addr = smem_addr(ring);
@@ -138,7 +139,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // Item info and block ids are loaded one item ahead of their use.
         auto load_item = [&](int j) -> int4 {
             const int k = snake_item(c, j, C);
-            return k < total ? __ldg(p.items + k) : make_int4(-1, 0, 0, 0);
+            return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
         };
         // Block ids of an item are copied into a double-buffered shared array
         // with cp.async one item ahead of their use.
@@ -238,7 +239,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     math.setup(lane);
     auto item_at = [&](int j) -> int4 {
         const int k = snake_item(c, j, C);
-        return k < total ? __ldg(p.items + k) : make_int4(-1, 0, 0, 0);
+        return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
     };
     int4 it = item_at(0);
     int4 it_next = item_at(1);

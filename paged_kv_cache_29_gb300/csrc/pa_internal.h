@@ -21,7 +21,6 @@ struct DecodeParams {
     const int32_t* context_lens;   // [B]
     float* part_o;                 // [B][Hq][max_parts][D] unnormalised partial outputs
     float* part_ml;                // [B][Hq][max_parts][2] (running max in log2 units, sum)
-    int* sched;                    // [0]: number of work items (written by the plan kernel)
     int4* items;                   // work items (sequence, KV head, partition, context length)
     int32_t* error_word;           // nullable
     float scale_log2;              // scale * log2(e): scores are kept in base 2
@@ -52,10 +51,7 @@ cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
 bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group);
 
-// Work list of a persistent decode launch (one CTA, before the decode kernel).
-cudaError_t launch_plan(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
-size_t plan_smem_bytes(int num_seqs);
-constexpr int kPlanMaxSeqs = 4096;   // sequences per plan/decode launch
+constexpr int kPlanMaxSeqs = 4096;   // sequences per persistent decode launch
 
 // Direct-load kernel for any block size and head dim <= 256.
 cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);

@@ -1,0 +1,167 @@
+// pa_plan.cuh -- the work list of one persistent decode launch, computed by
+// every CTA of that launch for itself.
+//
+// A work item is one (sequence, KV head, partition) of at most partition_size
+// rows. The items of the batch are numbered in one global order:
+//   1. every full partition (partition_size rows), by sequence, partition,
+//      KV head;
+//   2. then the partial last partitions, in kBuckets buckets of decreasing
+//      size (by sequence within a bucket), so that the last items a persistent
+//      CTA picks up are the smallest.
+// CTA c of C processes items c, 2C-1-c, 2C+c, ... (a snake, so that the
+// per-CTA totals even out). Each CTA walks the context lengths twice (the
+// prefix of full partitions, then the bucket ranks) and writes only its own
+// items into the workspace, which it then reads back in order; no other CTA
+// touches them. The order only decides which CTA does what and when: every
+// item's result and the merge order of a sequence's partitions are fixed by
+// the sequence's own length, so the output does not depend on the rest of the
+// batch.
+//
+// The walk also writes the zero output rows of empty sequences (sequence s by
+// CTA s % C) and flags context lengths outside [0, max_context_len] (those
+// sequences get no items).
+#pragma once
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kPlanBuckets = 16;
+
+// CTA c's j-th item in a snake over C CTAs.
+__device__ __forceinline__ int snake_item(int c, int j, int C) {
+    return j * C + ((j & 1) ? (C - 1 - c) : c);
+}
+
+// Shared ints plan_cta needs for NT threads.
+__host__ __device__ constexpr int plan_scratch_ints(int nt) {
+    return (nt / 32) * (1 + kPlanBuckets) + 3 * kPlanBuckets + 4;
+}
+
+// Calls f(k) for every k in [a, e) that is one of CTA c's items.
+template <typename F>
+__device__ __forceinline__ void for_own_items(int a, int e, int c, int C, F&& f) {
+    if (a >= e) return;
+    for (int j = a / C; j * C < e; ++j) {
+        const int k = snake_item(c, j, C);
+        if (k >= a && k < e) f(k);
+    }
+}
+
+// Context length of sequence s, or -1 (flagged) when it is out of range.
+__device__ __forceinline__ int plan_len(const DecodeParams& p, int s, bool flag) {
+    int n = __ldg(p.context_lens + s);
+    if (n < 0 || n > p.context_cap) {
+        if (flag) raise_error(p.error_word, PA_DEVERR_CONTEXT);
+        n = -1;
+    }
+    return n;
+}
+
+__device__ __forceinline__ int plan_bucket(int r, int P) {
+    return r > 0 ? min(kPlanBuckets - 1, ((P - r) * kPlanBuckets) / P) : -1;
+}
+
+// Writes CTA c's items and returns the number of items of the launch. All NT
+// threads of the CTA call it; `sm` holds plan_scratch_ints(NT) ints. Row bytes
+// of the output (num_heads * head_dim * sizeof(T)) are a multiple of 16.
+template <typename T, int NT>
+__device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
+    constexpr int NW = NT / 32;
+    int* wsum = sm;                          // [NW]
+    int* wcnt = wsum + NW;                   // [NW][kPlanBuckets]
+    int* bcount = wcnt + NW * kPlanBuckets;  // [kPlanBuckets]
+    int* bcursor = bcount + kPlanBuckets;    // [kPlanBuckets]
+    int* brun = bcursor + kPlanBuckets;      // [kPlanBuckets]
+    int* carry = brun + kPlanBuckets;        // [1] full partitions so far; [1] total
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.num_seqs, P = p.partition_size, Hkv = p.num_kv_heads;
+    if (tid < kPlanBuckets) {
+        bcount[tid] = 0;
+        brun[tid] = 0;
+    }
+    if (tid == 0) carry[0] = 0;
+    __syncthreads();
+
+    // Pass 1: exclusive prefix of full partitions, chunk by chunk; emit the
+    // full items; count partial partitions per bucket.
+    for (int s0 = 0; s0 < B; s0 += NT) {
+        const int s = s0 + tid;
+        const int n = s < B ? plan_len(p, s, s % C == c) : -1;
+        const int nf = n > 0 ? n / P : 0;
+        int incl = nf;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int base = carry[0], chunk = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w < warp) base += wsum[w];
+            chunk += wsum[w];
+        }
+        __syncthreads();
+        if (tid == 0) carry[0] += chunk;
+        const int pf = base + incl - nf;     // full partitions before sequence s
+        for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
+            const int unit = k / Hkv;
+            p.items[k] = make_int4(s, k - unit * Hkv, unit - pf, n);
+        });
+        const int b = n > 0 ? plan_bucket(n % P, P) : -1;
+        if (b >= 0) atomicAdd(&bcount[b], 1);
+        if (n == 0 && s % C == c) {
+            const int chunks = p.num_heads * p.head_dim * static_cast<int>(sizeof(T)) / 16;
+            uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
+                                                  static_cast<size_t>(s) * p.num_heads * p.head_dim);
+            for (int i = 0; i < chunks; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int b = 0; b < kPlanBuckets; ++b) {
+            bcursor[b] = acc;
+            acc += bcount[b];
+        }
+        carry[1] = (carry[0] + acc) * Hkv;
+    }
+    __syncthreads();
+    const int full_items = carry[0] * Hkv;
+    const int total = carry[1];
+
+    // Pass 2: each partial partition's rank: bucket start, then earlier
+    // sequences of the same bucket (earlier chunks, earlier warps, earlier
+    // lanes).
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int s0 = 0; s0 < B; s0 += NT) {
+        const int s = s0 + tid;
+        const int n = s < B ? plan_len(p, s, false) : -1;
+        const int b = n > 0 ? plan_bucket(n % P, P) : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, b);
+        if (lane < kPlanBuckets) wcnt[warp * kPlanBuckets + lane] = 0;
+        __syncwarp();
+        if (b >= 0 && (same & lt_mask) == 0) wcnt[warp * kPlanBuckets + b] = __popc(same);
+        __syncthreads();
+        if (b >= 0) {
+            int j = bcursor[b] + brun[b] + __popc(same & lt_mask);
+            for (int w = 0; w < warp; ++w) j += wcnt[w * kPlanBuckets + b];
+            const int a = full_items + j * Hkv;
+            const int nf = n / P;
+            for_own_items(a, a + Hkv, c, C, [&](int k) { p.items[k] = make_int4(s, k - a, nf, n); });
+        }
+        __syncthreads();
+        if (tid < kPlanBuckets) {
+            int add = 0;
+            for (int w = 0; w < NW; ++w) add += wcnt[w * kPlanBuckets + tid];
+            brun[tid] += add;
+        }
+        __syncthreads();
+    }
+    return total;
+}
+
+}  // namespace pa
