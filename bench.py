@@ -167,6 +167,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_over_ranks(timings, counts, device):
+    """Whole-job figures: the max of each timing and the sum of each work
+    count over all ranks (the inputs unchanged without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in timings], [float(x) for x in counts]
+    t = torch.tensor([float(x) for x in timings], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    c = torch.tensor([float(x) for x in counts], device=device, dtype=torch.float64)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    return t.tolist(), c.tolist()
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -390,17 +404,8 @@ def run_native(args) -> dict | None:
         e2e_ms.append(a.elapsed_time(b))
     e2e_total = sum(e2e_ms)
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_total, decode_avg], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_total, decode_avg = t.tolist()
-        nb = torch.tensor([float(bytes_.total), float(step.num_seqs)], device=dev,
-                          dtype=torch.float64)
-        dist.all_reduce(nb)
-        all_bytes, all_seqs = nb.tolist()
-    else:
-        all_bytes, all_seqs = float(bytes_.total), float(step.num_seqs)
+    (total_ms, e2e_total, decode_avg), (all_bytes, all_seqs) = reduce_over_ranks(
+        [total_ms, e2e_total, decode_avg], [float(bytes_.total), float(step.num_seqs)], dev)
     if rank != 0:
         return None
 
