@@ -54,6 +54,7 @@ METRIC = "paged decode attention: achieved KV GB/s (% of GB300 HBM peak) and seq
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+COPY_PAIRS = 4096
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_8b_gqa_ncu.md")
 CSRC = os.path.join(ROOT, "paged_kv_cache_29_gb300", "csrc")
 
@@ -296,7 +297,7 @@ def run_native(args) -> dict | None:
         # Evict the step's data (write), then replace the dirty lines with
         # clean ones (read), outside the timed region.
         flush.fill_(i & 0xff)
-        flush_clean.sum(dtype=torch.int64)
+        flush_clean.view(torch.int32).max()
     stream = torch.cuda.current_stream(dev)
     # append, decode, and the split-K merge when a sequence spans more than
     # one 512-row partition (batches of at most 4096 sequences: one launch each)
@@ -404,6 +405,23 @@ def run_native(args) -> dict | None:
         e2e_ms.append(a.elapsed_time(b))
     e2e_total = sum(e2e_ms)
 
+    # Copy-on-write block copies (pa_copy_blocks): COPY_PAIRS random distinct
+    # (src, dst) pairs of this pool, after every other measurement (it
+    # overwrites pool blocks).
+    pairs = min(COPY_PAIRS, step.num_blocks // 2)
+    perm = torch.randperm(step.num_blocks, generator=torch.Generator().manual_seed(7))
+    mapping = torch.stack([perm[:pairs], perm[pairs:2 * pairs]], dim=1).to(dev)
+    for _ in range(args.warmup):
+        pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err, stream=stream)
+    copy_ms = timed(lambda: pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err,
+                                              stream=stream), K)
+    block_bytes = step.num_kv_heads * step.block_size * step.head_dim * step.elem_bytes
+    copy_bytes = pairs * 2 * 2 * block_bytes + pairs * 16      # K and V read + written, the pairs
+    copy_avg = sum(copy_ms) / K
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
+
     (total_ms, e2e_total, decode_avg), (all_bytes, all_seqs) = reduce_over_ranks(
         [total_ms, e2e_total, decode_avg], [float(bytes_.total), float(step.num_seqs)], dev)
     if rank != 0:
@@ -467,6 +485,16 @@ def run_native(args) -> dict | None:
         },
         "gpu_launches": launches_per_step * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
+        "copy_blocks": {
+            "pairs": pairs,
+            "bytes_per_call": copy_bytes,
+            "ms_per_call": round(copy_avg, 5),
+            "achieved": round(copy_bytes / (copy_avg * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "frac": round(copy_bytes / (copy_avg * 1e-3) / 1e9 / peak, 4),
+            "note": "pa_copy_blocks of random distinct block pairs of this pool (copy-on-write), "
+                    "CUDA events per call, L2 flushed between calls",
+        },
         "clocks": clocks.summary(),
     }
     if step.meta.get("unique_blocks") and bytes_.kv_unique != bytes_.kv:

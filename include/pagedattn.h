@@ -1,7 +1,8 @@
 /*
  * pagedattn.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode library.
  *
- * One decode step of paged attention is two calls on one CUDA stream:
+ * One decode step of paged attention is two calls on one CUDA stream
+ * (three when a shared block must first be copied, pa_copy_blocks):
  *
  *   pa_reshape_and_cache  writes each sequence's new K and V row into its slot
  *                         of the paged pool (the cache append of the naive
@@ -85,6 +86,26 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
                                int num_tokens, int num_kv_heads, int head_dim,
                                int block_size, int num_blocks, pa_dtype dtype,
                                int32_t* error_word, struct CUstream_st* stream);
+
+/*
+ * Copy-on-write of whole blocks: for each pair i,
+ *   k_cache[dst][:][:][:] = k_cache[src][:][:][:]   (same for V),
+ *   src = block_mapping[2 i], dst = block_mapping[2 i + 1],
+ * every KV head's block_size rows, bit for bit. A block shared by several
+ * sequences (after a fork, or a shared prompt prefix) is copied before one of
+ * them appends into it ("MLSys Engineer -- Inference Systems Q&A", Q1, "Why
+ * this helps": copy-on-write sharing). block_mapping is int64 [num_pairs][2]
+ * in device memory, 8-byte aligned. A pair with a negative entry is skipped;
+ * a pair with an entry >= num_blocks is skipped and flagged PA_DEVERR_BLOCK_ID.
+ * Destinations must be distinct and no destination may be a source of
+ * another pair in the same call (such pairs race). head_dim * sizeof(T) must
+ * be a multiple of 16 and the pools 16-byte aligned. Returns PA_OK or an
+ * error; never blocks.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                         int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_dtype dtype, int32_t* error_word,
+                         struct CUstream_st* stream);
 
 /*
  * Decode attention for num_seqs sequences:

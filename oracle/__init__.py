@@ -67,6 +67,8 @@ def _load():
         P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         lib.pao_append.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
         lib.pao_append.restype = I
+        lib.pao_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I]
+        lib.pao_copy_blocks.restype = I
         lib.pao_decode.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode.restype = I
         lib.pao_attention_weights.argtypes = [P, P, P, P, D, I, I, P, I, I, I, I, I, I, I, I]
@@ -116,6 +118,22 @@ def append(k_new, v_new, slot_mapping, k_cache, v_cache) -> int:
                             _dtype_code(k_cache))
     if rc < 0:
         _check(rc, "append")
+    return rc
+
+
+def copy_blocks(k_cache, v_cache, block_mapping) -> int:
+    """Copy-on-write, in place: block dst := block src of K and V for each
+    (src, dst) row of block_mapping (int64 [n][2]), in order. Negative entries
+    skip a pair; returns the count of pairs with an entry past the pool."""
+    for a in (k_cache, v_cache):
+        if not a.flags.c_contiguous:
+            raise OracleError("caches must be C-contiguous (they are written in place)")
+    nb, hkv, bs, d = k_cache.shape
+    mapping = _c(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2))
+    rc = _load().pao_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(mapping),
+                                 int(mapping.shape[0]), hkv, d, bs, nb, _dtype_code(k_cache))
+    if rc < 0:
+        _check(rc, "copy_blocks")
     return rc
 
 
@@ -196,7 +214,7 @@ class use_library:
         _load()
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
-        for name in ("pao_append", "pao_decode", "pao_attention_weights",
+        for name in ("pao_append", "pao_copy_blocks", "pao_decode", "pao_attention_weights",
                      "pao_decode_partitions", "pao_combine_partitions"):
             src = getattr(self._saved, name)
             dst = getattr(lib, name)

@@ -15,6 +15,15 @@
  *           serving", "Code from memory", the naive incremental decoder (the
  *           cache append, then softmax over every row seen so far).
  *
+ *  copy     Copy-on-write of whole blocks: for each (src, dst) pair, every
+ *           KV head's block_size rows of K and of V in block src are copied,
+ *           bit for bit, over block dst. A block shared by several sequences
+ *           is copied before one of them writes into it ("MLSys Engineer --
+ *           Inference Systems Q&A", Q1, "Why this helps": copy-on-write
+ *           sharing; "Forward Deployed Engineering Interview", Chapter 2
+ *           "Batching and the KV Cache": the block manager's append copies a
+ *           shared last block first). Pairs are applied in order.
+ *
  *  gather   Row i of a sequence's K (and V) lives in physical block
  *           block_table[i / block_size] at offset i % block_size (same Q1).
  *           The oracle rebuilds the sequence's contiguous K and V this way.
@@ -90,6 +99,30 @@ int pao_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
             memcpy((char*)k_cache + dst, (const char*)k_new + src, row);
             memcpy((char*)v_cache + dst, (const char*)v_new + src, row);
         }
+    }
+    return bad;
+}
+
+/* Copy-on-write: block dst of K and V becomes a copy of block src, for each
+ * (src, dst) pair of block_mapping ([num_pairs][2]). A pair with a negative
+ * entry is skipped; a pair with an entry >= num_blocks is skipped and
+ * counted. Returns that count, or PAO_BAD_ARG. */
+int pao_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int num_pairs,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (dtype != 0 && dtype != 1))
+        return PAO_BAD_ARG;
+    const size_t block_bytes =
+        (size_t)num_kv_heads * block_size * head_dim * (size_t)elem_bytes_of(dtype);
+    int bad = 0;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t src = block_mapping[2 * i], dst = block_mapping[2 * i + 1];
+        if (src < 0 || dst < 0) continue;
+        if (src >= num_blocks || dst >= num_blocks) { ++bad; continue; }
+        memmove((char*)k_cache + (size_t)dst * block_bytes,
+                (const char*)k_cache + (size_t)src * block_bytes, block_bytes);
+        memmove((char*)v_cache + (size_t)dst * block_bytes,
+                (const char*)v_cache + (size_t)src * block_bytes, block_bytes);
     }
     return bad;
 }

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     PA_DEVERR_SLOT,
     PA_DEVERR_TIMEOUT,
     PagedAttentionError,
+    pa_copy_blocks,
     pa_decode,
     pa_decode_noalloc,
     pa_decode_workspace_size,
@@ -21,6 +22,6 @@ from ._binding import (  # noqa: F401
     pa_version,
 )
 
-__all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_status_string",
+__all__ = ["pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_status_string",
            "pa_version", "PagedAttentionError", "KERNELS", "block_manager", "workloads",
            "accounting"]

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
         L.pa_reshape_and_cache.restype = I
+        L.pa_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
+        L.pa_copy_blocks.restype = I
         L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
         L.pa_decode.restype = I
         L.pa_decode_ex.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
@@ -156,6 +158,25 @@ def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, error_wor
                                     _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None) -> None:
+    """Copy-on-write: block dst := block src of both pools for each (src, dst)
+    row of block_mapping (int64 [n][2]); negative entries skip a pair."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("block_mapping", block_mapping, torch.int64, 2)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != (nb, hkv, bs, d) or block_mapping.shape[1] != 2:
+        raise ValueError("v_cache must match k_cache and block_mapping must be [n][2]")
+    rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping),
+                              int(block_mapping.shape[0]), hkv, d, bs, nb,
+                              _dtype_code(k_cache), _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_copy_blocks")
 
 
 def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int,

@@ -155,6 +155,27 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
     return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                         int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_dtype dtype, int32_t* error_word,
+                         struct CUstream_st* stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || !valid_dtype(dtype))
+        return PA_ERR_INVALID_ARG;
+    const int row_bytes = head_dim * elem_bytes(dtype);
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    const long long block_bytes = static_cast<long long>(num_kv_heads) * block_size * row_bytes;
+    const cudaError_t err =
+        pa::launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, block_bytes,
+                               num_blocks, error_word, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const int32_t* context_lens, float scale,
                        void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,

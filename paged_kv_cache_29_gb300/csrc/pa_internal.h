@@ -42,6 +42,11 @@ cudaError_t launch_append(const void* k_new, const void* v_new, const int64_t* s
                           int row_bytes, int block_size, int num_blocks, int32_t* error_word,
                           cudaStream_t stream);
 
+// Copy-on-write block copies (block_bytes: one block of one pool, a multiple of 16).
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                               int num_pairs, long long block_bytes, int num_blocks,
+                               int32_t* error_word, cudaStream_t stream);
+
 // Persistent tile-ring kernels (one launch per call, sm_count SMs).
 // Return cudaErrorNotSupported for shapes without an instance.
 cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv,

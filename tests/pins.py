@@ -209,6 +209,57 @@ def pin_copy_on_write():
         np.testing.assert_array_equal(kp[blk, :, 40 % bs, :], slot_owner)
 
 
+# ---- P7b: the copy-on-write block copy ---------------------------------------
+
+def pin_copy_blocks():
+    """After a fork, the child's append copies the shared partial block
+    (oracle.copy_blocks) and then writes its row: the child must see the
+    parent's 40 rows followed by its own, the parent must see nothing new, and
+    no block but the copy's destination may change."""
+    bs, hkv, hq, d = 16, 2, 4, 8
+    for dtype in ("f32", "bf16"):
+        rng = np.random.default_rng(21)
+        nb = 24
+        mgr = BlockManager(nb, bs, free_order=rng.permutation(nb), prefix_caching=False)
+        mgr.admit("p", list(range(40)))          # last block holds 8 of 16 slots
+        mgr.fork("p", "c")
+        k = wl.to_cache_dtype(rng.standard_normal((nb, hkv, bs, d)).astype(np.float32), dtype)
+        v = wl.to_cache_dtype(rng.standard_normal((nb, hkv, bs, d)).astype(np.float32), dtype)
+        q = wl.to_cache_dtype(rng.standard_normal((1, hq, d)).astype(np.float32), dtype)
+        new_k = wl.to_cache_dtype(rng.standard_normal((1, hkv, d)).astype(np.float32), dtype)
+        new_v = wl.to_cache_dtype(rng.standard_normal((1, hkv, d)).astype(np.float32), dtype)
+        parent_table = mgr.block_table("p")
+        # the parent's 40 rows per KV head, read before anything is written
+        rows_k = np.stack([k[parent_table[i // bs], :, i % bs, :] for i in range(40)])
+        rows_v = np.stack([v[parent_table[i // bs], :, i % bs, :] for i in range(40)])
+        k0, v0 = k.copy(), v.copy()
+        res = mgr.append("c", 99)
+        assert res.copy_on_write is not None
+        src, dst = res.copy_on_write
+        assert oracle.copy_blocks(k, v, [[src, dst]]) == 0
+        changed = [b for b in range(nb) if not (np.array_equal(k[b], k0[b]) and
+                                                np.array_equal(v[b], v0[b]))]
+        assert changed == [dst], changed
+        oracle.append(new_k, new_v, np.array([res.slot], np.int64), k, v)
+        # The child's expected rows in one private block of 41 rows.
+        kc = np.concatenate([rows_k, new_k]).transpose(1, 0, 2)[None].copy()
+        vc = np.concatenate([rows_v, new_v]).transpose(1, 0, 2)[None].copy()
+        table_c = np.array([mgr.block_table("c") + [-1]], np.int32)
+        got = oracle.decode(q, k, v, table_c, np.array([41], np.int32), 0.3)
+        want = oracle.decode(q, kc, vc, np.zeros((1, 1), np.int32), np.array([41], np.int32), 0.3)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+        table_p = np.array([parent_table + [-1]], np.int32)
+        kp = np.stack([rows_k]).transpose(0, 2, 1, 3).copy()
+        vp = np.stack([rows_v]).transpose(0, 2, 1, 3).copy()
+        got_p = oracle.decode(q, k, v, table_p, np.array([40], np.int32), 0.3)
+        want_p = oracle.decode(q, kp, vp, np.zeros((1, 1), np.int32), np.array([40], np.int32), 0.3)
+        np.testing.assert_allclose(got_p, want_p, rtol=0, atol=1e-12)
+    # Skipped and out-of-range pairs: nothing is written, the latter are counted.
+    k1, v1 = k.copy(), v.copy()
+    assert oracle.copy_blocks(k1, v1, [[-1, 3], [2, -1], [nb, 1], [0, nb + 5]]) == 2
+    assert np.array_equal(k1, k) and np.array_equal(v1, v)
+
+
 # ---- P8: closed forms ---------------------------------------------------------
 
 def pin_closed_forms():
@@ -327,5 +378,6 @@ def pin_incremental_decoder():
 
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
+            pin_copy_blocks,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]

@@ -29,6 +29,14 @@ MUTANTS = [
      "const int hi = lo + partition_size < n + 1 ? lo + partition_size : n + 1;"),
     ("bf16_shift", "uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;",
      "uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 15;"),
+    ("copy_k_only",
+     "memmove((char*)v_cache + (size_t)dst * block_bytes,\n                (const char*)v_cache + (size_t)src * block_bytes, block_bytes);", ""),
+    ("copy_reversed",
+     "memmove((char*)k_cache + (size_t)dst * block_bytes,\n                (const char*)k_cache + (size_t)src * block_bytes, block_bytes);",
+     "memmove((char*)k_cache + (size_t)src * block_bytes,\n                (const char*)k_cache + (size_t)dst * block_bytes, block_bytes);"),
+    ("copy_one_head",
+     "(size_t)num_kv_heads * block_size * head_dim * (size_t)elem_bytes_of(dtype);\n    int bad",
+     "(size_t)block_size * head_dim * (size_t)elem_bytes_of(dtype);\n    int bad"),
     ("q_from_kv_head", "qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);",
      "qv[d] = load_elem(q, ((size_t)s * num_heads + h) * head_dim + d, dtype);"),
 ]
