@@ -69,6 +69,15 @@ def _load():
         lib.pao_append.restype = I
         lib.pao_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I]
         lib.pao_copy_blocks.restype = I
+        F = ctypes.c_float
+        lib.pao_e4m3_decode.argtypes = [I]
+        lib.pao_e4m3_decode.restype = D
+        lib.pao_e4m3_encode.argtypes = [F]
+        lib.pao_e4m3_encode.restype = I
+        lib.pao_append_fp8.argtypes = [P, P, I, P, P, P, I, I, I, I, I, F, F]
+        lib.pao_append_fp8.restype = I
+        lib.pao_decode_kv.argtypes = [P, I, P, P, I, D, D, P, P, D, P, I, I, I, I, I, I, I, I]
+        lib.pao_decode_kv.restype = I
         lib.pao_decode.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode.restype = I
         lib.pao_attention_weights.argtypes = [P, P, P, P, D, I, I, P, I, I, I, I, I, I, I, I]
@@ -91,7 +100,10 @@ def _dtype_code(a: np.ndarray) -> int:
         return 0
     if a.dtype == np.uint16:
         return 1
-    raise OracleError(f"cache dtype must be float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.uint8:
+        return 2
+    raise OracleError("cache dtype must be float32, uint16 (bf16 bits) or uint8 (e4m3 codes), "
+                      f"got {a.dtype}")
 
 
 def _c(a: np.ndarray, dtype=None) -> np.ndarray:
@@ -135,6 +147,59 @@ def copy_blocks(k_cache, v_cache, block_mapping) -> int:
     if rc < 0:
         _check(rc, "copy_blocks")
     return rc
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of e4m3 codes (any integer array; NaN for 0x7F/0xFF)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.int64)
+    return np.array([lib.pao_e4m3_decode(int(x)) for x in c.ravel()],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """Nearest e4m3 codes (uint8) of binary32 values (ties to even, saturating)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32)
+    return np.array([lib.pao_e4m3_encode(float(x)) for x in v.ravel()],
+                    dtype=np.uint8).reshape(v.shape)
+
+
+def append_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_scale=1.0) -> int:
+    """Quantising append into an FP8 cache (uint8 codes, in place): code =
+    e4m3(x / scale). k_new/v_new are fp32 or bf16 bits. Returns the
+    out-of-range slot count."""
+    for a in (k_cache, v_cache):
+        if not a.flags.c_contiguous or a.dtype != np.uint8:
+            raise OracleError("fp8 caches must be C-contiguous uint8 (written in place)")
+    nb, hkv, bs, d = k_cache.shape
+    k_new, v_new = _c(k_new), _c(v_new, k_new.dtype)
+    slots = _c(slot_mapping, np.int64)
+    rc = _load().pao_append_fp8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(slots),
+                                _ptr(k_cache), _ptr(v_cache), int(slots.shape[0]), hkv, d, bs,
+                                nb, float(k_scale), float(v_scale))
+    if rc < 0:
+        _check(rc, "append_fp8")
+    return rc
+
+
+def decode_kv(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.0,
+              v_scale=1.0, num_threads=0):
+    """fp64 decode attention with q and the caches in their own dtypes (the
+    caches may be e4m3 codes) and per-tensor K/V scales."""
+    q = _c(q)
+    k_cache, v_cache = _c(k_cache), _c(v_cache, k_cache.dtype)
+    bt, cl = _c(block_tables, np.int32), _c(context_lens, np.int32)
+    B, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    out = np.zeros((B, hq, d), dtype=np.float64)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    rc = _load().pao_decode_kv(_ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache),
+                               _dtype_code(k_cache), float(k_scale), float(v_scale), _ptr(bt),
+                               _ptr(cl), float(scale), _ptr(out), B, hq, hkv, d, bs, nb, mb,
+                               int(num_threads))
+    _check(rc, "decode_kv")
+    return out
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0):
@@ -214,7 +279,8 @@ class use_library:
         _load()
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
-        for name in ("pao_append", "pao_copy_blocks", "pao_decode", "pao_attention_weights",
+        for name in ("pao_append", "pao_copy_blocks", "pao_e4m3_decode", "pao_e4m3_encode",
+                     "pao_append_fp8", "pao_decode_kv", "pao_decode", "pao_attention_weights",
                      "pao_decode_partitions", "pao_combine_partitions"):
             src = getattr(self._saved, name)
             dst = getattr(lib, name)

@@ -24,6 +24,19 @@
  *           "Batching and the KV Cache": the block manager's append copies a
  *           shared last block first). Pairs are applied in order.
  *
+ *  fp8      An FP8 cache stores each element as an e4m3 code with one scale
+ *           per tensor (K and V each): value = scale * e4m3(code); an
+ *           uncalibrated scale is 1.0 ("Forward Deployed Engineering
+ *           Interview", Chapter 2: an FP8 cache halves the bytes per token,
+ *           scales per tensor). The pages name the format only; e4m3 is read
+ *           as the OCP 8-bit format: 1 sign bit, 4 exponent bits with bias 7,
+ *           3 mantissa bits, subnormals at exponent 0, no infinities, the
+ *           all-ones exponent-and-mantissa pattern (0x7F, 0xFF) is NaN, so
+ *           the largest finite magnitude is 448. Appending into an FP8 cache
+ *           divides each new value by the scale in fp32 (IEEE division) and
+ *           rounds the quotient to the nearest e4m3 value, ties to the even
+ *           code, magnitudes beyond 448 saturating to 448 (pao_e4m3_encode).
+ *
  *  gather   Row i of a sequence's K (and V) lives in physical block
  *           block_table[i / block_size] at offset i % block_size (same Q1).
  *           The oracle rebuilds the sequence's contiguous K and V this way.
@@ -49,7 +62,8 @@
  *   k/v cache      [num_blocks][num_kv_heads][block_size][head_dim]
  *   block_tables   int32 [num_seqs][max_blocks_per_seq]
  *   context_lens   int32 [num_seqs], counting the token appended this step
- * dtype: 0 = fp32, 1 = bf16 (raw 16-bit patterns). Context length 0 gives a
+ * dtype: 0 = fp32, 1 = bf16 (raw 16-bit patterns), 2 = fp8 e4m3 (raw 8-bit
+ * codes, caches only; see "fp8" above). Context length 0 gives a
  * zero output row (a reading: the pages say nothing about empty sequences).
  */
 #include <math.h>
@@ -66,8 +80,42 @@
 #define PAO_BAD_LEN (-3)
 #define PAO_NO_MEMORY (-4)
 
+/* The value of an e4m3 code (NaN for 0x7F and 0xFF). */
+double pao_e4m3_decode(int code) {
+    const int c = code & 0xFF;
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/* Nearest e4m3 code of a binary32 value: round to nearest, ties to the even
+ * code; |x| >= 448 gives +-448; NaN gives 0x7F. Within a binade of exponent
+ * E (2^E <= |x| < 2^(E+1), E >= -6) the codes are spaced 2^(E-3); below 2^-6
+ * they are spaced 2^-9 (subnormals). Rounding |x| / spacing to an integer q
+ * then gives code (E + 7) * 8 + (q - 8), or q below 2^-6; q = 16 carries into
+ * the next binade by the same formula. */
+int pao_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    const int sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int ex;
+    (void)frexp(a, &ex);                    /* a = f * 2^ex, f in [0.5, 1) */
+    const int E = ex - 1;
+    int code;
+    if (a == 0.0 || E < -6) {
+        code = (int)nearbyint(ldexp(a, 9));  /* exact quotient; ties to even */
+    } else {
+        const int q = (int)nearbyint(ldexp(a, 3 - E));
+        code = (E + 7) * 8 + (q - 8);
+    }
+    return sign | code;
+}
+
 static double load_elem(const void* base, size_t idx, int dtype) {
     if (dtype == 0) return (double)((const float*)base)[idx];
+    if (dtype == 2) return pao_e4m3_decode(((const uint8_t*)base)[idx]);
     /* bf16: the 16 stored bits are the high half of an IEEE binary32. */
     uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
     float f;
@@ -75,7 +123,7 @@ static double load_elem(const void* base, size_t idx, int dtype) {
     return (double)f;
 }
 
-static int elem_bytes_of(int dtype) { return dtype == 0 ? 4 : 2; }
+static int elem_bytes_of(int dtype) { return dtype == 0 ? 4 : dtype == 1 ? 2 : 1; }
 
 /* Copy every new K/V row into its slot. Negative slots are skipped (padding);
  * a slot past the pool is skipped and counted. Returns that count. */
@@ -83,7 +131,7 @@ int pao_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
                void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
                int head_dim, int block_size, int num_blocks, int dtype) {
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks < 0 || (dtype != 0 && dtype != 1))
+        num_blocks < 0 || dtype < 0 || dtype > 2)
         return PAO_BAD_ARG;
     const size_t row = (size_t)head_dim * (size_t)elem_bytes_of(dtype);
     const int64_t num_slots = (int64_t)num_blocks * block_size;
@@ -110,7 +158,7 @@ int pao_append(const void* k_new, const void* v_new, const int64_t* slot_mapping
 int pao_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int num_pairs,
                     int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype) {
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks < 0 || (dtype != 0 && dtype != 1))
+        num_blocks < 0 || dtype < 0 || dtype > 2)
         return PAO_BAD_ARG;
     const size_t block_bytes =
         (size_t)num_kv_heads * block_size * head_dim * (size_t)elem_bytes_of(dtype);
@@ -130,7 +178,8 @@ int pao_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, 
 /* Rebuild the contiguous K and V rows 0..n-1 of (seq, kv_head) as fp64. */
 static int gather(const void* k_cache, const void* v_cache, const int32_t* table, int n,
                   int kv_head, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, int dtype, double* Kc, double* Vc) {
+                  int num_blocks, int dtype, double k_scale, double v_scale, double* Kc,
+                  double* Vc) {
     for (int i = 0; i < n; ++i) {
         const int32_t blk = table[i / block_size];
         if (blk < 0 || blk >= num_blocks) return PAO_BAD_BLOCK;
@@ -138,8 +187,8 @@ static int gather(const void* k_cache, const void* v_cache, const int32_t* table
         const size_t base =
             (((size_t)blk * num_kv_heads + kv_head) * block_size + off) * (size_t)head_dim;
         for (int d = 0; d < head_dim; ++d) {
-            Kc[(size_t)i * head_dim + d] = load_elem(k_cache, base + d, dtype);
-            Vc[(size_t)i * head_dim + d] = load_elem(v_cache, base + d, dtype);
+            Kc[(size_t)i * head_dim + d] = k_scale * load_elem(k_cache, base + d, dtype);
+            Vc[(size_t)i * head_dim + d] = v_scale * load_elem(v_cache, base + d, dtype);
         }
     }
     return PAO_OK;
@@ -173,15 +222,18 @@ static int check_shapes(int num_seqs, int num_heads, int num_kv_heads, int head_
 }
 
 /* Full decode attention. out: fp64 [num_seqs][num_heads][head_dim].
- * num_threads <= 0 lets OpenMP (when compiled in) choose. */
-int pao_decode(const void* q, const void* k_cache, const void* v_cache,
-               const int32_t* block_tables, const int32_t* context_lens, double scale,
-               double* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-               int block_size, int num_blocks, int max_blocks_per_seq, int dtype,
-               int num_threads) {
+ * q in q_dtype (0 or 1); K and V in kv_dtype (0, 1 or 2), their values
+ * multiplied by k_scale and v_scale. num_threads <= 0 lets OpenMP (when
+ * compiled in) choose. */
+int pao_decode_kv(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                  int kv_dtype, double k_scale, double v_scale, const int32_t* block_tables,
+                  const int32_t* context_lens, double scale, double* out, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                  int max_blocks_per_seq, int num_threads) {
     int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                          num_blocks, max_blocks_per_seq, dtype);
+                          num_blocks, max_blocks_per_seq, q_dtype);
     if (rc != PAO_OK) return rc;
+    if (kv_dtype < 0 || kv_dtype > 2) return PAO_BAD_ARG;
     const int G = num_heads / num_kv_heads;
     const int units = num_seqs * num_kv_heads;
     int err = PAO_OK;
@@ -211,7 +263,8 @@ int pao_decode(const void* q, const void* k_cache, const void* v_cache,
             continue;
         }
         int grc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq, n, h,
-                         num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+                         num_kv_heads, head_dim, block_size, num_blocks, kv_dtype, k_scale,
+                         v_scale, Kc, Vc);
         if (grc != PAO_OK) {
 #pragma omp atomic write
             err = grc;
@@ -222,7 +275,7 @@ int pao_decode(const void* q, const void* k_cache, const void* v_cache,
             for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
             if (n == 0 || grc != PAO_OK) continue;
             for (int d = 0; d < head_dim; ++d)
-                qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);
+                qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, q_dtype);
             softmax_weights(qv, Kc, n, head_dim, scale, w);
             for (int i = 0; i < n; ++i)
                 for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
@@ -230,6 +283,49 @@ int pao_decode(const void* q, const void* k_cache, const void* v_cache,
         free(Kc); free(Vc); free(w); free(qv);
     }
     return err;
+}
+
+int pao_decode(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, const int32_t* context_lens, double scale,
+               double* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, int max_blocks_per_seq, int dtype,
+               int num_threads) {
+    if (dtype != 0 && dtype != 1) return PAO_BAD_ARG;
+    return pao_decode_kv(q, dtype, k_cache, v_cache, dtype, 1.0, 1.0, block_tables,
+                         context_lens, scale, out, num_seqs, num_heads, num_kv_heads, head_dim,
+                         block_size, num_blocks, max_blocks_per_seq, num_threads);
+}
+
+/* Append into an FP8 cache: code = e4m3(x / scale) for each new element x
+ * (k_new, v_new in new_dtype 0 or 1; the division in fp32), into the slots as
+ * pao_append. Returns the out-of-range slot count, or PAO_BAD_ARG. */
+int pao_append_fp8(const void* k_new, const void* v_new, int new_dtype,
+                   const int64_t* slot_mapping, uint8_t* k_cache, uint8_t* v_cache,
+                   int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, float k_scale, float v_scale) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (new_dtype != 0 && new_dtype != 1) || !(k_scale > 0.0f) ||
+        !(v_scale > 0.0f))
+        return PAO_BAD_ARG;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    int bad = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) { ++bad; continue; }
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)t * num_kv_heads + h) * (size_t)head_dim;
+            const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                const float kx = (float)load_elem(k_new, src + d, new_dtype);
+                const float vx = (float)load_elem(v_new, src + d, new_dtype);
+                k_cache[dst + d] = (uint8_t)pao_e4m3_encode(kx / k_scale);
+                v_cache[dst + d] = (uint8_t)pao_e4m3_encode(vx / v_scale);
+            }
+        }
+    }
+    return bad;
 }
 
 /* The normalised softmax weights of one (seq, query head): w[0..n-1]. */
@@ -251,7 +347,7 @@ int pao_attention_weights(const void* q, const void* k_cache, const int32_t* blo
     if (!Kc || !Vc || !qv) { free(Kc); free(Vc); free(qv); return PAO_NO_MEMORY; }
     /* V is gathered along with K and ignored: one gather routine for both. */
     rc = gather(k_cache, k_cache, block_tables + (size_t)seq * max_blocks_per_seq, n, h,
-                num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+                num_kv_heads, head_dim, block_size, num_blocks, dtype, 1.0, 1.0, Kc, Vc);
     if (rc == PAO_OK) {
         for (int d = 0; d < head_dim; ++d)
             qv[d] = load_elem(q, ((size_t)seq * num_heads + head) * head_dim + d, dtype);
@@ -288,7 +384,7 @@ int pao_decode_partitions(const void* q, const void* k_cache, const void* v_cach
         if (!Kc || !Vc || !qv || !S) { free(Kc); free(Vc); free(qv); free(S); return PAO_NO_MEMORY; }
         for (int h = 0; h < num_kv_heads && rc == PAO_OK; ++h) {
             rc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq, n, h,
-                        num_kv_heads, head_dim, block_size, num_blocks, dtype, Kc, Vc);
+                        num_kv_heads, head_dim, block_size, num_blocks, dtype, 1.0, 1.0, Kc, Vc);
             if (rc != PAO_OK) break;
             for (int g = 0; g < G; ++g) {
                 const int qh = h * G + g;

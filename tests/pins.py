@@ -260,6 +260,119 @@ def pin_copy_blocks():
     assert np.array_equal(k1, k) and np.array_equal(v1, v)
 
 
+# ---- FP8 (e4m3) cache: the format, the quantising append, the dequantised decode
+
+# Code -> value from the OCP 8-bit e4m3 definition (bias 7, 3 mantissa bits,
+# subnormals at exponent 0, 0x7F/0xFF NaN): written out by hand.
+E4M3_KNOWN = [(0x00, 0.0), (0x01, 2.0 ** -9), (0x02, 2.0 ** -8), (0x07, 7 * 2.0 ** -9),
+              (0x08, 2.0 ** -6), (0x09, 1.125 * 2.0 ** -6), (0x30, 0.5), (0x38, 1.0),
+              (0x39, 1.125), (0x3F, 1.875), (0x40, 2.0), (0x44, 3.0), (0x50, 8.0),
+              (0x78, 256.0), (0x7D, 416.0), (0x7E, 448.0), (0x80, -0.0), (0xB8, -1.0),
+              (0xC4, -3.0), (0xFE, -448.0)]
+
+
+def _e4m3_brute(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code by searching every finite code's value (ties to the
+    even code, saturating at +-448): a table search, unlike the oracle's
+    binade arithmetic."""
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.int64)
+    vals = np.array([dict(E4M3_TABLE)[c] for c in codes])
+    out = np.empty(x.shape, dtype=np.uint8)
+    for i, xv in enumerate(np.asarray(x, dtype=np.float64).ravel()):
+        neg = math.copysign(1.0, xv) < 0
+        if abs(xv) >= 448.0:
+            out.flat[i] = 0xFE if neg else 0x7E
+            continue
+        same = codes[(codes >= 0x80) == neg]
+        d = np.abs(vals[(codes >= 0x80) == neg] - xv)
+        best = np.flatnonzero(d == d.min())
+        cand = same[best]
+        out.flat[i] = int(cand[0]) if len(cand) == 1 else int([c for c in cand if c % 2 == 0][0])
+    return out
+
+
+def _e4m3_table():
+    t = []
+    for c in range(256):
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        t.append((c, -mag if c & 0x80 else mag))
+    return t
+
+
+E4M3_TABLE = _e4m3_table()
+
+
+def pin_e4m3_format():
+    table = dict(E4M3_TABLE)
+    for code, val in E4M3_KNOWN:
+        assert table[code] == val and math.copysign(1, table[code]) == math.copysign(1, val)
+    got = oracle.e4m3_decode(np.arange(256))
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            assert math.isnan(got[c]), c
+        else:
+            assert got[c] == table[c] and math.copysign(1, got[c]) == math.copysign(1, table[c]), c
+    pos = got[:0x7F]
+    assert np.all(np.diff(pos) > 0)                       # strictly increasing magnitudes
+    np.testing.assert_array_equal(got[0x80:0xFF], -pos)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F])
+    np.testing.assert_array_equal(oracle.e4m3_encode(got[finite].astype(np.float32)), finite)
+    rng = np.random.default_rng(8)
+    mids = (pos[:-1] + pos[1:]) / 2                       # exact in binary32
+    xs = np.concatenate([
+        rng.standard_normal(3000) * 10.0 ** rng.uniform(-4, 2.8, 3000),
+        mids, -mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+        np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+        [440.0, 447.9, 448.0, 455.9, 464.0, 470.0, 479.9, 480.0, 1e6, -1e9, 2.0 ** -10,
+         3 * 2.0 ** -11, 1e-30, -1e-30, 0.0, -0.0]]).astype(np.float32)
+    np.testing.assert_array_equal(oracle.e4m3_encode(xs), _e4m3_brute(xs))
+    assert int(oracle.e4m3_encode(np.array([np.nan], np.float32))[0]) == 0x7F
+
+
+def pin_fp8_append():
+    rng = np.random.default_rng(31)
+    nb, hkv, bs, d, T = 6, 2, 4, 16, 5
+    for new_dtype in ("bf16", "f32"):
+        for k_scale, v_scale in ((1.0, 1.0), (0.37, 3.0), (2.0, 0.5)):
+            kn = wl.to_cache_dtype(rng.standard_normal((T, hkv, d)).astype(np.float32) * 3, new_dtype)
+            vn = wl.to_cache_dtype(rng.standard_normal((T, hkv, d)).astype(np.float32) * 3, new_dtype)
+            kc = rng.integers(0, 256, (nb, hkv, bs, d)).astype(np.uint8)
+            vc = rng.integers(0, 256, (nb, hkv, bs, d)).astype(np.uint8)
+            slots = np.array([3, -1, 17, 0, nb * bs + 2], np.int64)
+            k0, v0 = kc.copy(), vc.copy()
+            assert oracle.append_fp8(kn, vn, slots, kc, vc, k_scale, v_scale) == 1
+            kx = wl.as_f32(kn, new_dtype) / np.float32(k_scale)     # binary32 division
+            vx = wl.as_f32(vn, new_dtype) / np.float32(v_scale)
+            for t, slot in enumerate(slots):
+                if 0 <= slot < nb * bs:
+                    k0[slot // bs, :, slot % bs, :] = _e4m3_brute(kx[t])
+                    v0[slot // bs, :, slot % bs, :] = _e4m3_brute(vx[t])
+            np.testing.assert_array_equal(kc, k0)
+            np.testing.assert_array_equal(vc, v0)
+
+
+def pin_fp8_decode():
+    """Attention over an e4m3 cache equals attention over a binary32 cache
+    holding scale * value(code) (exact for power-of-two scales)."""
+    rng = np.random.default_rng(41)
+    step = small_step((1, 9, 16, 40), hq=8, hkv=2, d=16, dtype="bf16", bs=4, seed=5)
+    codes_ok = np.array([c for c, _ in E4M3_TABLE], dtype=np.uint8)
+    kc = codes_ok[rng.integers(0, len(codes_ok), step.k_cache.shape)]
+    vc = codes_ok[rng.integers(0, len(codes_ok), step.v_cache.shape)]
+    vals = dict(E4M3_TABLE)
+    for k_scale, v_scale in ((1.0, 1.0), (0.5, 2.0), (0.015625, 8.0)):
+        got = oracle.decode_kv(step.q, kc, vc, step.block_tables, step.context_lens,
+                               step.scale, k_scale, v_scale)
+        kf = (np.vectorize(vals.get)(kc) * k_scale).astype(np.float32)
+        vf = (np.vectorize(vals.get)(vc) * v_scale).astype(np.float32)
+        qf = wl.as_f32(step.q, "bf16")
+        want = oracle.decode(qf, kf, vf, step.block_tables, step.context_lens, step.scale)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
 # ---- P8: closed forms ---------------------------------------------------------
 
 def pin_closed_forms():
@@ -378,6 +491,6 @@ def pin_incremental_decoder():
 
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
-            pin_copy_blocks,
+            pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]

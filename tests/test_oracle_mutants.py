@@ -37,8 +37,16 @@ MUTANTS = [
     ("copy_one_head",
      "(size_t)num_kv_heads * block_size * head_dim * (size_t)elem_bytes_of(dtype);\n    int bad",
      "(size_t)block_size * head_dim * (size_t)elem_bytes_of(dtype);\n    int bad"),
-    ("q_from_kv_head", "qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);",
-     "qv[d] = load_elem(q, ((size_t)s * num_heads + h) * head_dim + d, dtype);"),
+    ("q_from_kv_head", "qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, q_dtype);",
+     "qv[d] = load_elem(q, ((size_t)s * num_heads + h) * head_dim + d, q_dtype);"),
+    ("e4m3_bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
+    ("e4m3_truncates", "const int q = (int)nearbyint(ldexp(a, 3 - E));",
+     "const int q = (int)floor(ldexp(a, 3 - E));"),
+    ("e4m3_late_saturation", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7E;"),
+    ("e4m3_subnormal_step", "code = (int)nearbyint(ldexp(a, 9));", "code = (int)nearbyint(ldexp(a, 8));"),
+    ("fp8_scales_swapped", "Kc[(size_t)i * head_dim + d] = k_scale * load_elem",
+     "Kc[(size_t)i * head_dim + d] = v_scale * load_elem"),
+    ("fp8_append_multiplies", "pao_e4m3_encode(kx / k_scale)", "pao_e4m3_encode(kx * k_scale)"),
 ]
 
 
