@@ -276,9 +276,12 @@ def run_native(args) -> dict | None:
     bytes_ = accounting.step_bytes_for(step)
     cd = step.cache_dtype
 
+    fp8 = cd == "fp8"
+
     def up(a):
+        # bf16 arrays are uint16 bit patterns; FP8 pools stay uint8 codes
         t = torch.from_numpy(np.ascontiguousarray(a))
-        if cd == "bf16" and a.dtype == np.uint16:
+        if a.dtype == np.uint16:
             t = t.view(torch.bfloat16)
         return t.to(dev)
 
@@ -304,11 +307,21 @@ def run_native(args) -> dict | None:
     launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
 
     def do_append(st):
-        pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err, stream=st)
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(k_new, v_new, slots, k_cache, v_cache, step.k_scale,
+                                        step.v_scale, error_word=err, stream=st)
+        else:
+            pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
+                                    stream=st)
 
     def do_decode(st):
-        pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
-                     workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
+        if fp8:
+            pa.pa_decode_fp8(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                             step.k_scale, step.v_scale, workspace=workspace, error_word=err,
+                             stream=st)
+        else:
+            pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                         workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
 
     def do_step(st=None):
         do_append(st)
@@ -376,7 +389,7 @@ def run_native(args) -> dict | None:
            for name, a in (("q", step.q), ("k_new", step.k_new), ("v_new", step.v_new),
                            ("slots", step.slot_mapping), ("tables", step.block_tables),
                            ("lens", step.context_lens))}
-    if cd == "bf16":
+    if step.act_dtype == "bf16":
         for name in ("q", "k_new", "v_new"):
             pin[name] = pin[name].view(torch.bfloat16)
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -444,7 +457,7 @@ def run_native(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": cd,
+        "dtype": "fp8_e4m3" if fp8 else cd,
         "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
         "config": {
             "workload": args.workload,

@@ -64,7 +64,14 @@ typedef enum pa_status {
     PA_ERR_DEVICE_BOUNDS = 5 /* returned by pa_check_error_word: PA_DEVERR_* set */
 } pa_status;
 
-typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 } pa_dtype;
+/* Element types. PA_DTYPE_FP8_E4M3 is a cache type only: each element is an
+ * 8-bit e4m3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * subnormals, largest finite 448, 0x7F/0xFF NaN) and the cached value is
+ * scale * e4m3(code) with one scale per tensor (pa_reshape_and_cache_fp8,
+ * pa_decode_fp8). An FP8 cache halves the bytes per token ("Forward Deployed
+ * Engineering Interview", Chapter 2 "Batching and the KV Cache": FP8 KV, scales
+ * per tensor, 1.0 when uncalibrated). */
+typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1, PA_DTYPE_FP8_E4M3 = 2 } pa_dtype;
 
 /* Bits the kernels OR into *error_word. */
 #define PA_DEVERR_BLOCK_ID 0x1  /* a block-table entry outside [0, num_blocks) */
@@ -79,13 +86,31 @@ typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 } pa_dtype;
  * Tokens with s >= num_blocks * block_size are skipped and flagged
  * PA_DEVERR_SLOT. Two tokens with the same slot race (last writer wins).
  * head_dim * sizeof(T) must be a multiple of 16 and every buffer 16-byte
- * aligned. Returns PA_OK or an error; never blocks.
+ * aligned. dtype may be PA_DTYPE_FP8_E4M3 (k_new/v_new then hold codes,
+ * copied as they are). Returns PA_OK or an error; never blocks.
  */
 pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
                                const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                int num_tokens, int num_kv_heads, int head_dim,
                                int block_size, int num_blocks, pa_dtype dtype,
                                int32_t* error_word, struct CUstream_st* stream);
+
+/*
+ * Quantising append into an FP8 (e4m3) cache:
+ *   k_cache[s / bs][h][s % bs][d] = e4m3(k_new[t][h][d] / k_scale)   (same for V)
+ * with the division in fp32 (IEEE, round to nearest) and the conversion
+ * rounding to the nearest e4m3 value, ties to even, saturating at +-448.
+ * k_new, v_new: new_dtype (PA_DTYPE_F32 or PA_DTYPE_BF16) [num_tokens]
+ * [num_kv_heads][head_dim]; k_cache, v_cache: uint8 codes
+ * [num_blocks][num_kv_heads][block_size][head_dim]. Scales > 0 and finite.
+ * Slots as in pa_reshape_and_cache; head_dim a multiple of 16; buffers
+ * 16-byte aligned. Returns PA_OK or an error; never blocks.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                                   const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                   int num_tokens, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, float k_scale, float v_scale,
+                                   int32_t* error_word, struct CUstream_st* stream);
 
 /*
  * Copy-on-write of whole blocks: for each pair i,
@@ -141,6 +166,24 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     int block_size, int num_blocks, int max_blocks_per_seq,
                     int max_context_len, pa_dtype dtype, void* workspace,
                     size_t workspace_bytes, int32_t* error_word, struct CUstream_st* stream);
+
+/*
+ * pa_decode over an FP8 (e4m3) cache with bf16 q and out:
+ *   out[s][qh][:] = sum_i softmax_i(scale * <q, k_scale * e4m3(K_i)>) * v_scale * e4m3(V_i)[:]
+ * The codes are widened to f16 in registers (exact) and multiplied on tensor
+ * cores with fp32 accumulation; q * scale * k_scale is rounded to f16 once per
+ * sequence and KV head. Same partitioning, merge, workspace
+ * (pa_decode_workspace_size) and error behaviour as pa_decode. Supported:
+ * head_dim 128, block_size a multiple of 16, 1, 2, 4 or 8 query heads per KV
+ * head (else PA_ERR_UNSUPPORTED). Scales > 0 and finite.
+ */
+pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, void* out, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        int max_blocks_per_seq, int max_context_len, void* workspace,
+                        size_t workspace_bytes, int32_t* error_word,
+                        struct CUstream_st* stream);
 
 /* Bytes of workspace pa_decode needs for these sizes (0 only for an empty
  * batch). */

@@ -15,13 +15,15 @@ from ._binding import (  # noqa: F401
     PagedAttentionError,
     pa_copy_blocks,
     pa_decode,
+    pa_decode_fp8,
     pa_decode_noalloc,
     pa_decode_workspace_size,
     pa_reshape_and_cache,
+    pa_reshape_and_cache_fp8,
     pa_status_string,
     pa_version,
 )
 
-__all__ = ["pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_status_string",
+__all__ = ["pa_reshape_and_cache", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_copy_blocks", "pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_status_string",
            "pa_version", "PagedAttentionError", "KERNELS", "block_manager", "workloads",
            "accounting"]

@@ -59,6 +59,10 @@ def lib() -> ctypes.CDLL:
         P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
         L.pa_reshape_and_cache.restype = I
+        L.pa_reshape_and_cache_fp8.argtypes = [P, P, I, P, P, P, I, I, I, I, I, F, F, P, P]
+        L.pa_reshape_and_cache_fp8.restype = I
+        L.pa_decode_fp8.argtypes = [P, P, P, P, P, F, F, F, P, I, I, I, I, I, I, I, I, P, S, P, P]
+        L.pa_decode_fp8.restype = I
         L.pa_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
         L.pa_copy_blocks.restype = I
         L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
@@ -102,12 +106,16 @@ def pa_version() -> int:
 
 
 def _dtype_code(t) -> int:
+    """float32 -> 0, bfloat16 -> 1; an FP8 cache is uint8 (e4m3 codes) or
+    torch.float8_e4m3fn -> 2."""
     import torch
     if t.dtype == torch.float32:
         return 0
     if t.dtype == torch.bfloat16:
         return 1
-    raise TypeError(f"cache dtype must be float32 or bfloat16, got {t.dtype}")
+    if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return 2
+    raise TypeError(f"dtype must be float32, bfloat16 or e4m3 codes, got {t.dtype}")
 
 
 def _ptr(t) -> int | None:
@@ -158,6 +166,66 @@ def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, error_wor
                                     _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_reshape_and_cache")
+
+
+def pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0,
+                             v_scale=1.0, error_word=None, stream=None) -> None:
+    """Quantising append: k_new/v_new (bf16 or fp32, [T][Hkv][D]) -> e4m3 codes
+    of x / scale in the FP8 pools (uint8 [NB][Hkv][bs][D])."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    if _dtype_code(k_cache) != 2:
+        raise TypeError("FP8 caches are uint8 (e4m3 codes) or float8_e4m3fn")
+    _check_cuda("k_new", k_new, ndim=3)
+    _check_cuda("v_new", v_new, k_new.dtype, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(v_cache.shape) != (nb, hkv, bs, d) or tuple(k_new.shape[1:]) != (hkv, d) \
+            or k_new.shape != v_new.shape or slot_mapping.shape[0] != k_new.shape[0]:
+        raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    rc = lib().pa_reshape_and_cache_fp8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                        _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                        int(k_new.shape[0]), hkv, d, bs, nb, float(k_scale),
+                                        float(v_scale), _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_reshape_and_cache_fp8")
+
+
+def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
+                  k_scale=1.0, v_scale=1.0, workspace=None, error_word=None,
+                  stream=None) -> None:
+    """Decode attention over FP8 pools (uint8 e4m3 codes) with bf16 q/out."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    if _dtype_code(k_cache) != 2:
+        raise TypeError("FP8 caches are uint8 (e4m3 codes) or float8_e4m3fn")
+    _check_cuda("q", q, torch.bfloat16, 3)
+    _check_cuda("out", out, torch.bfloat16, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                             _ptr(context_lens), float(scale), float(k_scale), float(v_scale),
+                             _ptr(out), B, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+                             int(max_context_len), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _ptr(error_word),
+                             _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_decode_fp8")
 
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None) -> None:

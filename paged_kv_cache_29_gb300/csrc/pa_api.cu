@@ -35,9 +35,13 @@ EncodeTiledFn encode_tiled() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int elem_bytes(pa_dtype d) { return d == PA_DTYPE_F32 ? 4 : 2; }
+int elem_bytes(pa_dtype d) { return d == PA_DTYPE_F32 ? 4 : d == PA_DTYPE_BF16 ? 2 : 1; }
 
+// Types of q, out and new rows.
 bool valid_dtype(pa_dtype d) { return d == PA_DTYPE_F32 || d == PA_DTYPE_BF16; }
+
+// Types a cache may hold.
+bool valid_cache_dtype(pa_dtype d) { return valid_dtype(d) || d == PA_DTYPE_FP8_E4M3; }
 
 // The pool viewed as a 3D tensor for TMA: x = element within a 128-byte
 // column half of a row, y = row (rows = blocks * kv_heads * block_size, stride
@@ -57,8 +61,9 @@ pa_status make_pool_map(CUtensorMap* map, const void* base, pa_dtype dtype, int 
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 16u, static_cast<cuuint32_t>(halves)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(map,
-                          dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          dtype == PA_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                          : dtype == PA_DTYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                           3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -100,6 +105,142 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int max_co
     return layout_for(num_seqs, num_heads, head_dim, max_context_len, partition_size).total;
 }
 
+// One decode call: q/out in act_dtype, the caches in dtype (act_dtype, or FP8
+// with bf16 q/out), K/V values scaled by k_scale/v_scale (1 unless FP8).
+pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale,
+                      float k_scale, float v_scale, void* out, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                      int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                      pa_dtype act_dtype, void* workspace, size_t workspace_bytes,
+                      int32_t* error_word, const pa_decode_options* options,
+                      struct CUstream_st* stream) {
+    const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
+    const int partition = (options && options->partition_size) ? options->partition_size
+                                                               : pa::kDefaultPartition;
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
+        !valid_cache_dtype(dtype) || !valid_dtype(act_dtype) || num_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
+    if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;   // NaN scale
+    if (head_dim > pa::kMaxHeadDim) return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_context_len) >
+        static_cast<long long>(max_blocks_per_seq) * block_size)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u) != 0)
+        return PA_ERR_INVALID_ARG;
+
+    const int group = num_heads / num_kv_heads;
+    const long long max_parts = max_context_len > 0 ? ceil_div(max_context_len, partition) : 1;
+    const long long chunk = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
+    if (max_parts * chunk * num_kv_heads > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
+
+    const WorkspaceLayout lay = layout_for(num_seqs, num_heads, head_dim, max_context_len, partition);
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
+        return PA_ERR_WORKSPACE;
+
+    const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+    const bool tma_shape = block_size % 16 == 0 && rows < 0x7fffffffLL &&
+                           (head_dim * elem_bytes(dtype)) % 128 == 0;
+    pa_kernel kernel = static_cast<pa_kernel>(kernel_req);
+    const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
+    if (fp8) {
+        // One kernel family: the FP8 tensor-core tile ring.
+        if (!tma_shape || !pa::has_fp8_instance(head_dim, group) ||
+            (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA))
+            return PA_ERR_UNSUPPORTED;
+        kernel = PA_KERNEL_MMA;
+    } else if (kernel == PA_KERNEL_AUTO) {
+        if (tma_shape && pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group))
+            kernel = PA_KERNEL_MMA;
+        else if (tma_shape && pa::has_tma_instance(PA_KERNEL_SIMT, dtype, head_dim, group))
+            kernel = PA_KERNEL_SIMT;
+        else
+            kernel = PA_KERNEL_GENERIC;
+    } else if (kernel != PA_KERNEL_GENERIC &&
+               (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group))) {
+        return PA_ERR_UNSUPPORTED;
+    }
+    if (kernel == PA_KERNEL_GENERIC &&
+        pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem)
+        return PA_ERR_UNSUPPORTED;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams base{};
+    base.k_cache = k_cache;
+    base.v_cache = v_cache;
+    base.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ml_off) : nullptr;
+    base.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.o_off) : nullptr;
+    base.items = reinterpret_cast<int4*>(ws + lay.items_off);
+    base.error_word = error_word;
+    base.scale_log2 = scale * kLog2e;
+    base.k_scale = k_scale;
+    base.v_scale = v_scale;
+    base.num_heads = num_heads;
+    base.num_kv_heads = num_kv_heads;
+    base.head_dim = head_dim;
+    base.block_size = block_size;
+    base.num_blocks = num_blocks;
+    base.max_blocks_per_seq = max_blocks_per_seq;
+    base.context_cap = max_context_len;
+    base.partition_size = partition;
+    base.max_parts = static_cast<int>(max_parts);
+
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap tk, tv;
+    int sm_count = 0;
+    if (kernel != PA_KERNEL_GENERIC) {
+        pa_status ps = make_pool_map(&tk, k_cache, dtype, head_dim, rows);
+        if (ps == PA_OK) ps = make_pool_map(&tv, v_cache, dtype, head_dim, rows);
+        if (ps != PA_OK) return ps;
+        static std::atomic<int> cached_sms[pa::kMaxDevices];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+        sm_count = dev < pa::kMaxDevices ? cached_sms[dev].load(std::memory_order_relaxed) : 0;
+        if (sm_count <= 0) {
+            if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sm_count <= 0)
+                return PA_ERR_CUDA;
+            if (dev < pa::kMaxDevices) cached_sms[dev].store(sm_count, std::memory_order_relaxed);
+        }
+    }
+    const size_t es = static_cast<size_t>(elem_bytes(act_dtype));   // q and out rows
+    // Batches above kPlanMaxSeqs sequences run as consecutive launches over
+    // slices of the batch; they reuse the workspace in stream order.
+    for (int s0 = 0; s0 < num_seqs; s0 += pa::kPlanMaxSeqs) {
+        const int bs_n = num_seqs - s0 < pa::kPlanMaxSeqs ? num_seqs - s0 : pa::kPlanMaxSeqs;
+        DecodeParams p = base;
+        const size_t qoff = static_cast<size_t>(s0) * num_heads * head_dim * es;
+        p.q = static_cast<const uint8_t*>(q) + qoff;
+        p.out = static_cast<uint8_t*>(out) + qoff;
+        p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
+        p.context_lens = context_lens + s0;
+        p.num_seqs = bs_n;
+        cudaError_t err;
+        if (kernel == PA_KERNEL_GENERIC) {
+            err = pa::launch_decode_generic(p, dtype, st);
+        } else {
+            err = fp8                      ? pa::launch_decode_fp8(tk, tv, p, sm_count, st)
+                  : kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
+                                            : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
+        }
+        if (err == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+        if (err != cudaSuccess) return PA_ERR_CUDA;
+        if (max_parts > 1) {
+            err = pa::launch_combine(p, act_dtype, st);
+            if (err != cudaSuccess) return PA_ERR_CUDA;
+        }
+    }
+    return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -139,7 +280,7 @@ pa_status pa_reshape_and_cache(const void* k_new, const void* v_new,
                                int num_blocks, pa_dtype dtype, int32_t* error_word,
                                struct CUstream_st* stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks <= 0 || !valid_dtype(dtype))
+        num_blocks <= 0 || !valid_cache_dtype(dtype))
         return PA_ERR_INVALID_ARG;
     const int row_bytes = head_dim * elem_bytes(dtype);
     if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
@@ -160,7 +301,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
                          int num_blocks, pa_dtype dtype, int32_t* error_word,
                          struct CUstream_st* stream) {
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks <= 0 || !valid_dtype(dtype))
+        num_blocks <= 0 || !valid_cache_dtype(dtype))
         return PA_ERR_INVALID_ARG;
     const int row_bytes = head_dim * elem_bytes(dtype);
     if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
@@ -183,120 +324,48 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
                        int max_context_len, pa_dtype dtype, void* workspace,
                        size_t workspace_bytes, int32_t* error_word,
                        const pa_decode_options* options, struct CUstream_st* stream) {
-    const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
-    const int partition = (options && options->partition_size) ? options->partition_size
-                                                               : pa::kDefaultPartition;
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
-        !valid_dtype(dtype) || num_heads % num_kv_heads != 0)
+    if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
+                       workspace_bytes, error_word, options, stream);
+}
+
+pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, void* out, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        int max_blocks_per_seq, int max_context_len, void* workspace,
+                        size_t workspace_bytes, int32_t* error_word,
+                        struct CUstream_st* stream) {
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || k_scale == INFINITY || v_scale == INFINITY)
         return PA_ERR_INVALID_ARG;
-    if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
-    if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
-    if (!(scale == scale)) return PA_ERR_INVALID_ARG;   // NaN scale
-    if (head_dim > pa::kMaxHeadDim) return PA_ERR_UNSUPPORTED;
-    if (static_cast<long long>(max_context_len) >
-        static_cast<long long>(max_blocks_per_seq) * block_size)
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                       out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_DTYPE_FP8_E4M3, PA_DTYPE_BF16,
+                       workspace, workspace_bytes, error_word, nullptr, stream);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                                   const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                   int num_tokens, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, float k_scale, float v_scale,
+                                   int32_t* error_word, struct CUstream_st* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || !valid_dtype(new_dtype) || !(k_scale > 0.0f) ||
+        !(v_scale > 0.0f) || k_scale == INFINITY || v_scale == INFINITY)
         return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PA_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    if (head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
         return PA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        (reinterpret_cast<uintptr_t>(block_tables) & 3u) != 0 ||
-        (reinterpret_cast<uintptr_t>(context_lens) & 3u) != 0)
-        return PA_ERR_INVALID_ARG;
-
-    const int group = num_heads / num_kv_heads;
-    const long long max_parts = max_context_len > 0 ? ceil_div(max_context_len, partition) : 1;
-    const long long chunk = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
-    if (max_parts * chunk * num_kv_heads > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
-
-    const WorkspaceLayout lay = layout_for(num_seqs, num_heads, head_dim, max_context_len, partition);
-    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
-        return PA_ERR_WORKSPACE;
-
-    const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
-    const bool tma_shape = block_size % 16 == 0 && rows < 0x7fffffffLL &&
-                           (head_dim * elem_bytes(dtype)) % 128 == 0;
-    pa_kernel kernel = static_cast<pa_kernel>(kernel_req);
-    if (kernel == PA_KERNEL_AUTO) {
-        if (tma_shape && pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group))
-            kernel = PA_KERNEL_MMA;
-        else if (tma_shape && pa::has_tma_instance(PA_KERNEL_SIMT, dtype, head_dim, group))
-            kernel = PA_KERNEL_SIMT;
-        else
-            kernel = PA_KERNEL_GENERIC;
-    } else if (kernel != PA_KERNEL_GENERIC &&
-               (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group))) {
-        return PA_ERR_UNSUPPORTED;
-    }
-    if (kernel == PA_KERNEL_GENERIC &&
-        pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem)
-        return PA_ERR_UNSUPPORTED;
-
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    DecodeParams base{};
-    base.k_cache = k_cache;
-    base.v_cache = v_cache;
-    base.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.ml_off) : nullptr;
-    base.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + lay.o_off) : nullptr;
-    base.items = reinterpret_cast<int4*>(ws + lay.items_off);
-    base.error_word = error_word;
-    base.scale_log2 = scale * kLog2e;
-    base.num_heads = num_heads;
-    base.num_kv_heads = num_kv_heads;
-    base.head_dim = head_dim;
-    base.block_size = block_size;
-    base.num_blocks = num_blocks;
-    base.max_blocks_per_seq = max_blocks_per_seq;
-    base.context_cap = max_context_len;
-    base.partition_size = partition;
-    base.max_parts = static_cast<int>(max_parts);
-
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    CUtensorMap tk, tv;
-    int sm_count = 0;
-    if (kernel != PA_KERNEL_GENERIC) {
-        pa_status ps = make_pool_map(&tk, k_cache, dtype, head_dim, rows);
-        if (ps == PA_OK) ps = make_pool_map(&tv, v_cache, dtype, head_dim, rows);
-        if (ps != PA_OK) return ps;
-        static std::atomic<int> cached_sms[pa::kMaxDevices];
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-        sm_count = dev < pa::kMaxDevices ? cached_sms[dev].load(std::memory_order_relaxed) : 0;
-        if (sm_count <= 0) {
-            if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                sm_count <= 0)
-                return PA_ERR_CUDA;
-            if (dev < pa::kMaxDevices) cached_sms[dev].store(sm_count, std::memory_order_relaxed);
-        }
-    }
-    const size_t es = static_cast<size_t>(elem_bytes(dtype));
-    // Batches above kPlanMaxSeqs sequences run as consecutive launches over
-    // slices of the batch; they reuse the workspace in stream order.
-    for (int s0 = 0; s0 < num_seqs; s0 += pa::kPlanMaxSeqs) {
-        const int bs_n = num_seqs - s0 < pa::kPlanMaxSeqs ? num_seqs - s0 : pa::kPlanMaxSeqs;
-        DecodeParams p = base;
-        const size_t qoff = static_cast<size_t>(s0) * num_heads * head_dim * es;
-        p.q = static_cast<const uint8_t*>(q) + qoff;
-        p.out = static_cast<uint8_t*>(out) + qoff;
-        p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
-        p.context_lens = context_lens + s0;
-        p.num_seqs = bs_n;
-        cudaError_t err;
-        if (kernel == PA_KERNEL_GENERIC) {
-            err = pa::launch_decode_generic(p, dtype, st);
-        } else {
-            err = kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
-                                          : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
-        }
-        if (err == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
-        if (err != cudaSuccess) return PA_ERR_CUDA;
-        if (max_parts > 1) {
-            err = pa::launch_combine(p, dtype, st);
-            if (err != cudaSuccess) return PA_ERR_CUDA;
-        }
-    }
-    return PA_OK;
+    const cudaError_t err = pa::launch_append_fp8(
+        k_new, v_new, new_dtype, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads,
+        head_dim, block_size, num_blocks, k_scale, v_scale, error_word,
+        reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,

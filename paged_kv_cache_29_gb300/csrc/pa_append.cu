@@ -7,6 +7,8 @@
 // vectors: one thread per 16-byte chunk of one (token, KV head) row, K and V
 // both. The read of k_new/v_new and the write into the pool are each one
 // coalesced pass over the row.
+#include <cuda_fp8.h>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -45,7 +47,83 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     }
 }
 
+// Quantising append into an FP8 (e4m3) cache: code = e4m3(x / scale), the
+// division in fp32 (IEEE, round to nearest), the conversion rounding to
+// nearest even and saturating at +-448. One thread per 16 codes (one 16-byte
+// store) of one (token, KV head) row; TIn is the new rows' type.
+template <typename TIn>
+__global__ void __launch_bounds__(kAppendThreads)
+append_fp8_kernel(const TIn* __restrict__ k_new, const TIn* __restrict__ v_new,
+                  const int64_t* __restrict__ slot_mapping, uint4* __restrict__ k_cache,
+                  uint4* __restrict__ v_cache, long long total_chunks, int chunks_per_row,
+                  int num_kv_heads, int block_size, long long num_slots, float k_scale,
+                  float v_scale, int32_t* error_word) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+         i < total_chunks; i += stride) {
+        const long long rowi = i / chunks_per_row;           // (token, kv head)
+        const int c = static_cast<int>(i - rowi * chunks_per_row);
+        const long long t = rowi / num_kv_heads;
+        const int h = static_cast<int>(rowi - t * num_kv_heads);
+        const long long slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (c == 0 && h == 0) raise_error(error_word, PA_DEVERR_SLOT);
+            continue;
+        }
+        const long long blk = slot / block_size;
+        const long long off = slot - blk * block_size;
+        const long long dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+        const TIn* ks = k_new + i * 16;
+        const TIn* vs = v_new + i * 16;
+        uint32_t kw[4], vw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t kb = 0, vb = 0;
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const float2 kx = make_float2(__fdiv_rn(ElemTraits<TIn>::load(ks + 4 * w + e), k_scale),
+                                              __fdiv_rn(ElemTraits<TIn>::load(ks + 4 * w + e + 1), k_scale));
+                const float2 vx = make_float2(__fdiv_rn(ElemTraits<TIn>::load(vs + 4 * w + e), v_scale),
+                                              __fdiv_rn(ElemTraits<TIn>::load(vs + 4 * w + e + 1), v_scale));
+                kb |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(kx, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+                vb |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(vx, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+            }
+            kw[w] = kb;
+            vw[w] = vb;
+        }
+        k_cache[dst] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        v_cache[dst] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_append_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                              const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                              int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float k_scale, float v_scale, int32_t* error_word,
+                              cudaStream_t stream) {
+    const int chunks_per_row = head_dim / 16;
+    const long long total = static_cast<long long>(num_tokens) * num_kv_heads * chunks_per_row;
+    if (total == 0) return cudaSuccess;
+    long long blocks = (total + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > 8192) blocks = 8192;
+    const long long num_slots = static_cast<long long>(num_blocks) * block_size;
+    if (new_dtype == PA_DTYPE_BF16) {
+        append_fp8_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+            slot_mapping, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), total,
+            chunks_per_row, num_kv_heads, block_size, num_slots, k_scale, v_scale, error_word);
+    } else {
+        append_fp8_kernel<float><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(
+            static_cast<const float*>(k_new), static_cast<const float*>(v_new), slot_mapping,
+            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), total, chunks_per_row,
+            num_kv_heads, block_size, num_slots, k_scale, v_scale, error_word);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                           void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,

@@ -236,7 +236,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // The next item's description and q are loaded one item ahead, so that an
     // item boundary costs no global-memory round trip.
     Math math;
-    math.setup(lane);
+    math.setup(lane, p);
     auto item_at = [&](int j) -> int4 {
         const int k = snake_item(c, j, C);
         return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);

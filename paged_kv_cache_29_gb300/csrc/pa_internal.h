@@ -24,6 +24,8 @@ struct DecodeParams {
     int4* items;                   // work items (sequence, KV head, partition, context length)
     int32_t* error_word;           // nullable
     float scale_log2;              // scale * log2(e): scores are kept in base 2
+    float k_scale;                 // FP8 caches: K value = k_scale * e4m3(code) (else 1)
+    float v_scale;                 // FP8 caches: V value = v_scale * e4m3(code) (else 1)
     int num_seqs;
     int num_heads;
     int num_kv_heads;
@@ -55,6 +57,19 @@ cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeParams& p, pa_dtype dtype, int sm_count,
                                cudaStream_t stream);
 bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group);
+
+// FP8 (e4m3) cache, bf16 q/out: tensor-core tile math (head dim 128; 1, 2, 4
+// or 8 query heads per KV head).
+cudaError_t launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, int sm_count, cudaStream_t stream);
+bool has_fp8_instance(int head_dim, int group);
+
+// Quantising append into an FP8 cache (new rows fp32 or bf16).
+cudaError_t launch_append_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                              const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                              int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float k_scale, float v_scale, int32_t* error_word,
+                              cudaStream_t stream);
 
 constexpr int kPlanMaxSeqs = 4096;   // sequences per persistent decode launch
 

@@ -80,6 +80,24 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
+// One warp copies q of (sequence s, KV head h) -- G rows of D bf16 -- into a
+// staging buffer whose rows are ROW_BYTES apart, with cp.async.
+template <int D, int G, int ROW_BYTES>
+__device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int s, int h, uint32_t qbuf,
+                                             int lane) {
+    constexpr int kChunksPerRow = D * 2 / 16;
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(
+        static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(s) * p.num_heads + h * G) * D);
+    for (int c = lane; c < G * kChunksPerRow; c += 32) {
+        const int g = c / kChunksPerRow, ch = c - g * kChunksPerRow;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         qbuf + static_cast<uint32_t>(g * ROW_BYTES + ch * 16)),
+                     "l"(q + static_cast<size_t>(g) * D * 2 + ch * 16)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Tensor-core tile math (bf16). Fragment layouts are those of mma.m16n8k16:
 // lane = 4 * gid + t4; accumulator c0,c1 = (row gid, cols 2t4, 2t4+1),
@@ -111,7 +129,7 @@ struct MmaMath {
     float m[2], l[2];
     int gid, t4;
 
-    __device__ __forceinline__ void setup(int lane) {
+    __device__ __forceinline__ void setup(int lane, const DecodeParams&) {
         gid = lane >> 2;
         t4 = lane & 3;
     }
@@ -119,17 +137,7 @@ struct MmaMath {
     // One warp copies q of (sequence s, KV head h) into the staging buffer.
     __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, uint32_t qbuf,
                                             int lane) const {
-        constexpr int kChunksPerRow = D * 2 / 16;
-        const uint8_t* q = reinterpret_cast<const uint8_t*>(static_cast<const T*>(p.q) +
-                                                            (static_cast<size_t>(s) * p.num_heads + h * G) * D);
-        for (int c = lane; c < G * kChunksPerRow; c += 32) {
-            const int g = c / kChunksPerRow, ch = c - g * kChunksPerRow;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                             qbuf + static_cast<uint32_t>(g * kQRowBytes + ch * 16)),
-                         "l"(q + static_cast<size_t>(g) * D * 2 + ch * 16)
-                         : "memory");
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        stage_q_rows<D, G, kQRowBytes>(p, s, h, qbuf, lane);
     }
 
     // Start an item: read q's B fragments from the staging buffer and clear
@@ -293,7 +301,7 @@ struct SimtMath {
     float m[G], l[G];
     int rr, ch;
 
-    __device__ __forceinline__ void setup(int lane) {
+    __device__ __forceinline__ void setup(int lane, const DecodeParams&) {
         rr = lane / kLpr;
         ch = lane % kLpr;
     }

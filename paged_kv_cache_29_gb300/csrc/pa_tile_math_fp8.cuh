@@ -1,0 +1,226 @@
+// pa_tile_math_fp8.cuh -- per-tile math for an FP8 (e4m3) KV cache with bf16 q
+// and output.
+//
+// Each cached element is an e4m3 code with one scale per tensor: value =
+// k_scale * e4m3(code) for K, v_scale * e4m3(code) for V (an FP8 cache halves
+// the bytes per token; scales are per tensor: "Forward Deployed Engineering
+// Interview", Chapter 2 "Batching and the KV Cache"). The codes are widened to
+// f16 in registers (cvt.rn.f16x2.e4m3x2, exact: every e4m3 value is an f16
+// value) and multiplied with m16n8k16 f16 MMAs accumulating in fp32; the
+// online softmax is that of MmaMath. The scales never touch the tile:
+//   scores  S = (q * scale * log2(e) * k_scale) . code(K): q is scaled and
+//           rounded to f16 once per item, so the accumulators are base-2
+//           scores;
+//   output  O = v_scale * sum_i p_i code(V_i): v_scale is applied when the
+//           warp state is written.
+//
+// Fragment assignment (lane = 4 * gid + t4; the dot products and the output
+// rows are sums and rows, so any fixed assignment of dims works when A, B and
+// the output agree on it):
+//   QK  k-step j (0..7) covers, for lane t4, dims 16 c + 4 (j % 4) .. + 3 of
+//       chunk c = 2 t4 + j / 4: the A registers of row gid are that 4-byte
+//       word of K row gid (two codes per register), q' is dealt the same way.
+//       Each lane reads whole 16-byte chunks 2 t4 and 2 t4 + 1 of rows gid
+//       and gid + 8; with the 128-byte swizzle the 8 lanes of a phase hit 8
+//       different chunks (no bank conflicts).
+//   PV  m-tile mt covers, for lane gid, dims 16 gid + 2 mt (row gid) and
+//       16 gid + 2 mt + 1 (row gid + 8); the A registers pair tokens (2 t4,
+//       2 t4 + 1) and (2 t4 + 8, 2 t4 + 9), read as chunk gid of those four
+//       token rows and interleaved with byte permutes.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "pa_tile_math.cuh"
+
+namespace pa {
+
+// Two e4m3 codes in each 16-bit half of w -> two f16x2 registers (the low
+// byte of each pair becomes the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// D (16x8, fp32) += A (16x16, f16, row) . B (16x8, f16, col)
+__device__ __forceinline__ void mma_16816_f16(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D, int G>
+struct Fp8MmaMath {
+    using T = __nv_bfloat16;                    // q and out
+    using Geom = TileGeom<uint8_t, D>;
+    static_assert(D == 128, "one 128-byte row of codes per token");
+    static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
+    static constexpr int kSteps = D / 16;
+
+    static constexpr bool kQInSmem = true;
+    static constexpr int kQRowBytes = D * 2 + 16;
+    static constexpr int kQBufBytes = ((G * kQRowBytes + 127) / 128) * 128;
+    struct QRegs {};
+
+    uint32_t qb[kSteps][2];
+    float o[kSteps][4];
+    float m[2], l[2];
+    float qscale, vscale;
+    int gid, t4;
+
+    __device__ __forceinline__ void setup(int lane, const DecodeParams& p) {
+        gid = lane >> 2;
+        t4 = lane & 3;
+        qscale = p.scale_log2 * p.k_scale;
+        vscale = p.v_scale;
+    }
+
+    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, uint32_t qbuf,
+                                            int lane) const {
+        stage_q_rows<D, G, kQRowBytes>(p, s, h, qbuf, lane);
+    }
+
+    // q' = q * scale * log2(e) * k_scale in f16, dealt as the k-steps deal
+    // the dims; the softmax state is cleared. Lanes of heads gid >= G read
+    // nothing (the buffer holds G rows) and hold zeros.
+    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf) {
+        const uint8_t* row = qbuf + gid * kQRowBytes;
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j) {
+            const int d0 = 16 * (2 * t4 + (j >> 2)) + 4 * (j & 3);
+            qb[j][0] = 0u;
+            qb[j][1] = 0u;
+            if (gid < G) {
+                const uint2 w = *reinterpret_cast<const uint2*>(row + d0 * 2);
+                qb[j][0] = pack_f16x2(bf16_lo(w.x) * qscale, bf16_hi(w.x) * qscale);
+                qb[j][1] = pack_f16x2(bf16_lo(w.y) * qscale, bf16_hi(w.y) * qscale);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[j][i] = 0.f;
+        }
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+    }
+
+    __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
+                                         float /*scale_log2: folded into q'*/, int /*lane*/) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 r0 = lds128(swizzled(kbase, gid, 2 * t4 + half));
+            const uint4 r1 = lds128(swizzled(kbase, gid + 8, 2 * t4 + half));
+            const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+            const uint32_t w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * half + jj;
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(w0[jj], a0, a2);
+                e4m3x4_to_f16x2x2(w1[jj], a1, a3);
+                mma_16816_f16(c, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+            }
+        }
+        if (valid < kTileRows) {
+            if (gid >= valid) c[0] = c[1] = -INFINITY;
+            if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+        }
+        float mx0 = fmaxf(c[0], c[2]);
+        float mx1 = fmaxf(c[1], c[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0);
+        const float mn1 = fmaxf(m[1], mx1);
+        const float al0 = fast_exp2(m[0] - mn0);
+        const float al1 = fast_exp2(m[1] - mn1);
+        const float p0 = fast_exp2(c[0] - mn0);
+        const float p1 = fast_exp2(c[1] - mn1);
+        const float p2 = fast_exp2(c[2] - mn0);
+        const float p3 = fast_exp2(c[3] - mn1);
+        l[0] = l[0] * al0 + (p0 + p2);
+        l[1] = l[1] * al1 + (p1 + p3);
+        m[0] = mn0;
+        m[1] = mn1;
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        // P^T as the f16 B operand, gathered as in MmaMath: lane (gid, t4)
+        // needs P[tokens 2t4, 2t4+1][head gid] and P[tokens 2t4+8, 2t4+9][head gid].
+        const uint32_t p01 = pack_f16x2(p0, p1);
+        const uint32_t p23 = pack_f16x2(p2, p3);
+        const int src_a = 8 * t4 + (gid >> 1);
+        const uint32_t v0 = __shfl_sync(0xffffffffu, p01, src_a);
+        const uint32_t v1 = __shfl_sync(0xffffffffu, p01, src_a + 4);
+        const uint32_t u0 = __shfl_sync(0xffffffffu, p23, src_a);
+        const uint32_t u1 = __shfl_sync(0xffffffffu, p23, src_a + 4);
+        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+        const uint32_t b0 = prmt(v0, v1, sel);
+        const uint32_t b1 = prmt(u0, u1, sel);
+        // V rows 2t4, 2t4+1, 2t4+8, 2t4+9, chunk gid (dims 16 gid .. 16 gid + 15).
+        const uint4 x0 = lds128(swizzled(vbase, 2 * t4, gid));
+        const uint4 x1 = lds128(swizzled(vbase, 2 * t4 + 1, gid));
+        const uint4 x2 = lds128(swizzled(vbase, 2 * t4 + 8, gid));
+        const uint4 x3 = lds128(swizzled(vbase, 2 * t4 + 9, gid));
+        const uint32_t e0[4] = {x0.x, x0.y, x0.z, x0.w};
+        const uint32_t e1[4] = {x1.x, x1.y, x1.z, x1.w};
+        const uint32_t e2[4] = {x2.x, x2.y, x2.z, x2.w};
+        const uint32_t e3[4] = {x3.x, x3.y, x3.z, x3.w};
+        // Rows past the sequence hold whatever the pool holds (possibly NaN
+        // codes): zero their V values so that 0 * V stays 0.
+        const int tk = 2 * t4;
+        const uint32_t mlo = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+        const uint32_t mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt) {
+            // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
+            const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
+            const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(lo, a0, a1);
+            e4m3x4_to_f16x2x2(hi, a2, a3);
+            mma_16816_f16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+        }
+    }
+
+    // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o scaled by v_scale.
+    __device__ __forceinline__ void write_state(float* st, int /*lane*/) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+        }
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+        if (gid == 0) {
+            if (h0 < G) { st[h0] = m[0]; st[G + h0] = l[0]; }
+            if (h1 < G) { st[h1] = m[1]; st[G + h1] = l[1]; }
+        }
+        float* so = st + 2 * G;
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt) {
+            const int d0 = 16 * gid + 2 * mt;
+            if (h0 < G) { so[h0 * D + d0] = o[mt][0] * vscale; so[h0 * D + d0 + 1] = o[mt][2] * vscale; }
+            if (h1 < G) { so[h1 * D + d0] = o[mt][1] * vscale; so[h1 * D + d0 + 1] = o[mt][3] * vscale; }
+        }
+    }
+};
+
+}  // namespace pa

@@ -20,10 +20,14 @@ workloads:
   prefix_shared  bf16, 64 samples forked from one 4,096-token prompt (256
                  shared blocks, reference count 64) plus private tails of
                  uniform [0, 300] tokens and the token appended this step
+  8b_gqa_fp8     the 8b_gqa batch over an FP8 (e4m3) cache with per-tensor
+                 scales 1.0 (uncalibrated); q and the new K/V rows stay bf16
+                 and the append quantises them
 
 Every value of q, of the new K/V rows and of the whole pool (used or not) is
 drawn N(0, 1) in fp32 and stored in the cache dtype (bf16 by round to nearest
-even). The pool holds 1.25x the blocks the batch needs (the tiny workload: 32)
+even). An FP8 pool holds e4m3 codes of N(0, 1) draws, made by PyTorch's
+float8_e4m3fn conversion; q and the new rows of an FP8 step are bf16. The pool holds 1.25x the blocks the batch needs (the tiny workload: 32)
 and hands them out in a seeded random order, so a sequence's blocks are
 scattered. Lengths count the token appended by this step: the cache holds
 n - 1 rows before the step and n after it. Unused block-table entries hold -1.
@@ -40,7 +44,8 @@ import numpy as np
 from .block_manager import BlockManager
 
 # Seeds of the five named workloads, in the order listed above.
-WORKLOAD_SEEDS = {"tiny": 0, "7b_mha": 1, "8b_gqa": 2, "long_skew": 3, "prefix_shared": 4}
+WORKLOAD_SEEDS = {"tiny": 0, "7b_mha": 1, "8b_gqa": 2, "long_skew": 3, "prefix_shared": 4,
+                  "8b_gqa_fp8": 2}     # the 8b_gqa batch (same lengths and tables)
 PAD_BLOCK = -1
 
 
@@ -56,17 +61,35 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _torch_e4m3():
+    import torch
+    return torch, torch.float8_e4m3fn
+
+
 def to_cache_dtype(x: np.ndarray, cache_dtype: str) -> np.ndarray:
     if cache_dtype == "f32":
         return np.ascontiguousarray(x, dtype=np.float32)
     if cache_dtype == "bf16":
         return round_to_bf16_bits(x)
+    if cache_dtype == "fp8":
+        torch, e4m3 = _torch_e4m3()
+        t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(e4m3)
+        return t.view(torch.uint8).numpy().copy()
     raise ValueError(f"unknown cache dtype {cache_dtype!r}")
 
 
 def as_f32(x: np.ndarray, cache_dtype: str) -> np.ndarray:
     """Values of a cache-dtype array as fp32 (exact)."""
-    return bf16_bits_to_f32(x) if cache_dtype == "bf16" else np.asarray(x, dtype=np.float32)
+    if cache_dtype == "bf16":
+        return bf16_bits_to_f32(x)
+    if cache_dtype == "fp8":
+        torch, e4m3 = _torch_e4m3()
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).view(e4m3).float().numpy()
+    return np.asarray(x, dtype=np.float32)
+
+
+_STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8}
+_BYTES = {"f32": 4, "bf16": 2, "fp8": 1}
 
 
 _CHUNK = 1 << 22
@@ -77,7 +100,7 @@ def _normal(rng: np.random.Generator, shape, cache_dtype: str) -> np.ndarray:
     chunks, each drawn from its own child seed of one SeedSequence taken from
     ``rng``, so the values do not depend on how many threads fill them."""
     n = int(np.prod(shape)) if len(shape) else 1
-    out = np.empty(n, dtype=np.float32 if cache_dtype == "f32" else np.uint16)
+    out = np.empty(n, dtype=_STORAGE[cache_dtype])
     root = np.random.SeedSequence(int(rng.integers(0, 2**63 - 1)))
     chunks = list(range(0, n, _CHUNK))
     seeds = root.spawn(len(chunks))
@@ -106,7 +129,7 @@ class DecodeStep:
     append (k_new/v_new into slot_mapping) and then attending over
     context_lens tokens per sequence is the step."""
     name: str
-    cache_dtype: str                  # "f32" or "bf16"
+    cache_dtype: str                  # "f32", "bf16" or "fp8" (e4m3 codes)
     num_heads: int
     num_kv_heads: int
     head_dim: int
@@ -122,6 +145,13 @@ class DecodeStep:
     scale: float
     seed: int
     meta: dict = field(default_factory=dict)
+    act_dtype: str = ""               # dtype of q, out, k_new, v_new ("" = cache_dtype)
+    k_scale: float = 1.0              # FP8 caches: value = scale * e4m3(code)
+    v_scale: float = 1.0
+
+    def __post_init__(self):
+        if not self.act_dtype:
+            self.act_dtype = self.cache_dtype
 
     @property
     def num_seqs(self) -> int:
@@ -141,7 +171,13 @@ class DecodeStep:
 
     @property
     def elem_bytes(self) -> int:
-        return 4 if self.cache_dtype == "f32" else 2
+        """Bytes per cache element."""
+        return _BYTES[self.cache_dtype]
+
+    @property
+    def act_bytes(self) -> int:
+        """Bytes per element of q, out and the new K/V rows."""
+        return _BYTES[self.act_dtype]
 
 
 def build_step(name: str, context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
@@ -191,9 +227,10 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
     for src, dst in cow_pairs:           # copy-on-write copies made while building
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
-    q = _normal(rng, (B, num_heads, head_dim), cache_dtype)
-    k_new = _normal(rng, (B, num_kv_heads, head_dim), cache_dtype)
-    v_new = _normal(rng, (B, num_kv_heads, head_dim), cache_dtype)
+    act = "bf16" if cache_dtype == "fp8" else cache_dtype
+    q = _normal(rng, (B, num_heads, head_dim), act)
+    k_new = _normal(rng, (B, num_kv_heads, head_dim), act)
+    v_new = _normal(rng, (B, num_kv_heads, head_dim), act)
     used = sorted({b for t in tables for b in t})
     meta = dict(meta, unique_blocks=len(used), max_blocks_per_seq=max_blocks)
     return DecodeStep(name=name, cache_dtype=cache_dtype, num_heads=num_heads,
@@ -202,7 +239,7 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
                       k_cache=k_cache, v_cache=v_cache, block_tables=bt,
                       context_lens=np.asarray(lens, dtype=np.int32),
                       scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale),
-                      seed=seed, meta=meta)
+                      seed=seed, meta=meta, act_dtype=act)
 
 
 # ---- the five named workloads ------------------------------------------------
@@ -234,6 +271,13 @@ def gqa_8b(seed: int = WORKLOAD_SEEDS["8b_gqa"], batch: int = 128) -> DecodeStep
     lens = gqa_8b_lengths(rng, batch)
     return build_step("8b_gqa", lens, num_heads=32, num_kv_heads=8, head_dim=128,
                       seed=seed, rng=rng)
+
+
+def gqa_8b_fp8(seed: int = WORKLOAD_SEEDS["8b_gqa_fp8"], batch: int = 128) -> DecodeStep:
+    rng = np.random.default_rng(seed)
+    lens = gqa_8b_lengths(rng, batch)
+    return build_step("8b_gqa_fp8", lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                      cache_dtype="fp8", seed=seed, rng=rng)
 
 
 def long_skew(seed: int = WORKLOAD_SEEDS["long_skew"]) -> DecodeStep:
@@ -284,6 +328,7 @@ WORKLOADS = {
     "8b_gqa": gqa_8b,
     "long_skew": long_skew,
     "prefix_shared": prefix_shared,
+    "8b_gqa_fp8": gqa_8b_fp8,
 }
 
 
