@@ -122,6 +122,7 @@ struct MmaMath {
     static constexpr bool kQInSmem = true;
     static constexpr int kQRowBytes = D * 2 + 16;
     static constexpr int kQBufBytes = ((G * kQRowBytes + 127) / 128) * 128;
+    static constexpr int kTilesPerStep = 1;
     struct QRegs {};
 
     uint32_t qb[kSteps][2];
@@ -193,14 +194,19 @@ struct MmaMath {
         const float p3 = fast_exp2(c[3] - mn1);
         l[0] = l[0] * al0 + (p0 + p2);
         l[1] = l[1] * al1 + (p1 + p3);
+        // The rescale factor is exactly 1 where the max did not grow: skip the
+        // multiply when that holds for the whole warp.
+        const bool grew = __any_sync(0xffffffffu, (mn0 != m[0]) | (mn1 != m[1]));
         m[0] = mn0;
         m[1] = mn1;
+        if (grew) {
 #pragma unroll
-        for (int mt = 0; mt < kSteps; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int mt = 0; mt < kSteps; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
         }
         // P^T as the B operand: lane (gid, t4) needs P[token 2t4, 2t4+1][head gid]
         // (b0) and P[token 2t4+8, 2t4+9][head gid] (b1). Lane (g', t') holds
@@ -290,6 +296,7 @@ struct SimtMath {
     // loads it (the extra registers would spill).
     static constexpr bool kPrefetch = G * kEpc <= 32;
     static constexpr bool kQInSmem = false;
+    static constexpr int kTilesPerStep = 1;
     static constexpr int kQBufBytes = 0;
     struct QRegs {
         float f[kPrefetch ? G : 1][kPrefetch ? kEpc : 1];

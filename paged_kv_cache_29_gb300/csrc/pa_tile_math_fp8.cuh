@@ -114,9 +114,8 @@ struct Fp8MmaMath {
         l[0] = l[1] = 0.f;
     }
 
-    __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
-                                         float /*scale_log2: folded into q'*/, int /*lane*/) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T of one 16-row tile: c = S^T[token gid, gid + 8][heads 2 t4, 2 t4 + 1].
+    __device__ __forceinline__ void qk(uint32_t kbase, int valid, float* c) const {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint4 r0 = lds128(swizzled(kbase, gid, 2 * t4 + half));
@@ -136,6 +135,72 @@ struct Fp8MmaMath {
             if (gid >= valid) c[0] = c[1] = -INFINITY;
             if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
         }
+    }
+
+    // P^T B fragments of one tile from its probabilities (as in MmaMath):
+    // lane (gid, t4) gets P[tokens 2t4, 2t4+1][head gid] and P[tokens 2t4+8,
+    // 2t4+9][head gid].
+    __device__ __forceinline__ void p_fragments(float p0, float p1, float p2, float p3,
+                                                uint32_t& b0, uint32_t& b1) const {
+        const uint32_t p01 = pack_f16x2(p0, p1);
+        const uint32_t p23 = pack_f16x2(p2, p3);
+        const int src_a = 8 * t4 + (gid >> 1);
+        const uint32_t v0 = __shfl_sync(0xffffffffu, p01, src_a);
+        const uint32_t v1 = __shfl_sync(0xffffffffu, p01, src_a + 4);
+        const uint32_t u0 = __shfl_sync(0xffffffffu, p23, src_a);
+        const uint32_t u1 = __shfl_sync(0xffffffffu, p23, src_a + 4);
+        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+        b0 = prmt(v0, v1, sel);
+        b1 = prmt(u0, u1, sel);
+    }
+
+    // O^T += V^T . P^T over one 16-row tile: V rows 2t4, 2t4+1, 2t4+8, 2t4+9,
+    // chunk gid (dims 16 gid .. 16 gid + 15). Rows past the sequence hold
+    // whatever the pool holds (possibly NaN codes): their V values are zeroed
+    // so that 0 * V stays 0.
+    __device__ __forceinline__ void pv(uint32_t vbase, int valid, uint32_t b0, uint32_t b1) {
+        const uint4 x0 = lds128(swizzled(vbase, 2 * t4, gid));
+        const uint4 x1 = lds128(swizzled(vbase, 2 * t4 + 1, gid));
+        const uint4 x2 = lds128(swizzled(vbase, 2 * t4 + 8, gid));
+        const uint4 x3 = lds128(swizzled(vbase, 2 * t4 + 9, gid));
+        const uint32_t e0[4] = {x0.x, x0.y, x0.z, x0.w};
+        const uint32_t e1[4] = {x1.x, x1.y, x1.z, x1.w};
+        const uint32_t e2[4] = {x2.x, x2.y, x2.z, x2.w};
+        const uint32_t e3[4] = {x3.x, x3.y, x3.z, x3.w};
+        if (valid == kTileRows) {
+#pragma unroll
+            for (int mt = 0; mt < kSteps; ++mt) {
+                // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
+                const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
+                const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(lo, a0, a1);
+                e4m3x4_to_f16x2x2(hi, a2, a3);
+                mma_16816_f16(o[mt], a0, a1, a2, a3, b0, b1);
+            }
+        } else {
+            const int tk = 2 * t4;
+            const uint32_t mlo = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+            const uint32_t mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < kSteps; ++mt) {
+                const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
+                const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(lo, a0, a1);
+                e4m3x4_to_f16x2x2(hi, a2, a3);
+                mma_16816_f16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+            }
+        }
+    }
+
+    // One 16-row tile per step.
+    __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
+                                         float /*scale_log2: folded into q'*/, int /*lane*/) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        qk(kbase, valid, c);
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
 #pragma unroll
@@ -153,52 +218,71 @@ struct Fp8MmaMath {
         const float p3 = fast_exp2(c[3] - mn1);
         l[0] = l[0] * al0 + (p0 + p2);
         l[1] = l[1] * al1 + (p1 + p3);
+        // The rescale factor is exactly 1 where the max did not grow: skip the
+        // multiply when that holds for the whole warp.
+        const bool grew = __any_sync(0xffffffffu, (mn0 != m[0]) | (mn1 != m[1]));
         m[0] = mn0;
         m[1] = mn1;
+        if (grew) {
 #pragma unroll
-        for (int mt = 0; mt < kSteps; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int mt = 0; mt < kSteps; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
         }
-        // P^T as the f16 B operand, gathered as in MmaMath: lane (gid, t4)
-        // needs P[tokens 2t4, 2t4+1][head gid] and P[tokens 2t4+8, 2t4+9][head gid].
-        const uint32_t p01 = pack_f16x2(p0, p1);
-        const uint32_t p23 = pack_f16x2(p2, p3);
-        const int src_a = 8 * t4 + (gid >> 1);
-        const uint32_t v0 = __shfl_sync(0xffffffffu, p01, src_a);
-        const uint32_t v1 = __shfl_sync(0xffffffffu, p01, src_a + 4);
-        const uint32_t u0 = __shfl_sync(0xffffffffu, p23, src_a);
-        const uint32_t u1 = __shfl_sync(0xffffffffu, p23, src_a + 4);
-        const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
-        const uint32_t b0 = prmt(v0, v1, sel);
-        const uint32_t b1 = prmt(u0, u1, sel);
-        // V rows 2t4, 2t4+1, 2t4+8, 2t4+9, chunk gid (dims 16 gid .. 16 gid + 15).
-        const uint4 x0 = lds128(swizzled(vbase, 2 * t4, gid));
-        const uint4 x1 = lds128(swizzled(vbase, 2 * t4 + 1, gid));
-        const uint4 x2 = lds128(swizzled(vbase, 2 * t4 + 8, gid));
-        const uint4 x3 = lds128(swizzled(vbase, 2 * t4 + 9, gid));
-        const uint32_t e0[4] = {x0.x, x0.y, x0.z, x0.w};
-        const uint32_t e1[4] = {x1.x, x1.y, x1.z, x1.w};
-        const uint32_t e2[4] = {x2.x, x2.y, x2.z, x2.w};
-        const uint32_t e3[4] = {x3.x, x3.y, x3.z, x3.w};
-        // Rows past the sequence hold whatever the pool holds (possibly NaN
-        // codes): zero their V values so that 0 * V stays 0.
-        const int tk = 2 * t4;
-        const uint32_t mlo = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
-        const uint32_t mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+        uint32_t b0, b1;
+        p_fragments(p0, p1, p2, p3, b0, b1);
+        pv(vbase, valid, b0, b1);
+    }
+
+    // Two consecutive 16-row tiles (32 rows) per step: one max, one rescale
+    // and one state update for both. valid1 may be 0 (no second tile).
+    static constexpr int kTilesPerStep = 1;
+    __device__ __forceinline__ void tile2(uint32_t kb0, uint32_t vb0, int valid0, uint32_t kb1,
+                                          uint32_t vb1, int valid1) {
+        float ca[4] = {0.f, 0.f, 0.f, 0.f};
+        float cb[4] = {0.f, 0.f, 0.f, 0.f};
+        qk(kb0, valid0, ca);
+        qk(kb1, valid1, cb);
+        float mx0 = fmaxf(fmaxf(ca[0], ca[2]), fmaxf(cb[0], cb[2]));
+        float mx1 = fmaxf(fmaxf(ca[1], ca[3]), fmaxf(cb[1], cb[3]));
 #pragma unroll
-        for (int mt = 0; mt < kSteps; ++mt) {
-            // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
-            const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
-            const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(lo, a0, a1);
-            e4m3x4_to_f16x2x2(hi, a2, a3);
-            mma_16816_f16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
+        const float mn0 = fmaxf(m[0], mx0);
+        const float mn1 = fmaxf(m[1], mx1);
+        const float al0 = fast_exp2(m[0] - mn0);
+        const float al1 = fast_exp2(m[1] - mn1);
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            ca[i] = fast_exp2(ca[i] - mn0);
+            ca[i + 1] = fast_exp2(ca[i + 1] - mn1);
+            cb[i] = fast_exp2(cb[i] - mn0);
+            cb[i + 1] = fast_exp2(cb[i + 1] - mn1);
+        }
+        l[0] = l[0] * al0 + ((ca[0] + ca[2]) + (cb[0] + cb[2]));
+        l[1] = l[1] * al1 + ((ca[1] + ca[3]) + (cb[1] + cb[3]));
+        const bool grew = __any_sync(0xffffffffu, (mn0 != m[0]) | (mn1 != m[1]));
+        m[0] = mn0;
+        m[1] = mn1;
+        if (grew) {
+#pragma unroll
+            for (int mt = 0; mt < kSteps; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        uint32_t b0, b1;
+        p_fragments(ca[0], ca[1], ca[2], ca[3], b0, b1);
+        pv(vb0, valid0, b0, b1);
+        p_fragments(cb[0], cb[1], cb[2], cb[3], b0, b1);
+        pv(vb1, valid1, b0, b1);
     }
 
     // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o scaled by v_scale.
