@@ -85,9 +85,7 @@ template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
 __global__ void __launch_bounds__((W + 1) * 32, MIN_CTAS)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-    // A consumer step takes TPW consecutive tiles (stages).
-    constexpr int TPW = Math::kTilesPerStep;
-    static_assert(STAGES % (W * TPW) == 0, "each ring stage must belong to exactly one consumer warp");
+    static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
     using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes>;
@@ -178,12 +176,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
             if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
             // The item's tiles are padded with data-less slots up to a multiple
-            // of W * TPW, so that every item starts at a stream index divisible
-            // by W * TPW and warp w always takes the same tiles of the item
-            // (w * TPW .. w * TPW + TPW - 1, then those + W * TPW, ...): the
+            // of W, so that every item starts at a stream index divisible by W
+            // and warp w always takes tiles w, w + W, ... of the item: the
             // rounding of an item's result never depends on what the CTA
             // streamed before it.
-            const int span = ((ntiles + W * TPW - 1) / (W * TPW)) * (W * TPW);
+            const int span = ((ntiles + W - 1) / W) * W;
             for (int tt = 0; tt < span; ++tt, ++t) {
                 const int tok = lo + kTileRows * tt;
                 const bool data = tt < ntiles && !cur_bad;
@@ -276,44 +273,25 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             math.begin(p, q_next);
             if (it_next.x >= 0) math.load_q(p, it_next.x, it_next.y, q_next);
         }
-        // padded as the producer pads
-        const int span = ((ntiles + W * TPW - 1) / (W * TPW)) * (W * TPW);
+        const int span = ((ntiles + W - 1) / W) * W;   // padded as the producer pads
         bool bad = false;
         if (!aborted) {
-            for (int t = t0 + warp * TPW; t < t0 + span; t += W * TPW) {
-                bool got = true;
-#pragma unroll
-                for (int i = 0; i < TPW; ++i)
-                    got &= mbar_wait(smem_addr(&full[(t + i) % STAGES]), ((t + i) / STAGES) & 1);
+            for (int t = t0 + warp; t < t0 + span; t += W) {
+                const int stage = t % STAGES;
+                const bool got = mbar_wait(smem_addr(&full[stage]), (t / STAGES) & 1);
                 if (!__all_sync(0xffffffffu, got)) {
                     aborted = true;
                     break;
                 }
-                bool step_bad = false;
-#pragma unroll
-                for (int i = 0; i < TPW; ++i) step_bad |= stage_bad[(t + i) % STAGES] != 0;
-                if (step_bad) {
+                if (stage_bad[stage]) {
                     bad = true;
                 } else if (t - t0 < ntiles) {
                     const int valid = min(kTileRows, hi - (lo + kTileRows * (t - t0)));
-                    const uint32_t kb = ring_addr + (t % STAGES) * Geom::kStageBytes;
-                    if constexpr (TPW == 1) {
-                        math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
-                    } else {
-                        // Second tile: rows past hi (or a data-less slot) count as invalid.
-                        const int valid1 = t + 1 - t0 < ntiles
-                                               ? min(kTileRows, hi - (lo + kTileRows * (t + 1 - t0)))
-                                               : 0;
-                        const uint32_t kb1 = ring_addr + ((t + 1) % STAGES) * Geom::kStageBytes;
-                        math.tile2(kb, kb + Geom::kTileBytes, valid, kb1, kb1 + Geom::kTileBytes,
-                                   valid1);
-                    }
+                    const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
+                    math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
                 }
                 __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int i = 0; i < TPW; ++i) mbar_arrive(smem_addr(&empty[(t + i) % STAGES]));
-                }
+                if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
             }
         }
         it = it_next;

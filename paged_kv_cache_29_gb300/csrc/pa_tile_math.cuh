@@ -122,7 +122,6 @@ struct MmaMath {
     static constexpr bool kQInSmem = true;
     static constexpr int kQRowBytes = D * 2 + 16;
     static constexpr int kQBufBytes = ((G * kQRowBytes + 127) / 128) * 128;
-    static constexpr int kTilesPerStep = 1;
     struct QRegs {};
 
     uint32_t qb[kSteps][2];
@@ -296,7 +295,6 @@ struct SimtMath {
     // loads it (the extra registers would spill).
     static constexpr bool kPrefetch = G * kEpc <= 32;
     static constexpr bool kQInSmem = false;
-    static constexpr int kTilesPerStep = 1;
     static constexpr int kQBufBytes = 0;
     struct QRegs {
         float f[kPrefetch ? G : 1][kPrefetch ? kEpc : 1];

@@ -237,54 +237,6 @@ struct Fp8MmaMath {
         pv(vbase, valid, b0, b1);
     }
 
-    // Two consecutive 16-row tiles (32 rows) per step: one max, one rescale
-    // and one state update for both. valid1 may be 0 (no second tile).
-    static constexpr int kTilesPerStep = 1;
-    __device__ __forceinline__ void tile2(uint32_t kb0, uint32_t vb0, int valid0, uint32_t kb1,
-                                          uint32_t vb1, int valid1) {
-        float ca[4] = {0.f, 0.f, 0.f, 0.f};
-        float cb[4] = {0.f, 0.f, 0.f, 0.f};
-        qk(kb0, valid0, ca);
-        qk(kb1, valid1, cb);
-        float mx0 = fmaxf(fmaxf(ca[0], ca[2]), fmaxf(cb[0], cb[2]));
-        float mx1 = fmaxf(fmaxf(ca[1], ca[3]), fmaxf(cb[1], cb[3]));
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0);
-        const float mn1 = fmaxf(m[1], mx1);
-        const float al0 = fast_exp2(m[0] - mn0);
-        const float al1 = fast_exp2(m[1] - mn1);
-#pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-            ca[i] = fast_exp2(ca[i] - mn0);
-            ca[i + 1] = fast_exp2(ca[i + 1] - mn1);
-            cb[i] = fast_exp2(cb[i] - mn0);
-            cb[i + 1] = fast_exp2(cb[i + 1] - mn1);
-        }
-        l[0] = l[0] * al0 + ((ca[0] + ca[2]) + (cb[0] + cb[2]));
-        l[1] = l[1] * al1 + ((ca[1] + ca[3]) + (cb[1] + cb[3]));
-        const bool grew = __any_sync(0xffffffffu, (mn0 != m[0]) | (mn1 != m[1]));
-        m[0] = mn0;
-        m[1] = mn1;
-        if (grew) {
-#pragma unroll
-            for (int mt = 0; mt < kSteps; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-            }
-        }
-        uint32_t b0, b1;
-        p_fragments(ca[0], ca[1], ca[2], ca[3], b0, b1);
-        pv(vb0, valid0, b0, b1);
-        p_fragments(cb[0], cb[1], cb[2], cb[3], b0, b1);
-        pv(vb1, valid1, b0, b1);
-    }
-
     // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o scaled by v_scale.
     __device__ __forceinline__ void write_state(float* st, int /*lane*/) {
 #pragma unroll

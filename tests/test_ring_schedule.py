@@ -8,23 +8,21 @@ parity, so it cannot tell phase u from phase u + 2. This model replays random
 interleavings with those semantics and checks that every consumer reads the
 tile it waited for. Stage counts that are a multiple of the warp count (each
 stage owned by one warp) are safe; others are not, which is why the kernel
-asserts STAGES % W == 0 at compile time. A consumer step may take TPW
-consecutive tiles (tiles TPW k .. TPW k + TPW - 1 go to warp k % W); then
-STAGES must be a multiple of W * TPW.
+asserts STAGES % W == 0 at compile time.
 """
 import random
 
 import pytest
 
 
-def replay(stages, warps, ntiles, seed, tpw=1):
+def replay(stages, warps, ntiles, seed):
     rnd = random.Random(seed)
     full = [0] * stages           # completed phases per barrier
     empty = [0] * stages
     in_flight = {}
     content = [None] * stages
     issued = 0
-    nxt = [w * tpw for w in range(warps)]
+    nxt = list(range(warps))
 
     def done(completed, parity):
         return completed > 0 and ((completed - 1) & 1) == parity
@@ -38,9 +36,7 @@ def replay(stages, warps, ntiles, seed, tpw=1):
                 acts.append(("issue", t))
         acts += [("land", s) for s in in_flight]
         acts += [("take", w) for w in range(warps)
-                 if nxt[w] < ntiles and all(done(full[(nxt[w] + i) % stages],
-                                                 ((nxt[w] + i) // stages) & 1)
-                                            for i in range(tpw))]
+                 if nxt[w] < ntiles and done(full[nxt[w] % stages], (nxt[w] // stages) & 1)]
         if not acts:
             break
         kind, x = rnd.choice(acts)
@@ -53,11 +49,10 @@ def replay(stages, warps, ntiles, seed, tpw=1):
             content[x] = in_flight.pop(x)
             full[x] += 1
         else:
-            for i in range(tpw):
-                t = nxt[x] + i
-                wrong += content[t % stages] != t
-                empty[t % stages] += 1
-            nxt[x] += warps * tpw
+            t = nxt[x]
+            wrong += content[t % stages] != t
+            empty[t % stages] += 1
+            nxt[x] += warps
     finished = all(n >= ntiles for n in nxt)
     return wrong, finished
 
@@ -71,16 +66,4 @@ def test_owned_stages_are_safe(stages, warps):
 
 def test_shared_stages_break():
     bad = sum(replay(6, 4, 40, seed)[0] > 0 for seed in range(200))
-    assert bad > 0
-
-
-@pytest.mark.parametrize("stages,warps,tpw", [(8, 4, 2), (16, 4, 2), (4, 2, 2), (6, 3, 2)])
-def test_multi_tile_steps_with_owned_stages_are_safe(stages, warps, tpw):
-    for seed in range(40):
-        wrong, finished = replay(stages, warps, 48, seed, tpw)
-        assert wrong == 0 and finished, seed
-
-
-def test_multi_tile_steps_with_shared_stages_break():
-    bad = sum(replay(4, 4, 48, seed, 2)[0] > 0 for seed in range(200))
     assert bad > 0
