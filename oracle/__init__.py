@@ -78,6 +78,8 @@ def _load():
         lib.pao_append_fp8.restype = I
         lib.pao_decode_kv.argtypes = [P, I, P, P, I, D, D, P, P, D, P, I, I, I, I, I, I, I, I]
         lib.pao_decode_kv.restype = I
+        lib.pao_decode_multi.argtypes = [P, I, P, P, I, D, D, P, P, D, P, I, I, I, I, I, I, I, I, I]
+        lib.pao_decode_multi.restype = I
         lib.pao_decode.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode.restype = I
         lib.pao_attention_weights.argtypes = [P, P, P, P, D, I, I, P, I, I, I, I, I, I, I, I]
@@ -202,6 +204,25 @@ def decode_kv(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.
     return out
 
 
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.0,
+                 v_scale=1.0, num_threads=0):
+    """Multi-query decode, fp64. q: [B][Q][Hq][D]; query j of sequence s attends
+    to rows 0 .. n - Q + j. Returns [B][Q][Hq][D] float64."""
+    q = _c(q)
+    k_cache, v_cache = _c(k_cache), _c(v_cache, k_cache.dtype)
+    bt, cl = _c(block_tables, np.int32), _c(context_lens, np.int32)
+    B, Q, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    out = np.zeros((B, Q, hq, d), dtype=np.float64)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    rc = _load().pao_decode_multi(_ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache),
+                                  _dtype_code(k_cache), float(k_scale), float(v_scale),
+                                  _ptr(bt), _ptr(cl), float(scale), _ptr(out), B, Q, hq, hkv,
+                                  d, bs, nb, mb, int(num_threads))
+    _check(rc, "decode_multi")
+    return out
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0):
     """fp64 decode attention. q: [B][Hq][D] in the cache dtype -> [B][Hq][D] float64."""
     q = _c(q, k_cache.dtype)
@@ -280,7 +301,8 @@ class use_library:
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("pao_append", "pao_copy_blocks", "pao_e4m3_decode", "pao_e4m3_encode",
-                     "pao_append_fp8", "pao_decode_kv", "pao_decode", "pao_attention_weights",
+                     "pao_append_fp8", "pao_decode_kv", "pao_decode_multi", "pao_decode",
+                     "pao_attention_weights",
                      "pao_decode_partitions", "pao_combine_partitions"):
             src = getattr(self._saved, name)
             dst = getattr(lib, name)

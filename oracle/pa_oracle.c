@@ -51,6 +51,14 @@
  *           "What are MQA and GQA"; consecutive grouping is this library's
  *           reading of "each shared by H/H_kv query heads").
  *
+ *  multi    Several query tokens per sequence (pao_decode_multi): the last Q
+ *           of a sequence's n rows are new tokens verified together, as in
+ *           speculative decoding ("MLSys Engineer -- Inference Systems Q&A",
+ *           Q6: verifying K draft tokens in one pass reads the cache once; Q2,
+ *           phase 3: each draft token attends only to its ancestors). Query j
+ *           (0-based) sits at row n - Q + j and attends to rows 0 .. n - Q + j,
+ *           each by the single-query definition above.
+ *
  *  split    pao_decode_partitions / pao_combine_partitions restate the same
  *           attention as per-partition (max, sum, unnormalised output)
  *           triples merged by rescaling with exp(m_p - M), the rescale rule of
@@ -279,6 +287,81 @@ int pao_decode_kv(const void* q, int q_dtype, const void* k_cache, const void* v
             softmax_weights(qv, Kc, n, head_dim, scale, w);
             for (int i = 0; i < n; ++i)
                 for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
+        }
+        free(Kc); free(Vc); free(w); free(qv);
+    }
+    return err;
+}
+
+/* Multi-query decode. q: [num_seqs][num_queries][num_heads][head_dim] in
+ * q_dtype; out: fp64, same shape. Query j of sequence s attends to rows
+ * 0 .. n - num_queries + j (n = context_lens[s]). n == 0 gives zero rows;
+ * 0 < n < num_queries is PAO_BAD_LEN (that sequence's rows are left zero). */
+int pao_decode_multi(const void* q, int q_dtype, const void* k_cache, const void* v_cache,
+                     int kv_dtype, double k_scale, double v_scale,
+                     const int32_t* block_tables, const int32_t* context_lens, double scale,
+                     double* out, int num_seqs, int num_queries, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                     int max_blocks_per_seq, int num_threads) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, q_dtype);
+    if (rc != PAO_OK) return rc;
+    if (kv_dtype < 0 || kv_dtype > 2 || num_queries < 1) return PAO_BAD_ARG;
+    const int G = num_heads / num_kv_heads;
+    const int Q = num_queries;
+    const int units = num_seqs * num_kv_heads;
+    int err = PAO_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#else
+    const int nt = 1;
+    (void)num_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int u = 0; u < units; ++u) {
+        const int s = u / num_kv_heads, h = u % num_kv_heads;
+        const int n = context_lens[s];
+        for (int j = 0; j < Q; ++j)
+            for (int g = 0; g < G; ++g) {
+                double* o = out + (((size_t)s * Q + j) * num_heads + h * G + g) * head_dim;
+                for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+            }
+        if (n < 0 || (long)n > (long)max_blocks_per_seq * block_size || (n > 0 && n < Q)) {
+#pragma omp atomic write
+            err = PAO_BAD_LEN;
+            continue;
+        }
+        if (n == 0) continue;
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* w = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!Kc || !Vc || !w || !qv) {
+#pragma omp atomic write
+            err = PAO_NO_MEMORY;
+            free(Kc); free(Vc); free(w); free(qv);
+            continue;
+        }
+        const int grc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq,
+                               n, h, num_kv_heads, head_dim, block_size, num_blocks, kv_dtype,
+                               k_scale, v_scale, Kc, Vc);
+        if (grc != PAO_OK) {
+#pragma omp atomic write
+            err = grc;
+        } else {
+            for (int j = 0; j < Q; ++j) {
+                const int rows = n - Q + j + 1;       /* rows 0 .. n - Q + j */
+                for (int g = 0; g < G; ++g) {
+                    const int qh = h * G + g;
+                    const size_t qrow = ((size_t)s * Q + j) * num_heads + qh;
+                    double* o = out + qrow * head_dim;
+                    for (int d = 0; d < head_dim; ++d)
+                        qv[d] = load_elem(q, qrow * head_dim + d, q_dtype);
+                    softmax_weights(qv, Kc, rows, head_dim, scale, w);
+                    for (int i = 0; i < rows; ++i)
+                        for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
+                }
+            }
         }
         free(Kc); free(Vc); free(w); free(qv);
     }

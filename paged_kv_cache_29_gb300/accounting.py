@@ -52,20 +52,22 @@ class StepBytes:
 
 def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
                elem_bytes: int, block_size: int = 16, block_tables=None,
-               act_bytes: int | None = None) -> StepBytes:
+               act_bytes: int | None = None, num_queries: int = 1) -> StepBytes:
     """elem_bytes: bytes per cache element; act_bytes: bytes per element of q,
-    out and the new K/V rows (default: elem_bytes)."""
+    out and the new K/V rows (default: elem_bytes); num_queries: new tokens
+    (queries) per sequence."""
     act = elem_bytes if act_bytes is None else act_bytes
     lens = np.asarray(context_lens, dtype=np.int64)
     B = int(lens.shape[0])
     row = num_kv_heads * head_dim * elem_bytes          # one token, all KV heads, K or V
     kv = int(lens.sum()) * row * 2
-    q_out = B * num_heads * head_dim * act * 2
+    Q = int(num_queries)
+    q_out = B * Q * num_heads * head_dim * act * 2
     used_entries = int(sum(blocks_for_tokens(int(n), block_size) for n in lens))
     tables = used_entries * 4 + B * 4
     active = int((lens > 0).sum())
     # new K and V rows read (act dtype) and written (cache dtype), slots read
-    append = active * num_kv_heads * head_dim * 2 * (act + elem_bytes) + B * 8
+    append = active * Q * num_kv_heads * head_dim * 2 * (act + elem_bytes) + B * Q * 8
     if block_tables is None:
         kv_unique = kv
     else:
@@ -80,7 +82,8 @@ def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
 def step_bytes_for(step) -> StepBytes:
     """StepBytes of a workloads.DecodeStep."""
     return step_bytes(step.context_lens, step.num_heads, step.num_kv_heads, step.head_dim,
-                      step.elem_bytes, step.block_size, step.block_tables, step.act_bytes)
+                      step.elem_bytes, step.block_size, step.block_tables, step.act_bytes,
+                      step.num_queries)
 
 
 def decode_flops(context_lens, num_heads: int, head_dim: int) -> int:

@@ -23,6 +23,8 @@ workloads:
   8b_gqa_fp8     the 8b_gqa batch over an FP8 (e4m3) cache with per-tensor
                  scales 1.0 (uncalibrated); q and the new K/V rows stay bf16
                  and the append quantises them
+  8b_gqa_mq2     the 8b_gqa batch with two new tokens per sequence verified
+                 together (multi-query decode: each query attends causally)
 
 Every value of q, of the new K/V rows and of the whole pool (used or not) is
 drawn N(0, 1) in fp32 and stored in the cache dtype (bf16 by round to nearest
@@ -45,7 +47,7 @@ from .block_manager import BlockManager
 
 # Seeds of the five named workloads, in the order listed above.
 WORKLOAD_SEEDS = {"tiny": 0, "7b_mha": 1, "8b_gqa": 2, "long_skew": 3, "prefix_shared": 4,
-                  "8b_gqa_fp8": 2}     # the 8b_gqa batch (same lengths and tables)
+                  "8b_gqa_fp8": 2, "8b_gqa_mq2": 2}   # variants of the 8b_gqa batch
 PAD_BLOCK = -1
 
 
@@ -134,10 +136,10 @@ class DecodeStep:
     num_kv_heads: int
     head_dim: int
     block_size: int
-    q: np.ndarray                     # [B][Hq][D]
-    k_new: np.ndarray                 # [B][Hkv][D]
-    v_new: np.ndarray                 # [B][Hkv][D]
-    slot_mapping: np.ndarray          # int64 [B]; -1 = no append
+    q: np.ndarray                     # [B][Hq][D]; [B][Q][Hq][D] with Q > 1 queries
+    k_new: np.ndarray                 # [B * Q][Hkv][D] (token t = s * Q + j)
+    v_new: np.ndarray                 # [B * Q][Hkv][D]
+    slot_mapping: np.ndarray          # int64 [B * Q]; -1 = no append
     k_cache: np.ndarray               # [NB][Hkv][bs][D]
     v_cache: np.ndarray               # [NB][Hkv][bs][D]
     block_tables: np.ndarray          # int32 [B][max_blocks]
@@ -146,6 +148,7 @@ class DecodeStep:
     seed: int
     meta: dict = field(default_factory=dict)
     act_dtype: str = ""               # dtype of q, out, k_new, v_new ("" = cache_dtype)
+    num_queries: int = 1              # new tokens per sequence, the last rows of each
     k_scale: float = 1.0              # FP8 caches: value = scale * e4m3(code)
     v_scale: float = 1.0
 
@@ -183,17 +186,19 @@ class DecodeStep:
 def build_step(name: str, context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
                cache_dtype: str = "bf16", block_size: int = 16, seed: int = 0,
                pool_factor: float = 1.25, num_blocks: int | None = None,
-               scale: float | None = None, rng: np.random.Generator | None = None
-               ) -> DecodeStep:
+               scale: float | None = None, rng: np.random.Generator | None = None,
+               num_queries: int = 1) -> DecodeStep:
     """A decode step over independent sequences of the given lengths.
 
-    Each sequence is admitted with n - 1 tokens and then gets one appended
-    token; the block manager hands out blocks from a seeded permutation of the
-    pool. Length 0 means an idle sequence: no blocks, no append."""
+    Each sequence is admitted with n - Q tokens and then gets Q appended
+    tokens (Q = num_queries, 1 for plain decode); the block manager hands out
+    blocks from a seeded permutation of the pool. Length 0 means an idle
+    sequence: no blocks, no append."""
     rng = np.random.default_rng(seed) if rng is None else rng
     lens = [int(n) for n in context_lens]
-    if any(n < 0 for n in lens):
-        raise ValueError("context lengths must be >= 0")
+    Q = int(num_queries)
+    if any(n < 0 for n in lens) or Q < 1 or any(0 < n < Q for n in lens):
+        raise ValueError("context lengths must be 0 or >= the number of queries")
     need = sum(math.ceil(n / block_size) for n in lens)
     if num_blocks is None:
         num_blocks = max(1, math.ceil(pool_factor * need))
@@ -201,19 +206,21 @@ def build_step(name: str, context_lens, num_heads: int, num_kv_heads: int, head_
         raise ValueError(f"pool of {num_blocks} blocks cannot hold {need}")
     mgr = BlockManager(num_blocks, block_size, free_order=rng.permutation(num_blocks),
                        prefix_caching=False)
-    slots = np.full(len(lens), -1, dtype=np.int64)
+    slots = np.full(len(lens) * Q, -1, dtype=np.int64)
     for s, n in enumerate(lens):
-        mgr.admit(f"s{s}", [0] * max(n - 1, 0))
+        mgr.admit(f"s{s}", [0] * max(n - Q, 0))
         if n > 0:
-            slots[s] = mgr.append(f"s{s}", 0).slot
+            for j in range(Q):
+                slots[s * Q + j] = mgr.append(f"s{s}", 0).slot
     tables = [mgr.block_table(f"s{s}") for s in range(len(lens))]
     return _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_size,
                         lens, tables, slots, num_blocks, rng, seed, scale, cow_pairs=[],
-                        meta={"pool_factor": pool_factor, "blocks_needed": need})
+                        meta={"pool_factor": pool_factor, "blocks_needed": need},
+                        num_queries=Q)
 
 
 def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_size, lens,
-                 tables, slots, num_blocks, rng, seed, scale, cow_pairs, meta):
+                 tables, slots, num_blocks, rng, seed, scale, cow_pairs, meta, num_queries=1):
     if num_heads % num_kv_heads:
         raise ValueError("num_heads must be a multiple of num_kv_heads")
     B = len(lens)
@@ -228,9 +235,10 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
     act = "bf16" if cache_dtype == "fp8" else cache_dtype
-    q = _normal(rng, (B, num_heads, head_dim), act)
-    k_new = _normal(rng, (B, num_kv_heads, head_dim), act)
-    v_new = _normal(rng, (B, num_kv_heads, head_dim), act)
+    Q = num_queries
+    q = _normal(rng, (B, num_heads, head_dim) if Q == 1 else (B, Q, num_heads, head_dim), act)
+    k_new = _normal(rng, (B * Q, num_kv_heads, head_dim), act)
+    v_new = _normal(rng, (B * Q, num_kv_heads, head_dim), act)
     used = sorted({b for t in tables for b in t})
     meta = dict(meta, unique_blocks=len(used), max_blocks_per_seq=max_blocks)
     return DecodeStep(name=name, cache_dtype=cache_dtype, num_heads=num_heads,
@@ -239,7 +247,7 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
                       k_cache=k_cache, v_cache=v_cache, block_tables=bt,
                       context_lens=np.asarray(lens, dtype=np.int32),
                       scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale),
-                      seed=seed, meta=meta, act_dtype=act)
+                      seed=seed, meta=meta, act_dtype=act, num_queries=Q)
 
 
 # ---- the five named workloads ------------------------------------------------
@@ -278,6 +286,13 @@ def gqa_8b_fp8(seed: int = WORKLOAD_SEEDS["8b_gqa_fp8"], batch: int = 128) -> De
     lens = gqa_8b_lengths(rng, batch)
     return build_step("8b_gqa_fp8", lens, num_heads=32, num_kv_heads=8, head_dim=128,
                       cache_dtype="fp8", seed=seed, rng=rng)
+
+
+def gqa_8b_mq2(seed: int = WORKLOAD_SEEDS["8b_gqa_mq2"], batch: int = 128) -> DecodeStep:
+    rng = np.random.default_rng(seed)
+    lens = gqa_8b_lengths(rng, batch)
+    return build_step("8b_gqa_mq2", lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                      seed=seed, rng=rng, num_queries=2)
 
 
 def long_skew(seed: int = WORKLOAD_SEEDS["long_skew"]) -> DecodeStep:
@@ -329,6 +344,7 @@ WORKLOADS = {
     "long_skew": long_skew,
     "prefix_shared": prefix_shared,
     "8b_gqa_fp8": gqa_8b_fp8,
+    "8b_gqa_mq2": gqa_8b_mq2,
 }
 
 

@@ -373,6 +373,43 @@ def pin_fp8_decode():
         np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
 
 
+# ---- multi-query decode: causal within the new tokens ------------------------
+
+def pin_multi_query():
+    """Query j of a sequence with n rows and Q new tokens equals the pinned
+    single-query decode of the same sequence cut to its first n - Q + j + 1
+    rows; Q = 1 equals decode(); empty sequences give zeros."""
+    for Q, dtype in ((3, "bf16"), (1, "f32"), (5, "f32")):
+        lens = (0, Q, 9, 16, 40) if Q < 9 else (Q, 40)
+        step = wl.build_step("mq", list(lens), 6, 2, 8, cache_dtype=dtype, block_size=4,
+                             seed=13 + Q, num_queries=Q)
+        k, v = step.k_cache.copy(), step.v_cache.copy()
+        oracle.append(step.k_new, step.v_new, step.slot_mapping, k, v)
+        q4 = step.q if Q > 1 else step.q[:, None]
+        got = oracle.decode_multi(q4, k, v, step.block_tables, step.context_lens, step.scale)
+        for s_, n in enumerate(step.context_lens):
+            for j in range(Q):
+                if n == 0:
+                    assert not got[s_, j].any()
+                    continue
+                want = oracle.decode(q4[s_:s_ + 1, j], k, v, step.block_tables[s_:s_ + 1],
+                                     np.array([n - Q + j + 1], np.int32), step.scale)
+                np.testing.assert_allclose(got[s_, j], want[0], rtol=0, atol=1e-12)
+        if Q == 1:
+            np.testing.assert_array_equal(got[:, 0], oracle.decode(step.q, k, v, step.block_tables,
+                                                                   step.context_lens, step.scale))
+    # a sequence shorter than its query count is an error
+    step = wl.build_step("mq", [5], 4, 2, 8, cache_dtype="f32", seed=3, num_queries=2)
+    q4 = step.q
+    try:
+        oracle.decode_multi(q4, step.k_cache, step.v_cache, step.block_tables,
+                            np.array([1], np.int32), step.scale)
+    except oracle.OracleError:
+        pass
+    else:
+        raise AssertionError("n < Q must be rejected")
+
+
 # ---- P8: closed forms ---------------------------------------------------------
 
 def pin_closed_forms():
@@ -491,6 +528,6 @@ def pin_incremental_decoder():
 
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
-            pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode,
+            pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode, pin_multi_query,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]

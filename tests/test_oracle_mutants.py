@@ -39,6 +39,10 @@ MUTANTS = [
      "(size_t)block_size * head_dim * (size_t)elem_bytes_of(dtype);\n    int bad"),
     ("q_from_kv_head", "qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, q_dtype);",
      "qv[d] = load_elem(q, ((size_t)s * num_heads + h) * head_dim + d, q_dtype);"),
+    ("multi_causal_off_by_one", "const int rows = n - Q + j + 1;", "const int rows = n - Q + j;"),
+    ("multi_no_causality", "const int rows = n - Q + j + 1;", "const int rows = n;"),
+    ("multi_q_head_major", "const size_t qrow = ((size_t)s * Q + j) * num_heads + qh;",
+     "const size_t qrow = ((size_t)s * num_heads + qh) * Q + j;"),
     ("e4m3_bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
     ("e4m3_truncates", "const int q = (int)nearbyint(ldexp(a, 3 - E));",
      "const int q = (int)floor(ldexp(a, 3 - E));"),
