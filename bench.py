@@ -291,7 +291,9 @@ def run_native(args) -> dict | None:
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     mcl = step.max_context_len
-    ws_bytes = pa.pa_decode_workspace_size(step.num_seqs, step.num_heads, step.head_dim, mcl)
+    Qn = step.num_queries
+    ws_bytes = pa.pa_decode_workspace_size_multi(step.num_seqs, Qn, step.num_heads,
+                                                 step.head_dim, mcl)
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_clean = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -319,6 +321,9 @@ def run_native(args) -> dict | None:
             pa.pa_decode_fp8(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                              step.k_scale, step.v_scale, workspace=workspace, error_word=err,
                              stream=st)
+        elif Qn > 1:
+            pa.pa_decode_multi(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
+                               workspace=workspace, error_word=err, stream=st)
         else:
             pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                          workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
@@ -461,7 +466,7 @@ def run_native(args) -> dict | None:
         "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
         "config": {
             "workload": args.workload,
-            "num_seqs": step.num_seqs, "num_heads": step.num_heads,
+            "num_seqs": step.num_seqs, "num_queries": step.num_queries, "num_heads": step.num_heads,
             "num_kv_heads": step.num_kv_heads, "head_dim": step.head_dim,
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),

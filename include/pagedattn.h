@@ -185,6 +185,36 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                         size_t workspace_bytes, int32_t* error_word,
                         struct CUstream_st* stream);
 
+/*
+ * Multi-query decode: num_queries (Q) new tokens per sequence verified
+ * together, as speculative decoding does ("MLSys Engineer -- Inference Systems
+ * Q&A", Q6: verifying K draft tokens in one pass costs about one decode's
+ * bandwidth; Q2, phase 3: each draft token attends only to its ancestors).
+ * The last Q of a sequence's n = context_lens[s] rows are the new tokens
+ * (appended beforehand, e.g. by pa_reshape_and_cache with Q tokens per
+ * sequence); query token j (0-based) sits at row n - Q + j and attends to
+ * rows 0 .. n - Q + j:
+ *   out[s][j][qh][:] = sum_{i <= n-Q+j} softmax_i(scale * <q[s][j][qh], K_i>) * V_i[:]
+ * q, out: [num_seqs][num_queries][num_heads][head_dim], bf16 (dtype must be
+ * PA_DTYPE_BF16). Each sequence's K/V rows are read once for all its query
+ * tokens. 0 < n < Q is flagged PA_DEVERR_CONTEXT (those rows are left
+ * unspecified); n == 0 gives zero rows. Workspace:
+ * pa_decode_workspace_size_multi. Supported: head_dim 64 or 128, block_size a
+ * multiple of 16, (num_heads / num_kv_heads) * num_queries <= 8 (else
+ * PA_ERR_UNSUPPORTED); 1 <= num_queries <= 8. Same partitioning, merge order
+ * and batch invariance as pa_decode.
+ */
+pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          void* out, int num_seqs, int num_queries, int num_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* error_word,
+                          struct CUstream_st* stream);
+
+size_t pa_decode_workspace_size_multi(int num_seqs, int num_queries, int num_heads,
+                                      int head_dim, int max_context_len);
+
 /* Bytes of workspace pa_decode needs for these sizes (0 only for an empty
  * batch). */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);

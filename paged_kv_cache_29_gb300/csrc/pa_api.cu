@@ -85,24 +85,26 @@ struct WorkspaceLayout {
 };
 
 WorkspaceLayout layout_for(int num_seqs, int num_heads, int head_dim, int max_context_len,
-                           int partition_size) {
+                           int partition_size, int num_queries = 1) {
     WorkspaceLayout w{0, 0, 0, 0};
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || partition_size <= 0 ||
-        max_context_len < 0)
+        max_context_len < 0 || num_queries < 1)
         return w;
     const long long seqs = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
     const long long parts = max_context_len > 0 ? ceil_div(max_context_len, partition_size) : 1;
-    const size_t units = static_cast<size_t>(seqs) * num_heads * parts;
+    const size_t units = static_cast<size_t>(seqs) * num_heads * parts;   // items (bounded)
+    const size_t prows = units * static_cast<size_t>(num_queries);          // partial rows
     w.items_off = 256;
     w.ml_off = w.items_off + 16 * units;
-    w.o_off = w.ml_off + (parts > 1 ? 8 * units : 0);
-    w.total = w.o_off + (parts > 1 ? 4 * units * static_cast<size_t>(head_dim) : 0);
+    w.o_off = w.ml_off + (parts > 1 ? 8 * prows : 0);
+    w.total = w.o_off + (parts > 1 ? 4 * prows * static_cast<size_t>(head_dim) : 0);
     return w;
 }
 
 size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int max_context_len,
-                           int partition_size) {
-    return layout_for(num_seqs, num_heads, head_dim, max_context_len, partition_size).total;
+                           int partition_size, int num_queries = 1) {
+    return layout_for(num_seqs, num_heads, head_dim, max_context_len, partition_size, num_queries)
+        .total;
 }
 
 // One decode call: q/out in act_dtype, the caches in dtype (act_dtype, or FP8
@@ -114,13 +116,14 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
                       pa_dtype act_dtype, void* workspace, size_t workspace_bytes,
                       int32_t* error_word, const pa_decode_options* options,
-                      struct CUstream_st* stream) {
+                      struct CUstream_st* stream, int num_queries = 1) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
                                                                : pa::kDefaultPartition;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
-        !valid_cache_dtype(dtype) || !valid_dtype(act_dtype) || num_heads % num_kv_heads != 0)
+        !valid_cache_dtype(dtype) || !valid_dtype(act_dtype) || num_heads % num_kv_heads != 0 ||
+        num_queries < 1)
         return PA_ERR_INVALID_ARG;
     if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
     if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
@@ -142,7 +145,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     const long long chunk = num_seqs < pa::kPlanMaxSeqs ? num_seqs : pa::kPlanMaxSeqs;
     if (max_parts * chunk * num_kv_heads > 0x3fffffffLL) return PA_ERR_UNSUPPORTED;
 
-    const WorkspaceLayout lay = layout_for(num_seqs, num_heads, head_dim, max_context_len, partition);
+    const WorkspaceLayout lay =
+        layout_for(num_seqs, num_heads, head_dim, max_context_len, partition, num_queries);
     if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
         return PA_ERR_WORKSPACE;
 
@@ -151,21 +155,28 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                            (head_dim * elem_bytes(dtype)) % 128 == 0;
     pa_kernel kernel = static_cast<pa_kernel>(kernel_req);
     const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
-    if (fp8) {
+    if (num_queries > 1) {
+        // Several query tokens per sequence: the bf16 tensor-core tile ring.
+        if (fp8 || !tma_shape ||
+            !pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group, num_queries) ||
+            (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA))
+            return PA_ERR_UNSUPPORTED;
+        kernel = PA_KERNEL_MMA;
+    } else if (fp8) {
         // One kernel family: the FP8 tensor-core tile ring.
         if (!tma_shape || !pa::has_fp8_instance(head_dim, group) ||
             (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA))
             return PA_ERR_UNSUPPORTED;
         kernel = PA_KERNEL_MMA;
     } else if (kernel == PA_KERNEL_AUTO) {
-        if (tma_shape && pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group))
+        if (tma_shape && pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group, 1))
             kernel = PA_KERNEL_MMA;
-        else if (tma_shape && pa::has_tma_instance(PA_KERNEL_SIMT, dtype, head_dim, group))
+        else if (tma_shape && pa::has_tma_instance(PA_KERNEL_SIMT, dtype, head_dim, group, 1))
             kernel = PA_KERNEL_SIMT;
         else
             kernel = PA_KERNEL_GENERIC;
     } else if (kernel != PA_KERNEL_GENERIC &&
-               (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group))) {
+               (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group, 1))) {
         return PA_ERR_UNSUPPORTED;
     }
     if (kernel == PA_KERNEL_GENERIC &&
@@ -183,6 +194,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     base.scale_log2 = scale * kLog2e;
     base.k_scale = k_scale;
     base.v_scale = v_scale;
+    base.num_queries = num_queries;
     base.num_heads = num_heads;
     base.num_kv_heads = num_kv_heads;
     base.head_dim = head_dim;
@@ -217,7 +229,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     for (int s0 = 0; s0 < num_seqs; s0 += pa::kPlanMaxSeqs) {
         const int bs_n = num_seqs - s0 < pa::kPlanMaxSeqs ? num_seqs - s0 : pa::kPlanMaxSeqs;
         DecodeParams p = base;
-        const size_t qoff = static_cast<size_t>(s0) * num_heads * head_dim * es;
+        const size_t qoff = static_cast<size_t>(s0) * num_queries * num_heads * head_dim * es;
         p.q = static_cast<const uint8_t*>(q) + qoff;
         p.out = static_cast<uint8_t*>(out) + qoff;
         p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
@@ -344,6 +356,26 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                        out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, PA_DTYPE_FP8_E4M3, PA_DTYPE_BF16,
                        workspace, workspace_bytes, error_word, nullptr, stream);
+}
+
+pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          void* out, int num_seqs, int num_queries, int num_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* error_word,
+                          struct CUstream_st* stream) {
+    if (!valid_dtype(dtype) || num_queries < 1 || num_queries > 8) return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
+                       workspace_bytes, error_word, nullptr, stream, num_queries);
+}
+
+size_t pa_decode_workspace_size_multi(int num_seqs, int num_queries, int num_heads,
+                                      int head_dim, int max_context_len) {
+    return workspace_bytes_for(num_seqs, num_heads, head_dim, max_context_len,
+                               pa::kDefaultPartition, num_queries);
 }
 
 pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,

@@ -163,7 +163,8 @@ __host__ __device__ __forceinline__ int combine_warps(int np) {
     return w < kCombineMaxWarps ? w : kCombineMaxWarps;
 }
 
-// One CTA per (sequence, query head) of a sequence longer than one partition.
+// One CTA per (sequence, query token, query head) of a sequence longer than
+// one partition (one query token per sequence for plain decode).
 // Each warp merges its chunks (lane q holds partition q's max and sum; the o
 // rows are loaded kCombineBatch partitions at a time), then the warp results
 // are merged in warp order.
@@ -174,14 +175,16 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
     // partials before reading anything.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int qh = blockIdx.x;
-    const int s = blockIdx.y;
+    const int sq = blockIdx.y;                 // s * num_queries + query token
+    const int s = sq / p.num_queries;
     const int n = __ldg(p.context_lens + s);
     const int P = p.partition_size;
     if (n <= P || n > p.context_cap) return;   // one partition (written directly) or flagged
+    if (n < p.num_queries) return;             // flagged
     const int np = (n + P - 1) / P;
     const int nw = combine_warps(np);
     const int D = p.head_dim;
-    const size_t row = static_cast<size_t>(s) * p.num_heads + qh;
+    const size_t row = static_cast<size_t>(sq) * p.num_heads + qh;
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row * p.max_parts;
     const float* o = p.part_o + row * p.max_parts * static_cast<size_t>(D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,8 +197,11 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
             const int cnt = min(kCombineChunk, np - c0);
             const float2 v = lane < cnt ? ml[c0 + lane] : make_float2(-INFINITY, 0.f);
             const float Mc = fmaxf(M, warp_max(v.x));
-            const float w = lane < cnt ? fast_exp2(v.x - Mc) : 0.f;
-            const float rescale = fast_exp2(M - Mc);          // 0 on the first chunk
+            // Partitions a query token does not reach (several tokens per
+            // sequence) hold m = -inf, l = 0: weight 0, never NaN.
+            const float ref = Mc == -INFINITY ? 0.f : Mc;
+            const float w = lane < cnt ? fast_exp2(v.x - ref) : 0.f;
+            const float rescale = fast_exp2(M - ref);         // 0 on the first chunk
             L = L * rescale + warp_sum(w * v.y);
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] *= rescale;
@@ -279,7 +285,7 @@ cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t s
     const int warps = combine_warps(p.max_parts);   // enough for the longest sequence
     const size_t smem = static_cast<size_t>(warps) * (p.head_dim + 2) * sizeof(float);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_heads, p.num_seqs);
+    cfg.gridDim = dim3(p.num_heads, p.num_seqs * p.num_queries);
     cfg.blockDim = dim3(32 * warps);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -1,6 +1,7 @@
 // pa_decode_mma.cu -- instances of the tile-ring decode kernel with the
-// tensor-core tile math (bf16 caches; head dim 64 or 128; 1, 2, 4 or 8 query
-// heads per KV head).
+// tensor-core tile math (bf16 caches; head dim 64 or 128; up to 8 query
+// columns per item: 1, 2, 4 or 8 query heads per KV head, times the query
+// tokens per sequence).
 #include "pa_decode_stream.cuh"
 
 namespace pa {
@@ -17,16 +18,17 @@ cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams
         tk, tv, p, sm_count, stream);
 }
 
+// The instance's column capacity: the query columns of an item (group heads x
+// query tokens per sequence) rounded up to 1, 2, 4 or 8.
 template <int D>
 cudaError_t by_group(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                      int sm_count, cudaStream_t stream) {
-    switch (p.num_heads / p.num_kv_heads) {
-        case 1: return run<D, 1>(tk, tv, p, sm_count, stream);
-        case 2: return run<D, 2>(tk, tv, p, sm_count, stream);
-        case 4: return run<D, 4>(tk, tv, p, sm_count, stream);
-        case 8: return run<D, 8>(tk, tv, p, sm_count, stream);
-        default: return cudaErrorNotSupported;
-    }
+    const int cols = (p.num_heads / p.num_kv_heads) * p.num_queries;
+    if (cols <= 1) return run<D, 1>(tk, tv, p, sm_count, stream);
+    if (cols <= 2) return run<D, 2>(tk, tv, p, sm_count, stream);
+    if (cols <= 4) return run<D, 4>(tk, tv, p, sm_count, stream);
+    if (cols <= 8) return run<D, 8>(tk, tv, p, sm_count, stream);
+    return cudaErrorNotSupported;
 }
 }  // namespace
 

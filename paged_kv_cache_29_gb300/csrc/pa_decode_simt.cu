@@ -51,11 +51,16 @@ cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
                                   : by_dim<float>(tk, tv, p, sm_count, stream);
 }
 
-bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group) {
-    const bool shape = (head_dim == 64 || head_dim == 128) &&
-                       (group == 1 || group == 2 || group == 4 || group == 8);
-    if (kernel == PA_KERNEL_MMA) return shape && dtype == PA_DTYPE_BF16;
-    if (kernel == PA_KERNEL_SIMT) return shape;
+bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group,
+                      int num_queries) {
+    const bool dims = head_dim == 64 || head_dim == 128;
+    const bool pow2_group = group == 1 || group == 2 || group == 4 || group == 8;
+    if (kernel == PA_KERNEL_MMA) {
+        // Query columns (heads x query tokens) fill the 8 MMA columns.
+        const bool cols = num_queries == 1 ? pow2_group : group * num_queries <= 8;
+        return dims && cols && dtype == PA_DTYPE_BF16;
+    }
+    if (kernel == PA_KERNEL_SIMT) return dims && pow2_group && num_queries == 1;
     return false;
 }
 

@@ -237,6 +237,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // item boundary costs no global-memory round trip.
     Math math;
     math.setup(lane, p);
+    // Query columns of an item: the group's heads x the query tokens per
+    // sequence (one for plain decode); at most G, the state's capacity.
+    const int grp = p.num_heads / p.num_kv_heads;
+    const int Qn = p.num_queries;
+    const int ncols = grp * Qn;
     auto item_at = [&](int j) -> int4 {
         const int k = snake_item(c, j, C);
         return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
@@ -247,7 +252,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if constexpr (Math::kQInSmem) {
         // q of item 0 now, then always one item ahead, copied by warp 0.
         if (warp == 0 && it.x >= 0) {
-            math.stage_q(p, it.x, it.y, smem_addr(qbuf), lane);
+            math.stage_q(p, it.x, it.y, ncols, grp, smem_addr(qbuf), lane);
             cp_async_wait_all();
         }
         named_barrier(1, W * 32);
@@ -263,17 +268,18 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
         const int4 it_after = item_at(j + 2);
         if constexpr (Math::kQInSmem) {
-            math.begin_staged(qbuf + (j & 1) * Math::kQBufBytes);
+            math.begin_staged(qbuf + (j & 1) * Math::kQBufBytes, ncols);
             // The other buffer was last read when item j - 1 began, before the
             // previous item's closing barrier.
             if (warp == 0 && it_next.x >= 0)
-                math.stage_q(p, it_next.x, it_next.y, smem_addr(qbuf + ((j + 1) & 1) * Math::kQBufBytes),
-                             lane);
+                math.stage_q(p, it_next.x, it_next.y, ncols, grp,
+                             smem_addr(qbuf + ((j + 1) & 1) * Math::kQBufBytes), lane);
         } else {
             math.begin(p, q_next);
             if (it_next.x >= 0) math.load_q(p, it_next.x, it_next.y, q_next);
         }
         const int span = ((ntiles + W - 1) / W) * W;   // padded as the producer pads
+        const int limit0 = n - Qn;                      // the last row query token 0 sees
         bool bad = false;
         if (!aborted) {
             for (int t = t0 + warp; t < t0 + span; t += W) {
@@ -286,9 +292,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (stage_bad[stage]) {
                     bad = true;
                 } else if (t - t0 < ntiles) {
-                    const int valid = min(kTileRows, hi - (lo + kTileRows * (t - t0)));
+                    const int row0 = lo + kTileRows * (t - t0);
+                    const int valid = min(kTileRows, hi - row0);
                     const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
-                    math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane);
+                    math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane, row0, limit0,
+                              grp);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
@@ -298,7 +306,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         it_next = it_after;
         t0 += span;
         float* buf = merge + (j & 1) * (W * Smem::kState);
-        math.write_state(buf + warp * Smem::kState, lane);
+        math.write_state(buf + warp * Smem::kState, lane, ncols);
         if constexpr (Math::kQInSmem) {
             if (warp == 0) cp_async_wait_all();   // next item's q is visible after the barrier
         }
@@ -316,22 +324,24 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         for (int w = 0; w < W; ++w) any_bad |= warp_bad[(j & 1) * W + w] != 0;
         if (any_bad) continue;              // flagged by the producer; output left unspecified
         const int nparts = (n + P - 1) / P;
-        const int qh0 = h * G;
-        for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-            const int g = idx / D;
+        for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+            const int g = idx / D;            // query column
             const int d = idx - g * D;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < W; ++w) M = fmaxf(M, buf[w * Smem::kState + g]);
+            // A column that sees no row of this partition (several queries per
+            // sequence) merges to m = -inf, l = 0, o = 0.
+            const float ref = M == -INFINITY ? 0.f : M;
             float L = 0.f, O = 0.f;
 #pragma unroll
             for (int w = 0; w < W; ++w) {
                 const float* sw = buf + w * Smem::kState;
-                const float cw = fast_exp2(sw[g] - M);
+                const float cw = fast_exp2(sw[g] - ref);
                 L = fmaf(cw, sw[G + g], L);
                 O = fmaf(cw, sw[2 * G + g * D + d], O);
             }
-            const size_t row = static_cast<size_t>(s) * p.num_heads + qh0 + g;
+            const size_t row = query_row(p, s, h, g, grp);
             if (nparts == 1) {
                 ElemTraits<T>::store(static_cast<T*>(p.out) + row * D + d, O / L);
             } else {

@@ -27,6 +27,7 @@ struct DecodeParams {
     float k_scale;                 // FP8 caches: K value = k_scale * e4m3(code) (else 1)
     float v_scale;                 // FP8 caches: V value = v_scale * e4m3(code) (else 1)
     int num_seqs;
+    int num_queries;               // query tokens per sequence, the last rows of each (>= 1)
     int num_heads;
     int num_kv_heads;
     int head_dim;
@@ -56,7 +57,8 @@ cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv,
 cudaError_t launch_decode_simt(const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeParams& p, pa_dtype dtype, int sm_count,
                                cudaStream_t stream);
-bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group);
+bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group,
+                      int num_queries);
 
 // FP8 (e4m3) cache, bf16 q/out: tensor-core tile math (head dim 128; 1, 2, 4
 // or 8 query heads per KV head).

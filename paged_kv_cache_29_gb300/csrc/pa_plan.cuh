@@ -49,10 +49,11 @@ __device__ __forceinline__ void for_own_items(int a, int e, int c, int C, F&& f)
     }
 }
 
-// Context length of sequence s, or -1 (flagged) when it is out of range.
+// Context length of sequence s, or -1 (flagged) when it is out of range
+// (negative, past max_context_len, or shorter than the query tokens it holds).
 __device__ __forceinline__ int plan_len(const DecodeParams& p, int s, bool flag) {
     int n = __ldg(p.context_lens + s);
-    if (n < 0 || n > p.context_cap) {
+    if (n < 0 || n > p.context_cap || (n > 0 && n < p.num_queries)) {
         if (flag) raise_error(p.error_word, PA_DEVERR_CONTEXT);
         n = -1;
     }
@@ -114,9 +115,12 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
         const int b = n > 0 ? plan_bucket(n % P, P) : -1;
         if (b >= 0) atomicAdd(&bcount[b], 1);
         if (n == 0 && s % C == c) {
-            const int chunks = p.num_heads * p.head_dim * static_cast<int>(sizeof(T)) / 16;
-            uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                  static_cast<size_t>(s) * p.num_heads * p.head_dim);
+            // the sequence's num_queries output rows
+            const int chunks =
+                p.num_queries * p.num_heads * p.head_dim * static_cast<int>(sizeof(T)) / 16;
+            uint4* row = reinterpret_cast<uint4*>(
+                static_cast<T*>(p.out) +
+                static_cast<size_t>(s) * p.num_queries * p.num_heads * p.head_dim);
             for (int i = 0; i < chunks; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
         }
     }

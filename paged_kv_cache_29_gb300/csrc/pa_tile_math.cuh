@@ -80,19 +80,27 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// One warp copies q of (sequence s, KV head h) -- G rows of D bf16 -- into a
-// staging buffer whose rows are ROW_BYTES apart, with cp.async.
-template <int D, int G, int ROW_BYTES>
-__device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int s, int h, uint32_t qbuf,
-                                             int lane) {
+// The query columns of one work item (sequence s, KV head h): with Q query
+// tokens per sequence and G query heads per KV head, column c is query token
+// j = c / G of head h * G + c % G, i.e. row (s * Q + j) * num_heads + h * G +
+// c % G of q and out. One query per sequence: the G heads of the group.
+__device__ __forceinline__ size_t query_row(const DecodeParams& p, int s, int h, int c, int grp) {
+    const int j = c / grp;
+    return (static_cast<size_t>(s) * p.num_queries + j) * p.num_heads + h * grp + (c - j * grp);
+}
+
+// One warp copies the ncols q rows (D bf16 each) of (sequence s, KV head h)
+// into a staging buffer whose rows are ROW_BYTES apart, with cp.async.
+template <int D, int ROW_BYTES>
+__device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int s, int h, int ncols,
+                                             int grp, uint32_t qbuf, int lane) {
     constexpr int kChunksPerRow = D * 2 / 16;
-    const uint8_t* q = reinterpret_cast<const uint8_t*>(
-        static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(s) * p.num_heads + h * G) * D);
-    for (int c = lane; c < G * kChunksPerRow; c += 32) {
-        const int g = c / kChunksPerRow, ch = c - g * kChunksPerRow;
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(p.q);
+    for (int c = lane; c < ncols * kChunksPerRow; c += 32) {
+        const int col = c / kChunksPerRow, ch = c - col * kChunksPerRow;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                         qbuf + static_cast<uint32_t>(g * ROW_BYTES + ch * 16)),
-                     "l"(q + static_cast<size_t>(g) * D * 2 + ch * 16)
+                         qbuf + static_cast<uint32_t>(col * ROW_BYTES + ch * 16)),
+                     "l"(q + query_row(p, s, h, col, grp) * D * 2 + ch * 16)
                      : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -102,9 +110,11 @@ __device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int s, int h
 // Tensor-core tile math (bf16). Fragment layouts are those of mma.m16n8k16:
 // lane = 4 * gid + t4; accumulator c0,c1 = (row gid, cols 2t4, 2t4+1),
 // c2,c3 = (row gid + 8, same cols).
-//   QK:  C = S^T [16 tokens][8 heads], A = K tile [16 tokens][16 dims] per
-//        k-step (ldmatrix), B = Q^T [16 dims][8 heads] (registers; heads >= G
-//        are zero).
+//   QK:  C = S^T [16 tokens][8 columns], A = K tile [16 tokens][16 dims] per
+//        k-step (ldmatrix), B = Q^T [16 dims][8 columns] (registers). The
+//        columns are the item's query columns (query_row): the G <= 8 heads of
+//        the group, or G heads x Q query tokens when several tokens per
+//        sequence are verified together; columns past them are zero.
 //   PV:  C = O^T [16 dims][8 heads] per m-tile of 16 dims, A = V^T [16 dims]
 //        [16 tokens] (ldmatrix.trans of the V tile), B = P^T [16 tokens]
 //        [8 heads], built from the QK accumulators with four shuffles.
@@ -114,7 +124,8 @@ struct MmaMath {
     using T = __nv_bfloat16;
     using Geom = TileGeom<T, D>;
     static constexpr int kSteps = D / 16;
-    static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
+    // G: query columns the state holds (a capacity: an item uses ncols <= G).
+    static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query columns");
 
     // q of the next item is staged in shared memory ([G][D] bf16 rows padded
     // to D * 2 + 16 bytes, so that the fragment reads below hit 32 different
@@ -135,19 +146,23 @@ struct MmaMath {
     }
 
     // One warp copies q of (sequence s, KV head h) into the staging buffer.
-    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, uint32_t qbuf,
-                                            int lane) const {
-        stage_q_rows<D, G, kQRowBytes>(p, s, h, qbuf, lane);
+    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, int ncols,
+                                            int grp, uint32_t qbuf, int lane) const {
+        stage_q_rows<D, kQRowBytes>(p, s, h, ncols, grp, qbuf, lane);
     }
 
     // Start an item: read q's B fragments from the staging buffer and clear
     // the softmax state.
-    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf) {
+    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf, int ncols) {
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             const uint8_t* r = qbuf + gid * kQRowBytes + (16 * kk + 2 * t4) * 2;
-            qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(r) : 0u;
-            qb[kk][1] = gid < G ? *reinterpret_cast<const uint32_t*>(r + 16) : 0u;
+            qb[kk][0] = 0u;
+            qb[kk][1] = 0u;
+            if (gid < ncols) {
+                qb[kk][0] = *reinterpret_cast<const uint32_t*>(r);
+                qb[kk][1] = *reinterpret_cast<const uint32_t*>(r + 16);
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[kk][i] = 0.f;
         }
@@ -155,8 +170,12 @@ struct MmaMath {
         l[0] = l[1] = 0.f;
     }
 
+    // valid: rows of the tile before the end of the sequence (V rows past it
+    // are zeroed). Row row0 + i is visible to query column c when row0 + i <=
+    // limit0 + c / grp (limit0: the last row query token 0 sees).
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
-                                         float scale_log2, int lane) {
+                                         float scale_log2, int lane, int row0, int limit0,
+                                         int grp) {
         const int mi = lane >> 3;
         const int lr = lane & 7;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -172,9 +191,15 @@ struct MmaMath {
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] *= scale_log2;
-        if (valid < kTileRows) {
-            if (gid >= valid) c[0] = c[1] = -INFINITY;
-            if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+        if (row0 + kTileRows - 1 > limit0) {
+            // Rows past what a column sees: past the sequence (one query per
+            // sequence), or past the query token's own row (several).
+            const int j0 = (2 * t4) / grp, j1 = (2 * t4 + 1) / grp;
+            const int r = row0 + gid;
+            if (r > limit0 + j0) c[0] = -INFINITY;
+            if (r > limit0 + j1) c[1] = -INFINITY;
+            if (r + 8 > limit0 + j0) c[2] = -INFINITY;
+            if (r + 8 > limit0 + j1) c[3] = -INFINITY;
         }
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
@@ -185,12 +210,16 @@ struct MmaMath {
         }
         const float mn0 = fmaxf(m[0], mx0);
         const float mn1 = fmaxf(m[1], mx1);
-        const float al0 = fast_exp2(m[0] - mn0);
-        const float al1 = fast_exp2(m[1] - mn1);
-        const float p0 = fast_exp2(c[0] - mn0);
-        const float p1 = fast_exp2(c[1] - mn1);
-        const float p2 = fast_exp2(c[2] - mn0);
-        const float p3 = fast_exp2(c[3] - mn1);
+        // A column with no visible row yet keeps max -inf: exponentiate
+        // against 0 then, so that its weights are 0 rather than NaN.
+        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m[0] - ref0);
+        const float al1 = fast_exp2(m[1] - ref1);
+        const float p0 = fast_exp2(c[0] - ref0);
+        const float p1 = fast_exp2(c[1] - ref1);
+        const float p2 = fast_exp2(c[2] - ref0);
+        const float p3 = fast_exp2(c[3] - ref1);
         l[0] = l[0] * al0 + (p0 + p2);
         l[1] = l[1] * al1 + (p1 + p3);
         // The rescale factor is exactly 1 where the max did not grow: skip the
@@ -247,8 +276,8 @@ struct MmaMath {
         }
     }
 
-    // State layout: m[G], l[G], o[G][D] (fp32, base-2 max).
-    __device__ __forceinline__ void write_state(float* st, int lane) {
+    // State layout: m[G], l[G], o[G][D] (fp32, base-2 max); columns < ncols.
+    __device__ __forceinline__ void write_state(float* st, int lane, int ncols) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
@@ -257,15 +286,15 @@ struct MmaMath {
         (void)lane;
         const int h0 = 2 * t4, h1 = 2 * t4 + 1;
         if (gid == 0) {
-            if (h0 < G) { st[h0] = m[0]; st[G + h0] = l[0]; }
-            if (h1 < G) { st[h1] = m[1]; st[G + h1] = l[1]; }
+            if (h0 < ncols) { st[h0] = m[0]; st[G + h0] = l[0]; }
+            if (h1 < ncols) { st[h1] = m[1]; st[G + h1] = l[1]; }
         }
         float* so = st + 2 * G;
 #pragma unroll
         for (int mt = 0; mt < kSteps; ++mt) {
             const int d0 = 16 * mt + gid;
-            if (h0 < G) { so[h0 * D + d0] = o[mt][0]; so[h0 * D + d0 + 8] = o[mt][2]; }
-            if (h1 < G) { so[h1 * D + d0] = o[mt][1]; so[h1 * D + d0 + 8] = o[mt][3]; }
+            if (h0 < ncols) { so[h0 * D + d0] = o[mt][0]; so[h0 * D + d0 + 8] = o[mt][2]; }
+            if (h1 < ncols) { so[h1 * D + d0] = o[mt][1]; so[h1 * D + d0 + 8] = o[mt][3]; }
         }
     }
 };
@@ -348,8 +377,11 @@ struct SimtMath {
         }
     }
 
+    // One query per sequence: rows past `valid` are masked (row0, limit0 and
+    // grp describe the same boundary and are not needed).
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
-                                         float /*scale_log2*/, int /*lane*/) {
+                                         float /*scale_log2*/, int /*lane*/, int /*row0*/,
+                                         int /*limit0*/, int /*grp*/) {
         const uint32_t kbox = kbase + (ch >> 3) * kBoxBytes;
         const uint32_t vbox = vbase + (ch >> 3) * kBoxBytes;
         const int cc = ch & 7;
@@ -420,7 +452,7 @@ struct SimtMath {
         }
     }
 
-    __device__ __forceinline__ void write_state(float* st, int lane) {
+    __device__ __forceinline__ void write_state(float* st, int lane, int /*ncols: G*/) {
 #pragma unroll
         for (int off = kLpr; off < 32; off <<= 1) {
 #pragma unroll

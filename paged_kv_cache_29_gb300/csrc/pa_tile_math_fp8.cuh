@@ -87,15 +87,15 @@ struct Fp8MmaMath {
         vscale = p.v_scale;
     }
 
-    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, uint32_t qbuf,
-                                            int lane) const {
-        stage_q_rows<D, G, kQRowBytes>(p, s, h, qbuf, lane);
+    __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, int ncols,
+                                            int grp, uint32_t qbuf, int lane) const {
+        stage_q_rows<D, kQRowBytes>(p, s, h, ncols, grp, qbuf, lane);
     }
 
     // q' = q * scale * log2(e) * k_scale in f16, dealt as the k-steps deal
     // the dims; the softmax state is cleared. Lanes of heads gid >= G read
     // nothing (the buffer holds G rows) and hold zeros.
-    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf) {
+    __device__ __forceinline__ void begin_staged(const uint8_t* qbuf, int /*ncols: G*/) {
         const uint8_t* row = qbuf + gid * kQRowBytes;
 #pragma unroll
         for (int j = 0; j < kSteps; ++j) {
@@ -197,8 +197,10 @@ struct Fp8MmaMath {
     }
 
     // One 16-row tile per step.
+    // One query per sequence: rows past `valid` are masked.
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
-                                         float /*scale_log2: folded into q'*/, int /*lane*/) {
+                                         float /*scale_log2: folded into q'*/, int /*lane*/,
+                                         int /*row0*/, int /*limit0*/, int /*grp*/) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         qk(kbase, valid, c);
         float mx0 = fmaxf(c[0], c[2]);
@@ -238,7 +240,7 @@ struct Fp8MmaMath {
     }
 
     // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o scaled by v_scale.
-    __device__ __forceinline__ void write_state(float* st, int /*lane*/) {
+    __device__ __forceinline__ void write_state(float* st, int /*lane*/, int /*ncols: G*/) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
