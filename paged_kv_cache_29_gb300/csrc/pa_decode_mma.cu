@@ -14,6 +14,11 @@ constexpr int kMinCtasPerSm = 4;   // four rings per SM (register budget 96 per 
 template <int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                 int sm_count, cudaStream_t stream) {
+    if constexpr (G > 1) {   // several query tokens fill at least two columns
+        if (p.num_queries > 1)
+            return launch_stream_instance<MmaMath<D, G, true>, D, G, kWarps, kStages,
+                                          kMinCtasPerSm>(tk, tv, p, sm_count, stream);
+    }
     return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages, kMinCtasPerSm>(
         tk, tv, p, sm_count, stream);
 }

@@ -238,10 +238,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     Math math;
     math.setup(lane, p);
     // Query columns of an item: the group's heads x the query tokens per
-    // sequence (one for plain decode); at most G, the state's capacity.
-    const int grp = p.num_heads / p.num_kv_heads;
-    const int Qn = p.num_queries;
-    const int ncols = grp * Qn;
+    // sequence, at most G (the state's capacity). Maths without causal
+    // masking serve one query per sequence with exactly G heads.
+    const int grp = Math::kCausal ? p.num_heads / p.num_kv_heads : G;
+    const int Qn = Math::kCausal ? p.num_queries : 1;
+    const int ncols = Math::kCausal ? grp * Qn : G;
     auto item_at = [&](int j) -> int4 {
         const int k = snake_item(c, j, C);
         return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
@@ -341,7 +342,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 L = fmaf(cw, sw[G + g], L);
                 O = fmaf(cw, sw[2 * G + g * D + d], O);
             }
-            const size_t row = query_row(p, s, h, g, grp);
+            const size_t row = Math::kCausal
+                                   ? query_row(p, s, h, g, grp)
+                                   : static_cast<size_t>(s) * p.num_heads + h * G + g;
             if (nparts == 1) {
                 ElemTraits<T>::store(static_cast<T*>(p.out) + row * D + d, O / L);
             } else {

@@ -119,9 +119,13 @@ __device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int s, int h
 //        [16 tokens] (ldmatrix.trans of the V tile), B = P^T [16 tokens]
 //        [8 heads], built from the QK accumulators with four shuffles.
 // ---------------------------------------------------------------------------
-template <int D, int G>
+// CAUSAL: items may carry several query tokens per sequence, each seeing
+// rows up to its own (masks per column, max -inf guards); otherwise one query
+// per sequence and rows past the sequence are the only masked ones.
+template <int D, int G, bool CAUSAL = false>
 struct MmaMath {
     using T = __nv_bfloat16;
+    static constexpr bool kCausal = CAUSAL;
     using Geom = TileGeom<T, D>;
     static constexpr int kSteps = D / 16;
     // G: query columns the state holds (a capacity: an item uses ncols <= G).
@@ -191,15 +195,20 @@ struct MmaMath {
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] *= scale_log2;
-        if (row0 + kTileRows - 1 > limit0) {
-            // Rows past what a column sees: past the sequence (one query per
-            // sequence), or past the query token's own row (several).
-            const int j0 = (2 * t4) / grp, j1 = (2 * t4 + 1) / grp;
-            const int r = row0 + gid;
-            if (r > limit0 + j0) c[0] = -INFINITY;
-            if (r > limit0 + j1) c[1] = -INFINITY;
-            if (r + 8 > limit0 + j0) c[2] = -INFINITY;
-            if (r + 8 > limit0 + j1) c[3] = -INFINITY;
+        if constexpr (CAUSAL) {
+            if (row0 + kTileRows - 1 > limit0) {
+                // Rows past the query token's own row.
+                const int j0 = (2 * t4) / grp, j1 = (2 * t4 + 1) / grp;
+                const int r = row0 + gid;
+                if (r > limit0 + j0) c[0] = -INFINITY;
+                if (r > limit0 + j1) c[1] = -INFINITY;
+                if (r + 8 > limit0 + j0) c[2] = -INFINITY;
+                if (r + 8 > limit0 + j1) c[3] = -INFINITY;
+            }
+        } else if (valid < kTileRows) {
+            // Rows past the sequence.
+            if (gid >= valid) c[0] = c[1] = -INFINITY;
+            if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
         }
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
@@ -210,10 +219,11 @@ struct MmaMath {
         }
         const float mn0 = fmaxf(m[0], mx0);
         const float mn1 = fmaxf(m[1], mx1);
-        // A column with no visible row yet keeps max -inf: exponentiate
-        // against 0 then, so that its weights are 0 rather than NaN.
-        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+        // With several query tokens, a column with no visible row yet keeps
+        // max -inf: exponentiate against 0 then, so that its weights are 0
+        // rather than NaN. (One query per sequence: every tile has a row.)
+        const float ref0 = (CAUSAL && mn0 == -INFINITY) ? 0.f : mn0;
+        const float ref1 = (CAUSAL && mn1 == -INFINITY) ? 0.f : mn1;
         const float al0 = fast_exp2(m[0] - ref0);
         const float al1 = fast_exp2(m[1] - ref1);
         const float p0 = fast_exp2(c[0] - ref0);
@@ -309,6 +319,7 @@ struct MmaMath {
 template <typename TT, int D, int G>
 struct SimtMath {
     using T = TT;
+    static constexpr bool kCausal = false;
     using Geom = TileGeom<T, D>;
     using E = ElemTraits<T>;
     static constexpr int kEpc = E::kPerChunk;               // elements per 16-byte chunk

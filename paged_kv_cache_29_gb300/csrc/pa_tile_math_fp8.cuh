@@ -64,6 +64,7 @@ __device__ __forceinline__ void mma_16816_f16(float* c, uint32_t a0, uint32_t a1
 template <int D, int G>
 struct Fp8MmaMath {
     using T = __nv_bfloat16;                    // q and out
+    static constexpr bool kCausal = false;
     using Geom = TileGeom<uint8_t, D>;
     static_assert(D == 128, "one 128-byte row of codes per token");
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
