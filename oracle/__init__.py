@@ -80,6 +80,8 @@ def _load():
         lib.pao_decode_kv.restype = I
         lib.pao_decode_multi.argtypes = [P, I, P, P, I, D, D, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode_multi.restype = I
+        lib.pao_decode_window.argtypes = [P, P, P, P, P, D, I, P, I, I, I, I, I, I, I, I, I]
+        lib.pao_decode_window.restype = I
         lib.pao_decode.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode.restype = I
         lib.pao_attention_weights.argtypes = [P, P, P, P, D, I, I, P, I, I, I, I, I, I, I, I]
@@ -223,6 +225,24 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale
     return out
 
 
+def decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, window,
+                  num_threads=0):
+    """fp64 sliding-window decode: each sequence attends to its last `window`
+    rows. q: [B][Hq][D] in the cache dtype -> [B][Hq][D] float64."""
+    q = _c(q, k_cache.dtype)
+    k_cache, v_cache = _c(k_cache), _c(v_cache)
+    bt, cl = _c(block_tables, np.int32), _c(context_lens, np.int32)
+    B, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    out = np.zeros((B, hq, d), dtype=np.float64)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    rc = _load().pao_decode_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(cl),
+                                   float(scale), int(window), _ptr(out), B, hq, hkv, d, bs, nb,
+                                   mb, _dtype_code(k_cache), int(num_threads))
+    _check(rc, "decode_window")
+    return out
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0):
     """fp64 decode attention. q: [B][Hq][D] in the cache dtype -> [B][Hq][D] float64."""
     q = _c(q, k_cache.dtype)
@@ -301,7 +321,8 @@ class use_library:
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("pao_append", "pao_copy_blocks", "pao_e4m3_decode", "pao_e4m3_encode",
-                     "pao_append_fp8", "pao_decode_kv", "pao_decode_multi", "pao_decode",
+                     "pao_append_fp8", "pao_decode_kv", "pao_decode_multi", "pao_decode_window",
+                     "pao_decode",
                      "pao_attention_weights",
                      "pao_decode_partitions", "pao_combine_partitions"):
             src = getattr(self._saved, name)

@@ -59,6 +59,11 @@
  *           (0-based) sits at row n - Q + j and attends to rows 0 .. n - Q + j,
  *           each by the single-query definition above.
  *
+ *  window   Sliding-window attention (pao_decode_window): a sequence of n rows
+ *           attends only to its last W rows, n - W .. n - 1 ("MLSys Engineer
+ *           -- Inference Systems Q&A", Q3: local-attention layers need only
+ *           the last W tokens; Q4: tiles wholly before the window are skipped).
+ *
  *  split    pao_decode_partitions / pao_combine_partitions restate the same
  *           attention as per-partition (max, sum, unnormalised output)
  *           triples merged by rescaling with exp(m_p - M), the rescale rule of
@@ -361,6 +366,75 @@ int pao_decode_multi(const void* q, int q_dtype, const void* k_cache, const void
                     for (int i = 0; i < rows; ++i)
                         for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
                 }
+            }
+        }
+        free(Kc); free(Vc); free(w); free(qv);
+    }
+    return err;
+}
+
+/* Sliding-window decode: sequence s attends to rows max(0, n - window) ..
+ * n - 1 (window >= 1). Same layouts and errors as pao_decode. */
+int pao_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, double scale,
+                      int window, double* out, int num_seqs, int num_heads, int num_kv_heads,
+                      int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                      int dtype, int num_threads) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, dtype);
+    if (rc != PAO_OK) return rc;
+    if (window < 1) return PAO_BAD_ARG;
+    const int G = num_heads / num_kv_heads;
+    const int units = num_seqs * num_kv_heads;
+    int err = PAO_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#else
+    const int nt = 1;
+    (void)num_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int u = 0; u < units; ++u) {
+        const int s = u / num_kv_heads, h = u % num_kv_heads;
+        const int n = context_lens[s];
+        for (int g = 0; g < G; ++g) {
+            double* o = out + ((size_t)s * num_heads + h * G + g) * head_dim;
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        }
+        if (n < 0 || (long)n > (long)max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            err = PAO_BAD_LEN;
+            continue;
+        }
+        if (n == 0) continue;
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* w = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!Kc || !Vc || !w || !qv) {
+#pragma omp atomic write
+            err = PAO_NO_MEMORY;
+            free(Kc); free(Vc); free(w); free(qv);
+            continue;
+        }
+        const int grc = gather(k_cache, v_cache, block_tables + (size_t)s * max_blocks_per_seq,
+                               n, h, num_kv_heads, head_dim, block_size, num_blocks, dtype, 1.0,
+                               1.0, Kc, Vc);
+        if (grc != PAO_OK) {
+#pragma omp atomic write
+            err = grc;
+        } else {
+            const int first = n > window ? n - window : 0;   /* rows first .. n - 1 */
+            const int rows = n - first;
+            for (int g = 0; g < G; ++g) {
+                const int qh = h * G + g;
+                double* o = out + ((size_t)s * num_heads + qh) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, dtype);
+                softmax_weights(qv, Kc + (size_t)first * head_dim, rows, head_dim, scale, w);
+                for (int i = 0; i < rows; ++i)
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += w[i] * Vc[(size_t)(first + i) * head_dim + d];
             }
         }
         free(Kc); free(Vc); free(w); free(qv);

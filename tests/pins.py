@@ -410,6 +410,36 @@ def pin_multi_query():
         raise AssertionError("n < Q must be rejected")
 
 
+# ---- sliding window ----------------------------------------------------------
+
+def pin_sliding_window():
+    """A window of W rows equals plain attention (scipy's softmax) over the
+    last W rows laid out contiguously; W >= n equals decode(); W = 1 returns
+    the last V row exactly."""
+    for dtype, bs in (("f32", 16), ("bf16", 4)):
+        step = small_step((1, 9, 16, 17, 40, 64), hq=6, hkv=3, d=8, dtype=dtype, bs=bs, seed=17)
+        k, v = _after_append(step)
+        full = oracle.decode(step.q, k, v, step.block_tables, step.context_lens, step.scale)
+        np.testing.assert_array_equal(
+            oracle.decode_window(step.q, k, v, step.block_tables, step.context_lens,
+                                 step.scale, 64), full)
+        kf, vf, qf = _f64(step, k), _f64(step, v), _f64(step, step.q)
+        G = step.num_heads // step.num_kv_heads
+        for W in (1, 5, 16, 17, 33):
+            got = oracle.decode_window(step.q, k, v, step.block_tables, step.context_lens,
+                                       step.scale, W)
+            for s_, n in enumerate(step.context_lens):
+                rows = [(step.block_tables[s_, i // bs], i % bs) for i in range(max(0, n - W), n)]
+                for qh in range(step.num_heads):
+                    h = qh // G
+                    K = np.array([kf[b, h, o] for b, o in rows])
+                    V = np.array([vf[b, h, o] for b, o in rows])
+                    w = softmax(step.scale * (K @ qf[s_, qh]))
+                    np.testing.assert_allclose(got[s_, qh], w @ V, rtol=0, atol=1e-12)
+                    if W == 1:
+                        np.testing.assert_array_equal(got[s_, qh], V[-1])
+
+
 # ---- P8: closed forms ---------------------------------------------------------
 
 def pin_closed_forms():
@@ -529,5 +559,6 @@ def pin_incremental_decoder():
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
             pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode, pin_multi_query,
+            pin_sliding_window,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]

@@ -43,6 +43,9 @@ MUTANTS = [
     ("multi_no_causality", "const int rows = n - Q + j + 1;", "const int rows = n;"),
     ("multi_q_head_major", "const size_t qrow = ((size_t)s * Q + j) * num_heads + qh;",
      "const size_t qrow = ((size_t)s * num_heads + qh) * Q + j;"),
+    ("window_off_by_one", "const int first = n > window ? n - window : 0;",
+     "const int first = n > window ? n - window + 1 : 0;"),
+    ("window_ignored", "const int first = n > window ? n - window : 0;", "const int first = 0;"),
     ("e4m3_bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
     ("e4m3_truncates", "const int q = (int)nearbyint(ldexp(a, 3 - E));",
      "const int q = (int)floor(ldexp(a, 3 - E));"),
