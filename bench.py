@@ -324,6 +324,9 @@ def run_native(args) -> dict | None:
         elif Qn > 1:
             pa.pa_decode_multi(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                                workspace=workspace, error_word=err, stream=st)
+        elif step.window > 0:
+            pa.pa_decode_window(q, k_cache, v_cache, tables, lens, step.scale, step.window, out,
+                                mcl, workspace=workspace, error_word=err, stream=st)
         else:
             pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                          workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
@@ -466,7 +469,8 @@ def run_native(args) -> dict | None:
         "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
         "config": {
             "workload": args.workload,
-            "num_seqs": step.num_seqs, "num_queries": step.num_queries, "num_heads": step.num_heads,
+            "num_seqs": step.num_seqs, "num_queries": step.num_queries, "window": step.window,
+            "num_heads": step.num_heads,
             "num_kv_heads": step.num_kv_heads, "head_dim": step.head_dim,
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),

@@ -215,6 +215,27 @@ pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cach
 size_t pa_decode_workspace_size_multi(int num_seqs, int num_queries, int num_heads,
                                       int head_dim, int max_context_len);
 
+/*
+ * Sliding-window decode: pa_decode where sequence s attends only to its last
+ * `window` rows, max(0, n - window) .. n - 1 (n = context_lens[s]), as
+ * local-attention layers do ("MLSys Engineer -- Inference Systems Q&A", Q3:
+ * local layers need only the last W tokens; Q4: tiles wholly before the
+ * window are never loaded). Partitions start at the 16-row tile holding the
+ * window's first row, so only about window rows per sequence are read.
+ * window >= 1 (window >= n attends to every row, as pa_decode). Same
+ * arguments, layouts, workspace (pa_decode_workspace_size is enough) and
+ * error behaviour as pa_decode; fp32 or bf16; block_size a multiple of 16,
+ * head_dim 64 or 128 and 1, 2, 4 or 8 query heads per KV head (else
+ * PA_ERR_UNSUPPORTED).
+ */
+pa_status pa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, int window, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, int32_t* error_word,
+                           struct CUstream_st* stream);
+
 /* Bytes of workspace pa_decode needs for these sizes (0 only for an empty
  * batch). */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);

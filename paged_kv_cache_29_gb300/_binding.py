@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_multi.restype = I
         L.pa_decode_workspace_size_multi.argtypes = [I, I, I, I, I]
         L.pa_decode_workspace_size_multi.restype = S
+        L.pa_decode_window.argtypes = [P, P, P, P, P, F, I, P, I, I, I, I, I, I, I, I, I, P, S,
+                                       P, P]
+        L.pa_decode_window.restype = I
         L.pa_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
         L.pa_copy_blocks.restype = I
         L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
@@ -268,6 +271,37 @@ def pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out,
                                _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode_multi")
+
+
+def pa_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
+                     max_context_len, workspace=None, error_word=None, stream=None) -> None:
+    """Sliding-window decode: each sequence attends to its last `window` rows."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("q", q, k_cache.dtype, 3)
+    _check_cuda("out", out, k_cache.dtype, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_decode_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), float(scale), int(window), _ptr(out), B, hq,
+                                hkv, d, bs, nb, int(block_tables.shape[1]), int(max_context_len),
+                                _dtype_code(k_cache), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(error_word),
+                                _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_decode_window")
 
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None) -> None:

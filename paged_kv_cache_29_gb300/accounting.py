@@ -52,18 +52,22 @@ class StepBytes:
 
 def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
                elem_bytes: int, block_size: int = 16, block_tables=None,
-               act_bytes: int | None = None, num_queries: int = 1) -> StepBytes:
+               act_bytes: int | None = None, num_queries: int = 1,
+               window: int = 0) -> StepBytes:
     """elem_bytes: bytes per cache element; act_bytes: bytes per element of q,
     out and the new K/V rows (default: elem_bytes); num_queries: new tokens
-    (queries) per sequence."""
+    (queries) per sequence; window: a sliding window of rows attended (0 =
+    all): K/V and table bytes count the attended rows only."""
     act = elem_bytes if act_bytes is None else act_bytes
     lens = np.asarray(context_lens, dtype=np.int64)
     B = int(lens.shape[0])
+    first = np.maximum(lens - window, 0) if window > 0 else np.zeros_like(lens)
     row = num_kv_heads * head_dim * elem_bytes          # one token, all KV heads, K or V
-    kv = int(lens.sum()) * row * 2
+    kv = int((lens - first).sum()) * row * 2
     Q = int(num_queries)
     q_out = B * Q * num_heads * head_dim * act * 2
-    used_entries = int(sum(blocks_for_tokens(int(n), block_size) for n in lens))
+    used_entries = int(sum(blocks_for_tokens(int(n), block_size) - int(f) // block_size
+                           for n, f in zip(lens, first)))
     tables = used_entries * 4 + B * 4
     active = int((lens > 0).sum())
     # new K and V rows read (act dtype) and written (cache dtype), slots read
@@ -72,8 +76,8 @@ def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
         kv_unique = kv
     else:
         bt = np.asarray(block_tables, dtype=np.int64)
-        slots = [bt[s, np.arange(n) // block_size] * block_size + np.arange(n) % block_size
-                 for s, n in enumerate(lens) if n > 0]
+        slots = [bt[s, np.arange(f, n) // block_size] * block_size + np.arange(f, n) % block_size
+                 for s, (n, f) in enumerate(zip(lens, first)) if n > 0]
         distinct = np.unique(np.concatenate(slots)).size if slots else 0
         kv_unique = int(distinct) * row * 2
     return StepBytes(kv=kv, q_out=q_out, tables=tables, append=append, kv_unique=kv_unique)
@@ -83,7 +87,7 @@ def step_bytes_for(step) -> StepBytes:
     """StepBytes of a workloads.DecodeStep."""
     return step_bytes(step.context_lens, step.num_heads, step.num_kv_heads, step.head_dim,
                       step.elem_bytes, step.block_size, step.block_tables, step.act_bytes,
-                      step.num_queries)
+                      step.num_queries, step.window)
 
 
 def decode_flops(context_lens, num_heads: int, head_dim: int) -> int:

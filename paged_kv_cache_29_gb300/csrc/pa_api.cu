@@ -116,14 +116,14 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
                       pa_dtype act_dtype, void* workspace, size_t workspace_bytes,
                       int32_t* error_word, const pa_decode_options* options,
-                      struct CUstream_st* stream, int num_queries = 1) {
+                      struct CUstream_st* stream, int num_queries = 1, int window = 0) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
                                                                : pa::kDefaultPartition;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
         !valid_cache_dtype(dtype) || !valid_dtype(act_dtype) || num_heads % num_kv_heads != 0 ||
-        num_queries < 1)
+        num_queries < 1 || window < 0 || (window > 0 && num_queries > 1))
         return PA_ERR_INVALID_ARG;
     if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
     if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
@@ -180,7 +180,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         return PA_ERR_UNSUPPORTED;
     }
     if (kernel == PA_KERNEL_GENERIC &&
-        pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem)
+        (window > 0 ||   // the direct-load kernel has no sliding window
+         pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem))
         return PA_ERR_UNSUPPORTED;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -195,6 +196,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     base.k_scale = k_scale;
     base.v_scale = v_scale;
     base.num_queries = num_queries;
+    base.window = window;
     base.num_heads = num_heads;
     base.num_kv_heads = num_kv_heads;
     base.head_dim = head_dim;
@@ -370,6 +372,20 @@ pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cach
                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
                        workspace_bytes, error_word, nullptr, stream, num_queries);
+}
+
+pa_status pa_decode_window(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, int window, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, int32_t* error_word,
+                           struct CUstream_st* stream) {
+    if (!valid_dtype(dtype) || window < 1) return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
+                       workspace_bytes, error_word, nullptr, stream, 1, window);
 }
 
 size_t pa_decode_workspace_size_multi(int num_seqs, int num_queries, int num_heads,

@@ -179,9 +179,10 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
     const int s = sq / p.num_queries;
     const int n = __ldg(p.context_lens + s);
     const int P = p.partition_size;
-    if (n <= P || n > p.context_cap) return;   // one partition (written directly) or flagged
-    if (n < p.num_queries) return;             // flagged
-    const int np = (n + P - 1) / P;
+    if (n > p.context_cap || n < p.num_queries) return;   // flagged
+    const int span = n - seq_row_base(n, p.window);       // rows of the partitions
+    if (span <= P) return;                     // one partition (written directly)
+    const int np = (span + P - 1) / P;
     const int nw = combine_warps(np);
     const int D = p.head_dim;
     const size_t row = static_cast<size_t>(sq) * p.num_heads + qh;

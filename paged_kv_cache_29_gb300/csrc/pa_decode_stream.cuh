@@ -145,7 +145,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // with cp.async one item ahead of their use.
         auto prefetch_ids = [&](const int4& it, int32_t* buf) {
             if (it.x >= 0) {
-                const int lo = it.z * P;
+                const int lo = seq_row_base(it.w, p.window) + it.z * P;
                 const int hi = min(it.w, lo + P);
                 const int b0 = lo / bs;
                 const int nblk = (hi - 1) / bs - b0 + 1;
@@ -166,13 +166,13 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
             cp_async_wait_group_1();                // this item's ids have landed
             __syncwarp();
-            const int b0 = (cur.z * P) / bs;
-            const int nblk = (min(cur.w, cur.z * P + P) - 1) / bs - b0 + 1;
+            const int lo = seq_row_base(cur.w, p.window) + cur.z * P;
+            const int hi = min(cur.w, lo + P);
+            const int b0 = lo / bs;
+            const int nblk = (hi - 1) / bs - b0 + 1;
             bool bad_lane = false;
             for (int i = lane; i < nblk; i += 32) bad_lane |= (ids[i] < 0) | (ids[i] >= p.num_blocks);
             const int cur_bad = __any_sync(0xffffffffu, bad_lane) ? 1 : 0;
-            const int lo = cur.z * P;
-            const int hi = min(cur.w, lo + P);
             const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
             if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
             // The item's tiles are padded with data-less slots up to a multiple
@@ -264,7 +264,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     bool aborted = false;
     for (int j = 0; it.x >= 0; ++j) {
         const int s = it.x, h = it.y, part = it.z, n = it.w;
-        const int lo = part * P;
+        const int base = seq_row_base(n, p.window);
+        const int lo = base + part * P;
         const int hi = min(n, lo + P);
         const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
         const int4 it_after = item_at(j + 2);
@@ -296,8 +297,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const int row0 = lo + kTileRows * (t - t0);
                     const int valid = min(kTileRows, hi - row0);
                     const uint32_t kb = ring_addr + stage * Geom::kStageBytes;
+                    // Rows of the tile before a sliding window (<= 0: none).
+                    const int skip = p.window > 0 ? n - p.window - row0 : 0;
                     math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane, row0, limit0,
-                              grp);
+                              grp, skip);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
@@ -324,7 +327,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
         for (int w = 0; w < W; ++w) any_bad |= warp_bad[(j & 1) * W + w] != 0;
         if (any_bad) continue;              // flagged by the producer; output left unspecified
-        const int nparts = (n + P - 1) / P;
+        const int nparts = (n - base + P - 1) / P;
         for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
             const int g = idx / D;            // query column
             const int d = idx - g * D;

@@ -28,6 +28,7 @@ struct DecodeParams {
     float v_scale;                 // FP8 caches: V value = v_scale * e4m3(code) (else 1)
     int num_seqs;
     int num_queries;               // query tokens per sequence, the last rows of each (>= 1)
+    int window;                    // sliding window: attend to the last `window` rows (0 = all)
     int num_heads;
     int num_kv_heads;
     int head_dim;
@@ -81,6 +82,13 @@ size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block
 
 // Merge of partition partials for sequences longer than one partition.
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
+
+// First row of a sequence's partitions: 0, or with a sliding window of W rows
+// the window's first row rounded down to a 16-row tile (partition p covers
+// rows base + p * partition_size ..). Depends only on n and W.
+__host__ __device__ inline int seq_row_base(int n, int window) {
+    return (window > 0 && n > window) ? ((n - window) / 16) * 16 : 0;
+}
 
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxDevices = 64;      // devices whose per-kernel launch set-up is cached

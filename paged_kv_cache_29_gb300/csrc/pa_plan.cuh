@@ -2,7 +2,9 @@
 // every CTA of that launch for itself.
 //
 // A work item is one (sequence, KV head, partition) of at most partition_size
-// rows. The items of the batch are numbered in one global order:
+// rows (partitions start at seq_row_base: row 0, or the tile holding the first
+// row of a sliding window). The items of the batch are numbered in one global
+// order:
 //   1. every full partition (partition_size rows), by sequence, partition,
 //      KV head;
 //   2. then the partial last partitions, in kBuckets buckets of decreasing
@@ -90,7 +92,8 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
     for (int s0 = 0; s0 < B; s0 += NT) {
         const int s = s0 + tid;
         const int n = s < B ? plan_len(p, s, s % C == c) : -1;
-        const int nf = n > 0 ? n / P : 0;
+        const int span = n > 0 ? n - seq_row_base(n, p.window) : 0;   // rows of its partitions
+        const int nf = span / P;
         int incl = nf;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -112,7 +115,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
             const int unit = k / Hkv;
             p.items[k] = make_int4(s, k - unit * Hkv, unit - pf, n);
         });
-        const int b = n > 0 ? plan_bucket(n % P, P) : -1;
+        const int b = n > 0 ? plan_bucket(span % P, P) : -1;
         if (b >= 0) atomicAdd(&bcount[b], 1);
         if (n == 0 && s % C == c) {
             // the sequence's num_queries output rows
@@ -144,7 +147,8 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
     for (int s0 = 0; s0 < B; s0 += NT) {
         const int s = s0 + tid;
         const int n = s < B ? plan_len(p, s, false) : -1;
-        const int b = n > 0 ? plan_bucket(n % P, P) : -1;
+        const int span = n > 0 ? n - seq_row_base(n, p.window) : 0;
+        const int b = n > 0 ? plan_bucket(span % P, P) : -1;
         const unsigned same = __match_any_sync(0xffffffffu, b);
         if (lane < kPlanBuckets) wcnt[warp * kPlanBuckets + lane] = 0;
         __syncwarp();
@@ -154,7 +158,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
             int j = bcursor[b] + brun[b] + __popc(same & lt_mask);
             for (int w = 0; w < warp; ++w) j += wcnt[w * kPlanBuckets + b];
             const int a = full_items + j * Hkv;
-            const int nf = n / P;
+            const int nf = span / P;
             for_own_items(a, a + Hkv, c, C, [&](int k) { p.items[k] = make_int4(s, k - a, nf, n); });
         }
         __syncthreads();

@@ -176,10 +176,12 @@ struct MmaMath {
 
     // valid: rows of the tile before the end of the sequence (V rows past it
     // are zeroed). Row row0 + i is visible to query column c when row0 + i <=
-    // limit0 + c / grp (limit0: the last row query token 0 sees).
+    // limit0 + c / grp (limit0: the last row query token 0 sees) and i >= skip
+    // (rows before a sliding window; skip <= 0 without one). A tile always
+    // holds a visible row for one query per sequence.
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float scale_log2, int lane, int row0, int limit0,
-                                         int grp) {
+                                         int grp, int skip) {
         const int mi = lane >> 3;
         const int lr = lane & 7;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -205,10 +207,17 @@ struct MmaMath {
                 if (r + 8 > limit0 + j0) c[2] = -INFINITY;
                 if (r + 8 > limit0 + j1) c[3] = -INFINITY;
             }
-        } else if (valid < kTileRows) {
-            // Rows past the sequence.
-            if (gid >= valid) c[0] = c[1] = -INFINITY;
-            if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+        } else {
+            if (valid < kTileRows) {
+                // Rows past the sequence.
+                if (gid >= valid) c[0] = c[1] = -INFINITY;
+                if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+            }
+            if (skip > 0) {
+                // Rows before a sliding window.
+                if (gid < skip) c[0] = c[1] = -INFINITY;
+                if (gid + 8 < skip) c[2] = c[3] = -INFINITY;
+            }
         }
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
@@ -388,11 +397,12 @@ struct SimtMath {
         }
     }
 
-    // One query per sequence: rows past `valid` are masked (row0, limit0 and
-    // grp describe the same boundary and are not needed).
+    // One query per sequence: rows past `valid` are masked (limit0 and grp
+    // describe the same boundary and are not needed), and the first `skip`
+    // rows (a sliding window starting inside this tile).
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float /*scale_log2*/, int /*lane*/, int /*row0*/,
-                                         int /*limit0*/, int /*grp*/) {
+                                         int /*limit0*/, int /*grp*/, int skip) {
         const uint32_t kbox = kbase + (ch >> 3) * kBoxBytes;
         const uint32_t vbox = vbase + (ch >> 3) * kBoxBytes;
         const int cc = ch & 7;
@@ -419,11 +429,11 @@ struct SimtMath {
 #pragma unroll
                     for (int off = 1; off < kLpr; off <<= 1)
                         sc[j][g] += __shfl_xor_sync(0xffffffffu, sc[j][g], off);
-            if (valid < kTileRows) {
+            if (valid < kTileRows || skip > 0) {
 #pragma unroll
                 for (int j = 0; j < kSub; ++j) {
                     const int row = (sub * kSub + j) * kRpp + rr;
-                    if (row >= valid)
+                    if (row >= valid || row < skip)
 #pragma unroll
                         for (int g = 0; g < G; ++g) sc[j][g] = -INFINITY;
                 }
@@ -437,14 +447,17 @@ struct SimtMath {
                 for (int off = kLpr; off < 32; off <<= 1)
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
                 const float mn = fmaxf(m[g], mx);
-                const float al = fast_exp2(m[g] - mn);
+                // Rows before a window can mask a whole sub-step while the
+                // max is still -inf: exponentiate against 0 then (weights 0).
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                const float al = fast_exp2(m[g] - ref);
                 m[g] = mn;
                 l[g] *= al;
 #pragma unroll
                 for (int e = 0; e < kEpc; ++e) o[g][e] *= al;
 #pragma unroll
                 for (int j = 0; j < kSub; ++j) {
-                    sc[j][g] = fast_exp2(sc[j][g] - mn);
+                    sc[j][g] = fast_exp2(sc[j][g] - ref);
                     l[g] += sc[j][g];
                 }
             }

@@ -116,7 +116,8 @@ struct Fp8MmaMath {
     }
 
     // S^T of one 16-row tile: c = S^T[token gid, gid + 8][heads 2 t4, 2 t4 + 1].
-    __device__ __forceinline__ void qk(uint32_t kbase, int valid, float* c) const {
+    // Rows past `valid` or before `skip` (a sliding window) are masked.
+    __device__ __forceinline__ void qk(uint32_t kbase, int valid, int skip, float* c) const {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint4 r0 = lds128(swizzled(kbase, gid, 2 * t4 + half));
@@ -135,6 +136,10 @@ struct Fp8MmaMath {
         if (valid < kTileRows) {
             if (gid >= valid) c[0] = c[1] = -INFINITY;
             if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+        }
+        if (skip > 0) {
+            if (gid < skip) c[0] = c[1] = -INFINITY;
+            if (gid + 8 < skip) c[2] = c[3] = -INFINITY;
         }
     }
 
@@ -198,12 +203,13 @@ struct Fp8MmaMath {
     }
 
     // One 16-row tile per step.
-    // One query per sequence: rows past `valid` are masked.
+    // One query per sequence: rows past `valid` and the first `skip` rows (a
+    // sliding window) are masked; a tile always holds a visible row.
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float /*scale_log2: folded into q'*/, int /*lane*/,
-                                         int /*row0*/, int /*limit0*/, int /*grp*/) {
+                                         int /*row0*/, int /*limit0*/, int /*grp*/, int skip) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
-        qk(kbase, valid, c);
+        qk(kbase, valid, skip, c);
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
 #pragma unroll

@@ -25,6 +25,8 @@ workloads:
                  and the append quantises them
   8b_gqa_mq2     the 8b_gqa batch with two new tokens per sequence verified
                  together (multi-query decode: each query attends causally)
+  8b_gqa_win1024 the 8b_gqa batch under a 1,024-row sliding window (a local
+                 attention layer)
 
 Every value of q, of the new K/V rows and of the whole pool (used or not) is
 drawn N(0, 1) in fp32 and stored in the cache dtype (bf16 by round to nearest
@@ -47,7 +49,8 @@ from .block_manager import BlockManager
 
 # Seeds of the five named workloads, in the order listed above.
 WORKLOAD_SEEDS = {"tiny": 0, "7b_mha": 1, "8b_gqa": 2, "long_skew": 3, "prefix_shared": 4,
-                  "8b_gqa_fp8": 2, "8b_gqa_mq2": 2}   # variants of the 8b_gqa batch
+                  "8b_gqa_fp8": 2, "8b_gqa_mq2": 2,
+                  "8b_gqa_win1024": 2}                # variants of the 8b_gqa batch
 PAD_BLOCK = -1
 
 
@@ -149,6 +152,7 @@ class DecodeStep:
     meta: dict = field(default_factory=dict)
     act_dtype: str = ""               # dtype of q, out, k_new, v_new ("" = cache_dtype)
     num_queries: int = 1              # new tokens per sequence, the last rows of each
+    window: int = 0                   # sliding window: attend to the last `window` rows
     k_scale: float = 1.0              # FP8 caches: value = scale * e4m3(code)
     v_scale: float = 1.0
 
@@ -295,6 +299,13 @@ def gqa_8b_mq2(seed: int = WORKLOAD_SEEDS["8b_gqa_mq2"], batch: int = 128) -> De
                       seed=seed, rng=rng, num_queries=2)
 
 
+def gqa_8b_win1024(seed: int = WORKLOAD_SEEDS["8b_gqa_win1024"], batch: int = 128) -> DecodeStep:
+    step = gqa_8b(seed, batch)
+    step.name = "8b_gqa_win1024"
+    step.window = 1024
+    return step
+
+
 def long_skew(seed: int = WORKLOAD_SEEDS["long_skew"]) -> DecodeStep:
     return build_step("long_skew", [100_000] + [1_500] * 7, num_heads=32, num_kv_heads=8,
                       head_dim=128, seed=seed)
@@ -345,6 +356,7 @@ WORKLOADS = {
     "prefix_shared": prefix_shared,
     "8b_gqa_fp8": gqa_8b_fp8,
     "8b_gqa_mq2": gqa_8b_mq2,
+    "8b_gqa_win1024": gqa_8b_win1024,
 }
 
 
