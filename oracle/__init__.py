@@ -82,6 +82,10 @@ def _load():
         lib.pao_decode_multi.restype = I
         lib.pao_decode_window.argtypes = [P, P, P, P, P, D, I, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode_window.restype = I
+        lib.pao_append_int8.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I]
+        lib.pao_append_int8.restype = I
+        lib.pao_decode_int8.argtypes = [P, I, P, P, P, P, P, P, D, P, I, I, I, I, I, I, I, I]
+        lib.pao_decode_int8.restype = I
         lib.pao_decode.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, I, I, I, I]
         lib.pao_decode.restype = I
         lib.pao_attention_weights.argtypes = [P, P, P, P, D, I, I, P, I, I, I, I, I, I, I, I]
@@ -243,6 +247,43 @@ def decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, window
     return out
 
 
+def append_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales, v_scales) -> int:
+    """Quantising append into an INT8 cache (in place): codes int8
+    [NB][Hkv][bs][D], scales float32 [NB][Hkv][bs]; scale = max|row| / 127,
+    code = round-half-even(x / scale). Returns the out-of-range slot count."""
+    for a, dt in ((k_cache, np.int8), (v_cache, np.int8), (k_scales, np.float32),
+                  (v_scales, np.float32)):
+        if not a.flags.c_contiguous or a.dtype != dt:
+            raise OracleError("INT8 caches and scales must be C-contiguous int8 / float32")
+    nb, hkv, bs, d = k_cache.shape
+    k_new, v_new = _c(k_new), _c(v_new, k_new.dtype)
+    slots = _c(slot_mapping, np.int64)
+    rc = _load().pao_append_int8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(slots),
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                 int(slots.shape[0]), hkv, d, bs, nb)
+    if rc < 0:
+        _check(rc, "append_int8")
+    return rc
+
+
+def decode_int8(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, scale,
+                num_threads=0):
+    """fp64 decode attention over an INT8 cache with per-row scales."""
+    q = _c(q)
+    k_cache, v_cache = _c(k_cache, np.int8), _c(v_cache, np.int8)
+    k_scales, v_scales = _c(k_scales, np.float32), _c(v_scales, np.float32)
+    bt, cl = _c(block_tables, np.int32), _c(context_lens, np.int32)
+    B, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    out = np.zeros((B, hq, d), dtype=np.float64)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    rc = _load().pao_decode_int8(_ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(k_scales), _ptr(v_scales), _ptr(bt), _ptr(cl), float(scale),
+                                 _ptr(out), B, hq, hkv, d, bs, nb, mb, int(num_threads))
+    _check(rc, "decode_int8")
+    return out
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0):
     """fp64 decode attention. q: [B][Hq][D] in the cache dtype -> [B][Hq][D] float64."""
     q = _c(q, k_cache.dtype)
@@ -322,6 +363,7 @@ class use_library:
         lib = ctypes.CDLL(self.path)
         for name in ("pao_append", "pao_copy_blocks", "pao_e4m3_decode", "pao_e4m3_encode",
                      "pao_append_fp8", "pao_decode_kv", "pao_decode_multi", "pao_decode_window",
+                     "pao_append_int8", "pao_decode_int8",
                      "pao_decode",
                      "pao_attention_weights",
                      "pao_decode_partitions", "pao_combine_partitions"):

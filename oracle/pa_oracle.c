@@ -59,6 +59,14 @@
  *           (0-based) sits at row n - Q + j and attends to rows 0 .. n - Q + j,
  *           each by the single-query definition above.
  *
+ *  int8     An INT8 cache stores each (token, KV head) row of K (and of V) as
+ *           int8 codes with one fp32 scale per row: scale = max|x| / 127 and
+ *           code = x / scale rounded to the nearest integer, ties to even
+ *           (the division in fp32), so value = scale * code ("MLSys Engineer
+ *           -- Inference Systems Q&A", Q3: INT8 KV with per-token scaling,
+ *           scale = max(|K_row|) / 127, dequantised before the softmax). An
+ *           all-zero row gets scale 0 and codes 0.
+ *
  *  window   Sliding-window attention (pao_decode_window): a sequence of n rows
  *           attends only to its last W rows, n - W .. n - 1 ("MLSys Engineer
  *           -- Inference Systems Q&A", Q3: local-attention layers need only
@@ -185,6 +193,56 @@ int pao_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, 
         memmove((char*)v_cache + (size_t)dst * block_bytes,
                 (const char*)v_cache + (size_t)src * block_bytes, block_bytes);
     }
+    return bad;
+}
+
+/* Per-row INT8 quantisation of one row of n binary32 values. */
+static float quantize_row_int8(const float* x, int n, int8_t* codes) {
+    float amax = 0.0f;
+    for (int d = 0; d < n; ++d) {
+        const float a = fabsf(x[d]);
+        if (a > amax) amax = a;
+    }
+    const float scale = amax / 127.0f;
+    for (int d = 0; d < n; ++d) {
+        if (scale == 0.0f) { codes[d] = 0; continue; }
+        float c = nearbyintf(x[d] / scale);
+        if (c > 127.0f) c = 127.0f;
+        if (c < -127.0f) c = -127.0f;
+        codes[d] = (int8_t)c;
+    }
+    return scale;
+}
+
+/* Append into an INT8 cache: codes [NB][Hkv][bs][D] int8, scales [NB][Hkv][bs]
+ * fp32, one per (row, KV head), for K and for V. k_new/v_new in new_dtype (0
+ * or 1). Returns the out-of-range slot count, or PAO_BAD_ARG. */
+int pao_append_int8(const void* k_new, const void* v_new, int new_dtype,
+                    const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
+                    float* k_scales, float* v_scales, int num_tokens, int num_kv_heads,
+                    int head_dim, int block_size, int num_blocks) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (new_dtype != 0 && new_dtype != 1))
+        return PAO_BAD_ARG;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    float* row = (float*)malloc(sizeof(float) * (size_t)head_dim);
+    if (!row) return PAO_NO_MEMORY;
+    int bad = 0;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) { ++bad; continue; }
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)t * num_kv_heads + h) * (size_t)head_dim;
+            const size_t r = ((size_t)blk * num_kv_heads + h) * block_size + off;
+            for (int d = 0; d < head_dim; ++d) row[d] = (float)load_elem(k_new, src + d, new_dtype);
+            k_scales[r] = quantize_row_int8(row, head_dim, k_cache + r * head_dim);
+            for (int d = 0; d < head_dim; ++d) row[d] = (float)load_elem(v_new, src + d, new_dtype);
+            v_scales[r] = quantize_row_int8(row, head_dim, v_cache + r * head_dim);
+        }
+    }
+    free(row);
     return bad;
 }
 
@@ -435,6 +493,79 @@ int pao_decode_window(const void* q, const void* k_cache, const void* v_cache,
                 for (int i = 0; i < rows; ++i)
                     for (int d = 0; d < head_dim; ++d)
                         o[d] += w[i] * Vc[(size_t)(first + i) * head_dim + d];
+            }
+        }
+        free(Kc); free(Vc); free(w); free(qv);
+    }
+    return err;
+}
+
+/* Decode attention over an INT8 cache with per-row scales: K_i = k_scale_i *
+ * code_i (fp64), same for V. q in q_dtype (0 or 1); out fp64. */
+int pao_decode_int8(const void* q, int q_dtype, const int8_t* k_cache, const int8_t* v_cache,
+                    const float* k_scales, const float* v_scales,
+                    const int32_t* block_tables, const int32_t* context_lens, double scale,
+                    double* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int max_blocks_per_seq, int num_threads) {
+    int rc = check_shapes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, q_dtype);
+    if (rc != PAO_OK) return rc;
+    const int G = num_heads / num_kv_heads;
+    const int units = num_seqs * num_kv_heads;
+    int err = PAO_OK;
+#ifdef _OPENMP
+    const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#else
+    const int nt = 1;
+    (void)num_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+    for (int u = 0; u < units; ++u) {
+        const int s = u / num_kv_heads, h = u % num_kv_heads;
+        const int n = context_lens[s];
+        for (int g = 0; g < G; ++g) {
+            double* o = out + ((size_t)s * num_heads + h * G + g) * head_dim;
+            for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        }
+        if (n < 0 || (long)n > (long)max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            err = PAO_BAD_LEN;
+            continue;
+        }
+        if (n == 0) continue;
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)n * head_dim + 1));
+        double* w = (double*)malloc(sizeof(double) * ((size_t)n + 1));
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!Kc || !Vc || !w || !qv) {
+#pragma omp atomic write
+            err = PAO_NO_MEMORY;
+            free(Kc); free(Vc); free(w); free(qv);
+            continue;
+        }
+        int grc = PAO_OK;
+        const int32_t* table = block_tables + (size_t)s * max_blocks_per_seq;
+        for (int i = 0; i < n && grc == PAO_OK; ++i) {
+            const int32_t blk = table[i / block_size];
+            if (blk < 0 || blk >= num_blocks) { grc = PAO_BAD_BLOCK; break; }
+            const size_t r = ((size_t)blk * num_kv_heads + h) * block_size + i % block_size;
+            for (int d = 0; d < head_dim; ++d) {
+                Kc[(size_t)i * head_dim + d] = (double)k_scales[r] * (double)k_cache[r * head_dim + d];
+                Vc[(size_t)i * head_dim + d] = (double)v_scales[r] * (double)v_cache[r * head_dim + d];
+            }
+        }
+        if (grc != PAO_OK) {
+#pragma omp atomic write
+            err = grc;
+        } else {
+            for (int g = 0; g < G; ++g) {
+                const int qh = h * G + g;
+                double* o = out + ((size_t)s * num_heads + qh) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    qv[d] = load_elem(q, ((size_t)s * num_heads + qh) * head_dim + d, q_dtype);
+                softmax_weights(qv, Kc, n, head_dim, scale, w);
+                for (int i = 0; i < n; ++i)
+                    for (int d = 0; d < head_dim; ++d) o[d] += w[i] * Vc[(size_t)i * head_dim + d];
             }
         }
         free(Kc); free(Vc); free(w); free(qv);

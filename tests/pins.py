@@ -410,6 +410,66 @@ def pin_multi_query():
         raise AssertionError("n < Q must be rejected")
 
 
+# ---- INT8 cache with per-row scales --------------------------------------------
+
+def pin_int8_append():
+    """Every appended row's codes reconstruct it within half a step of its
+    scale, stay within +-127 and reach 127 in magnitude at the row's largest
+    element; an all-zero row gets scale 0 and codes 0; nothing else moves."""
+    rng = np.random.default_rng(51)
+    nb, hkv, bs, d, T = 6, 2, 4, 16, 6
+    for new_dtype in ("f32", "bf16"):
+        x = rng.standard_normal((T, 2, hkv, d)).astype(np.float32)
+        x *= 10.0 ** rng.uniform(-3, 3, (T, 2, hkv, 1)).astype(np.float32)
+        x[2, :, 1] = 0.0                                       # an all-zero row
+        kn = wl.to_cache_dtype(x[:, 0], new_dtype)
+        vn = wl.to_cache_dtype(x[:, 1], new_dtype)
+        kc = rng.integers(-128, 128, (nb, hkv, bs, d)).astype(np.int8)
+        vc = rng.integers(-128, 128, (nb, hkv, bs, d)).astype(np.int8)
+        ks = rng.uniform(0.1, 1.0, (nb, hkv, bs)).astype(np.float32)
+        vs = rng.uniform(0.1, 1.0, (nb, hkv, bs)).astype(np.float32)
+        before = [a.copy() for a in (kc, vc, ks, vs)]
+        slots = np.array([3, -1, 17, 0, nb * bs + 2, 9], np.int64)
+        assert oracle.append_int8(kn, vn, slots, kc, vc, ks, vs) == 1
+        written = set()
+        for t, slot in enumerate(slots):
+            if not 0 <= slot < nb * bs:
+                continue
+            b, o = slot // bs, slot % bs
+            for new, codes, scales in ((kn, kc, ks), (vn, vc, vs)):
+                vals = wl.as_f32(new[t], new_dtype).astype(np.float64)
+                for h in range(hkv):
+                    row, c, sc = vals[h], codes[b, h, o].astype(np.float64), float(scales[b, h, o])
+                    written.add((b, h, o))
+                    if not row.any():
+                        assert sc == 0.0 and not c.any()
+                        continue
+                    assert np.abs(c).max() <= 127 and np.abs(c[np.argmax(np.abs(row))]) == 127
+                    assert np.all(np.abs(row - sc * c) <= sc / 2 * (1 + 1e-6)), (t, h)
+        for a, a0 in zip((kc, vc, ks, vs), before):
+            for idx in np.ndindex(nb, hkv, bs):
+                if idx not in written:
+                    np.testing.assert_array_equal(a[idx], a0[idx])
+
+
+def pin_int8_decode():
+    """Attention over INT8 codes with per-row scales equals the pure-Python
+    brute force over the fp64 values scale * code."""
+    rng = np.random.default_rng(52)
+    step = small_step((1, 7, 16, 23), hq=4, hkv=2, d=8, dtype="bf16", bs=4, seed=6)
+    kc = rng.integers(-127, 128, step.k_cache.shape).astype(np.int8)
+    vc = rng.integers(-127, 128, step.v_cache.shape).astype(np.int8)
+    ks = rng.uniform(0.005, 0.05, step.k_cache.shape[:3]).astype(np.float32)
+    vs = rng.uniform(0.005, 0.05, step.v_cache.shape[:3]).astype(np.float32)
+    got = oracle.decode_int8(step.q, kc, vc, ks, vs, step.block_tables, step.context_lens,
+                             step.scale)
+    kf = (ks[..., None].astype(np.float64) * kc).tolist()
+    vf = (vs[..., None].astype(np.float64) * vc).tolist()
+    want = np.array(brute.decode(_f64(step, step.q).tolist(), kf, vf, step.block_tables.tolist(),
+                                 step.context_lens.tolist(), step.scale, 4))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
 # ---- sliding window ----------------------------------------------------------
 
 def pin_sliding_window():
@@ -559,6 +619,6 @@ def pin_incremental_decoder():
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
             pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode, pin_multi_query,
-            pin_sliding_window,
+            pin_sliding_window, pin_int8_append, pin_int8_decode,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]
