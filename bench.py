@@ -277,6 +277,7 @@ def run_native(args) -> dict | None:
     cd = step.cache_dtype
 
     fp8 = cd == "fp8"
+    int8 = cd == "int8"
 
     def up(a):
         # bf16 arrays are uint16 bit patterns; FP8 pools stay uint8 codes
@@ -287,6 +288,8 @@ def run_native(args) -> dict | None:
 
     q, k_new, v_new = up(step.q), up(step.k_new), up(step.v_new)
     k_cache, v_cache = up(step.k_cache), up(step.v_cache)
+    if int8:
+        k_rs, v_rs = up(step.k_row_scales), up(step.v_row_scales)
     slots, tables, lens = up(step.slot_mapping), up(step.block_tables), up(step.context_lens)
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -309,7 +312,10 @@ def run_native(args) -> dict | None:
     launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
 
     def do_append(st):
-        if fp8:
+        if int8:
+            pa.pa_reshape_and_cache_int8(k_new, v_new, slots, k_cache, v_cache, k_rs, v_rs,
+                                         error_word=err, stream=st)
+        elif fp8:
             pa.pa_reshape_and_cache_fp8(k_new, v_new, slots, k_cache, v_cache, step.k_scale,
                                         step.v_scale, error_word=err, stream=st)
         else:
@@ -317,7 +323,10 @@ def run_native(args) -> dict | None:
                                     stream=st)
 
     def do_decode(st):
-        if fp8:
+        if int8:
+            pa.pa_decode_int8(q, k_cache, v_cache, k_rs, v_rs, tables, lens, step.scale, out,
+                              mcl, workspace=workspace, error_word=err, stream=st)
+        elif fp8:
             pa.pa_decode_fp8(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                              step.k_scale, step.v_scale, workspace=workspace, error_word=err,
                              stream=st)
@@ -428,17 +437,20 @@ def run_native(args) -> dict | None:
 
     # Copy-on-write block copies (pa_copy_blocks): COPY_PAIRS random distinct
     # (src, dst) pairs of this pool, after every other measurement (it
-    # overwrites pool blocks).
-    pairs = min(COPY_PAIRS, step.num_blocks // 2)
-    perm = torch.randperm(step.num_blocks, generator=torch.Generator().manual_seed(7))
-    mapping = torch.stack([perm[:pairs], perm[pairs:2 * pairs]], dim=1).to(dev)
-    for _ in range(args.warmup):
-        pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err, stream=stream)
-    copy_ms = timed(lambda: pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err,
-                                              stream=stream), K)
-    block_bytes = step.num_kv_heads * step.block_size * step.head_dim * step.elem_bytes
-    copy_bytes = pairs * 2 * 2 * block_bytes + pairs * 16      # K and V read + written, the pairs
-    copy_avg = sum(copy_ms) / K
+    # overwrites pool blocks). INT8 pools carry row scales pa_copy_blocks
+    # does not move: not measured there.
+    copy_info = None
+    if not int8:
+        pairs = min(COPY_PAIRS, step.num_blocks // 2)
+        perm = torch.randperm(step.num_blocks, generator=torch.Generator().manual_seed(7))
+        mapping = torch.stack([perm[:pairs], perm[pairs:2 * pairs]], dim=1).to(dev)
+        for _ in range(args.warmup):
+            pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err, stream=stream)
+        copy_ms = timed(lambda: pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err,
+                                                  stream=stream), K)
+        block_bytes = step.num_kv_heads * step.block_size * step.head_dim * step.elem_bytes
+        copy_bytes = pairs * 2 * 2 * block_bytes + pairs * 16   # K and V read + written, pairs
+        copy_info = (pairs, copy_bytes, sum(copy_ms) / K)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
@@ -465,7 +477,7 @@ def run_native(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if fp8 else cd,
+        "dtype": "fp8_e4m3" if fp8 else ("int8 codes, fp32 row scales" if int8 else cd),
         "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
         "config": {
             "workload": args.workload,
@@ -507,13 +519,13 @@ def run_native(args) -> dict | None:
         },
         "gpu_launches": launches_per_step * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
-        "copy_blocks": {
-            "pairs": pairs,
-            "bytes_per_call": copy_bytes,
-            "ms_per_call": round(copy_avg, 5),
-            "achieved": round(copy_bytes / (copy_avg * 1e-3) / 1e9, 2),
+        "copy_blocks": None if copy_info is None else {
+            "pairs": copy_info[0],
+            "bytes_per_call": copy_info[1],
+            "ms_per_call": round(copy_info[2], 5),
+            "achieved": round(copy_info[1] / (copy_info[2] * 1e-3) / 1e9, 2),
             "unit": "GB/s",
-            "frac": round(copy_bytes / (copy_avg * 1e-3) / 1e9 / peak, 4),
+            "frac": round(copy_info[1] / (copy_info[2] * 1e-3) / 1e9 / peak, 4),
             "note": "pa_copy_blocks of random distinct block pairs of this pool (copy-on-write), "
                     "CUDA events per call, L2 flushed between calls",
         },

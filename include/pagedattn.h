@@ -71,7 +71,13 @@ typedef enum pa_status {
  * pa_decode_fp8). An FP8 cache halves the bytes per token ("Forward Deployed
  * Engineering Interview", Chapter 2 "Batching and the KV Cache": FP8 KV, scales
  * per tensor, 1.0 when uncalibrated). */
-typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1, PA_DTYPE_FP8_E4M3 = 2 } pa_dtype;
+typedef enum pa_dtype {
+    PA_DTYPE_F32 = 0,
+    PA_DTYPE_BF16 = 1,
+    PA_DTYPE_FP8_E4M3 = 2,
+    PA_DTYPE_INT8 = 3 /* cache type only: int8 codes with one fp32 scale per (row, KV head);
+                         pa_reshape_and_cache_int8, pa_decode_int8 */
+} pa_dtype;
 
 /* Bits the kernels OR into *error_word. */
 #define PA_DEVERR_BLOCK_ID 0x1  /* a block-table entry outside [0, num_blocks) */
@@ -111,6 +117,43 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, pa_dtyp
                                    int num_tokens, int num_kv_heads, int head_dim,
                                    int block_size, int num_blocks, float k_scale, float v_scale,
                                    int32_t* error_word, struct CUstream_st* stream);
+
+/*
+ * Quantising append into an INT8 cache with one scale per (row, KV head)
+ * ("MLSys Engineer -- Inference Systems Q&A", Q3: INT8 KV with per-token
+ * scaling, scale = max(|K_row|) / 127):
+ *   scale = max_d |x[d]| / 127,  code[d] = round_half_even(x[d] / scale)
+ * for the new K row x = k_new[t][h] (and V), both divisions in fp32 (IEEE),
+ * codes clamped to [-127, 127]; an all-zero row gets scale 0 and codes 0.
+ * k_cache, v_cache: int8 [num_blocks][num_kv_heads][block_size][head_dim];
+ * k_scales, v_scales: fp32 [num_blocks][num_kv_heads][block_size], 16-byte
+ * aligned. k_new, v_new: new_dtype (PA_DTYPE_F32 or PA_DTYPE_BF16). head_dim
+ * 16..256, a multiple of 16. Slots as in pa_reshape_and_cache.
+ */
+pa_status pa_reshape_and_cache_int8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                                    const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                    float* k_scales, float* v_scales, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, int32_t* error_word,
+                                    struct CUstream_st* stream);
+
+/*
+ * pa_decode over an INT8 cache with per-row scales, bf16 q and out:
+ *   K_i = k_scales[row i] * code(K_i), V_i likewise, then the pa_decode sum.
+ * Codes are widened to f16 in registers (exact) and multiplied on tensor
+ * cores with fp32 accumulation; each score row is multiplied by its K scale
+ * and each probability by its V scale before the P.V product. Same
+ * partitioning, merge, workspace and error behaviour as pa_decode. Supported:
+ * head_dim 128, block_size a multiple of 16, 1, 2, 4 or 8 query heads per KV
+ * head (else PA_ERR_UNSUPPORTED).
+ */
+pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scales, const float* v_scales,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_seq,
+                         int max_context_len, void* workspace, size_t workspace_bytes,
+                         int32_t* error_word, struct CUstream_st* stream);
 
 /*
  * Copy-on-write of whole blocks: for each pair i,

@@ -70,6 +70,10 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_window.argtypes = [P, P, P, P, P, F, I, P, I, I, I, I, I, I, I, I, I, P, S,
                                        P, P]
         L.pa_decode_window.restype = I
+        L.pa_reshape_and_cache_int8.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, I, P, P]
+        L.pa_reshape_and_cache_int8.restype = I
+        L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, P, S, P, P]
+        L.pa_decode_int8.restype = I
         L.pa_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
         L.pa_copy_blocks.restype = I
         L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
@@ -302,6 +306,70 @@ def pa_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, win
                                 _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode_window")
+
+
+def _check_int8_pool(k_cache, v_cache, k_scales, v_scales):
+    import torch
+    _check_cuda("k_cache", k_cache, torch.int8, 4)
+    _check_cuda("v_cache", v_cache, torch.int8, 4)
+    _check_cuda("k_scales", k_scales, torch.float32, 3)
+    _check_cuda("v_scales", v_scales, torch.float32, 3)
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or \
+            tuple(k_scales.shape) != tuple(k_cache.shape[:3]) or \
+            tuple(v_scales.shape) != tuple(k_cache.shape[:3]):
+        raise ValueError("INT8 pools are [NB][Hkv][bs][D] codes with [NB][Hkv][bs] scales")
+
+
+def pa_reshape_and_cache_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales, v_scales,
+                              error_word=None, stream=None) -> None:
+    """Quantising append into an INT8 cache: one fp32 scale per (row, KV head)."""
+    import torch
+    _check_int8_pool(k_cache, v_cache, k_scales, v_scales)
+    _check_cuda("k_new", k_new, ndim=3)
+    _check_cuda("v_new", v_new, k_new.dtype, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape \
+            or slot_mapping.shape[0] != k_new.shape[0]:
+        raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    rc = lib().pa_reshape_and_cache_int8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                         _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(k_scales), _ptr(v_scales), int(k_new.shape[0]), hkv,
+                                         d, bs, nb, _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_reshape_and_cache_int8")
+
+
+def pa_decode_int8(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, scale,
+                   out, max_context_len, workspace=None, error_word=None, stream=None) -> None:
+    """Decode attention over an INT8 cache with per-row scales, bf16 q/out."""
+    import torch
+    _check_int8_pool(k_cache, v_cache, k_scales, v_scales)
+    _check_cuda("q", q, torch.bfloat16, 3)
+    _check_cuda("out", out, torch.bfloat16, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or block_tables.shape[0] != B \
+            or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_decode_int8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales),
+                              _ptr(v_scales), _ptr(block_tables), _ptr(context_lens),
+                              float(scale), _ptr(out), B, hq, hkv, d, bs, nb,
+                              int(block_tables.shape[1]), int(max_context_len), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(error_word),
+                              _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_decode_int8")
 
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None) -> None:

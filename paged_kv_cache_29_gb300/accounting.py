@@ -53,16 +53,18 @@ class StepBytes:
 def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
                elem_bytes: int, block_size: int = 16, block_tables=None,
                act_bytes: int | None = None, num_queries: int = 1,
-               window: int = 0) -> StepBytes:
+               window: int = 0, row_scale_bytes: int = 0) -> StepBytes:
     """elem_bytes: bytes per cache element; act_bytes: bytes per element of q,
     out and the new K/V rows (default: elem_bytes); num_queries: new tokens
     (queries) per sequence; window: a sliding window of rows attended (0 =
-    all): K/V and table bytes count the attended rows only."""
+    all): K/V and table bytes count the attended rows only; row_scale_bytes:
+    bytes of scale stored per (row, KV head) of K and of V (4 for an INT8
+    cache), read and written with the rows."""
     act = elem_bytes if act_bytes is None else act_bytes
     lens = np.asarray(context_lens, dtype=np.int64)
     B = int(lens.shape[0])
     first = np.maximum(lens - window, 0) if window > 0 else np.zeros_like(lens)
-    row = num_kv_heads * head_dim * elem_bytes          # one token, all KV heads, K or V
+    row = num_kv_heads * (head_dim * elem_bytes + row_scale_bytes)   # one token, K or V
     kv = int((lens - first).sum()) * row * 2
     Q = int(num_queries)
     q_out = B * Q * num_heads * head_dim * act * 2
@@ -71,7 +73,8 @@ def step_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
     tables = used_entries * 4 + B * 4
     active = int((lens > 0).sum())
     # new K and V rows read (act dtype) and written (cache dtype), slots read
-    append = active * Q * num_kv_heads * head_dim * 2 * (act + elem_bytes) + B * Q * 8
+    append = (active * Q * num_kv_heads * 2 * (head_dim * (act + elem_bytes) + row_scale_bytes)
+              + B * Q * 8)
     if block_tables is None:
         kv_unique = kv
     else:
@@ -87,7 +90,8 @@ def step_bytes_for(step) -> StepBytes:
     """StepBytes of a workloads.DecodeStep."""
     return step_bytes(step.context_lens, step.num_heads, step.num_kv_heads, step.head_dim,
                       step.elem_bytes, step.block_size, step.block_tables, step.act_bytes,
-                      step.num_queries, step.window)
+                      step.num_queries, step.window,
+                      4 if step.k_row_scales is not None else 0)
 
 
 def decode_flops(context_lens, num_heads: int, head_dim: int) -> int:

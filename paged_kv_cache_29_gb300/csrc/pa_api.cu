@@ -40,8 +40,10 @@ int elem_bytes(pa_dtype d) { return d == PA_DTYPE_F32 ? 4 : d == PA_DTYPE_BF16 ?
 // Types of q, out and new rows.
 bool valid_dtype(pa_dtype d) { return d == PA_DTYPE_F32 || d == PA_DTYPE_BF16; }
 
-// Types a cache may hold.
+// Types a cache may hold (an INT8 cache also carries per-row scales, so the
+// plain row copies leave it out).
 bool valid_cache_dtype(pa_dtype d) { return valid_dtype(d) || d == PA_DTYPE_FP8_E4M3; }
+bool valid_decode_cache_dtype(pa_dtype d) { return valid_cache_dtype(d) || d == PA_DTYPE_INT8; }
 
 // The pool viewed as a 3D tensor for TMA: x = element within a 128-byte
 // column half of a row, y = row (rows = blocks * kv_heads * block_size, stride
@@ -116,14 +118,16 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
                       pa_dtype act_dtype, void* workspace, size_t workspace_bytes,
                       int32_t* error_word, const pa_decode_options* options,
-                      struct CUstream_st* stream, int num_queries = 1, int window = 0) {
+                      struct CUstream_st* stream, int num_queries = 1, int window = 0,
+                      const float* k_row_scales = nullptr, const float* v_row_scales = nullptr) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
                                                                : pa::kDefaultPartition;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
-        !valid_cache_dtype(dtype) || !valid_dtype(act_dtype) || num_heads % num_kv_heads != 0 ||
-        num_queries < 1 || window < 0 || (window > 0 && num_queries > 1))
+        !valid_decode_cache_dtype(dtype) || !valid_dtype(act_dtype) ||
+        num_heads % num_kv_heads != 0 || num_queries < 1 || window < 0 ||
+        (window > 0 && num_queries > 1))
         return PA_ERR_INVALID_ARG;
     if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
     if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
@@ -155,7 +159,15 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                            (head_dim * elem_bytes(dtype)) % 128 == 0;
     pa_kernel kernel = static_cast<pa_kernel>(kernel_req);
     const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
-    if (num_queries > 1) {
+    const bool int8 = dtype == PA_DTYPE_INT8;
+    if (int8) {
+        // One kernel family: the INT8 tensor-core tile ring.
+        if (!tma_shape || !pa::has_fp8_instance(head_dim, group) || num_queries > 1 ||
+            window > 0 || !k_row_scales || !v_row_scales || !aligned16(k_row_scales) ||
+            !aligned16(v_row_scales) || (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA))
+            return (!k_row_scales || !v_row_scales) ? PA_ERR_INVALID_ARG : PA_ERR_UNSUPPORTED;
+        kernel = PA_KERNEL_MMA;
+    } else if (num_queries > 1) {
         // Several query tokens per sequence: the bf16 tensor-core tile ring.
         if (fp8 || !tma_shape ||
             !pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group, num_queries) ||
@@ -197,6 +209,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     base.v_scale = v_scale;
     base.num_queries = num_queries;
     base.window = window;
+    base.k_row_scales = k_row_scales;
+    base.v_row_scales = v_row_scales;
     base.num_heads = num_heads;
     base.num_kv_heads = num_kv_heads;
     base.head_dim = head_dim;
@@ -242,6 +256,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
             err = pa::launch_decode_generic(p, dtype, st);
         } else {
             err = fp8                      ? pa::launch_decode_fp8(tk, tv, p, sm_count, st)
+                  : int8                    ? pa::launch_decode_int8(tk, tv, p, sm_count, st)
                   : kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
                                             : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
         }
@@ -386,6 +401,45 @@ pa_status pa_decode_window(const void* q, const void* k_cache, const void* v_cac
                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
                        workspace_bytes, error_word, nullptr, stream, 1, window);
+}
+
+pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scales, const float* v_scales,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_seq,
+                         int max_context_len, void* workspace, size_t workspace_bytes,
+                         int32_t* error_word, struct CUstream_st* stream) {
+    if (num_seqs > 0 && (!k_scales || !v_scales)) return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_DTYPE_INT8, PA_DTYPE_BF16,
+                       workspace, workspace_bytes, error_word, nullptr, stream, 1, 0, k_scales,
+                       v_scales);
+}
+
+pa_status pa_reshape_and_cache_int8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                                    const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                    float* k_scales, float* v_scales, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, int32_t* error_word,
+                                    struct CUstream_st* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0 || !valid_dtype(new_dtype))
+        return PA_ERR_INVALID_ARG;
+    if (head_dim % 16 != 0 || head_dim > pa::kMaxHeadDim) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scales || !v_scales)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(k_scales) || !aligned16(v_scales) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t err = pa::launch_append_int8(
+        k_new, v_new, new_dtype, slot_mapping, k_cache, v_cache, k_scales, v_scales, num_tokens,
+        num_kv_heads, head_dim, block_size, num_blocks, error_word,
+        reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 size_t pa_decode_workspace_size_multi(int num_seqs, int num_queries, int num_heads,

@@ -98,7 +98,88 @@ append_fp8_kernel(const TIn* __restrict__ k_new, const TIn* __restrict__ v_new,
     }
 }
 
+// Quantising append into an INT8 cache with one scale per (row, KV head):
+// scale = max|x| / 127 and code = x / scale rounded to the nearest integer,
+// ties to even (both divisions in fp32, IEEE), clamped to [-127, 127]; an
+// all-zero row gets scale 0 and codes 0. One warp per (token, KV head, K or
+// V) row: the lanes hold the row, a butterfly max gives the scale.
+constexpr int kInt8MaxPerLane = kMaxHeadDim / 32;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kAppendThreads)
+append_int8_kernel(const TIn* __restrict__ k_new, const TIn* __restrict__ v_new,
+                   const int64_t* __restrict__ slot_mapping, int8_t* __restrict__ k_cache,
+                   int8_t* __restrict__ v_cache, float* __restrict__ k_scales,
+                   float* __restrict__ v_scales, long long rows, int head_dim,
+                   int num_kv_heads, int block_size, long long num_slots, int32_t* error_word) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         w < 2 * rows; w += warps) {
+        const bool is_v = w >= rows;
+        const long long rowi = is_v ? w - rows : w;          // (token, kv head)
+        const long long t = rowi / num_kv_heads;
+        const int h = static_cast<int>(rowi - t * num_kv_heads);
+        const long long slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (lane == 0 && h == 0 && !is_v) raise_error(error_word, PA_DEVERR_SLOT);
+            continue;
+        }
+        const TIn* src = (is_v ? v_new : k_new) + rowi * head_dim;
+        float x[kInt8MaxPerLane];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kInt8MaxPerLane; ++i) {
+            const int d = lane + 32 * i;
+            x[i] = d < head_dim ? ElemTraits<TIn>::load(src + d) : 0.f;
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = __fdiv_rn(amax, 127.0f);
+        const long long blk = slot / block_size;
+        const long long r = (blk * num_kv_heads + h) * block_size + (slot - blk * block_size);
+        int8_t* dst = (is_v ? v_cache : k_cache) + r * head_dim;
+#pragma unroll
+        for (int i = 0; i < kInt8MaxPerLane; ++i) {
+            const int d = lane + 32 * i;
+            if (d < head_dim) {
+                int c = 0;
+                if (scale != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], scale))));
+                dst[d] = static_cast<int8_t>(c);
+            }
+        }
+        if (lane == 0) (is_v ? v_scales : k_scales)[r] = scale;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_append_int8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               float* k_scales, float* v_scales, int num_tokens,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int32_t* error_word, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(num_tokens) * num_kv_heads;
+    if (rows == 0) return cudaSuccess;
+    long long blocks = (2 * rows * 32 + kAppendThreads - 1) / kAppendThreads;
+    if (blocks > 8192) blocks = 8192;
+    const long long num_slots = static_cast<long long>(num_blocks) * block_size;
+    if (new_dtype == PA_DTYPE_BF16) {
+        append_int8_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+            slot_mapping, static_cast<int8_t*>(k_cache), static_cast<int8_t*>(v_cache), k_scales,
+            v_scales, rows, head_dim, num_kv_heads, block_size, num_slots, error_word);
+    } else {
+        append_int8_kernel<float><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(
+            static_cast<const float*>(k_new), static_cast<const float*>(v_new), slot_mapping,
+            static_cast<int8_t*>(k_cache), static_cast<int8_t*>(v_cache), k_scales, v_scales,
+            rows, head_dim, num_kv_heads, block_size, num_slots, error_word);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,
                               const int64_t* slot_mapping, void* k_cache, void* v_cache,

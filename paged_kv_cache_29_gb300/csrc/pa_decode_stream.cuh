@@ -67,7 +67,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes>
+template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes, int XBYTES = 0>
 struct StreamSmem {
     static constexpr int kRing = STAGES * Geom::kStageBytes;
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
@@ -76,7 +76,9 @@ struct StreamSmem {
     static constexpr int kFlags = (STAGES + 2 * W + 8) * 4;
     static constexpr int kIds = 2 * kMaxItemBlocks * 4;
     static constexpr size_t kQBuf = 2 * Math_kQBufBytes;
-    static constexpr size_t kBytes = 1024 + kRing + kMerge + kBarriers + kFlags + kIds + kQBuf;
+    static constexpr size_t kExtra = static_cast<size_t>(STAGES) * XBYTES;   // per-stage side data
+    static constexpr size_t kBytes =
+        1024 + kRing + kMerge + kBarriers + kFlags + kIds + kQBuf + kExtra;
 };
 
 // MIN_CTAS: resident CTAs per SM the register budget is sized for (see
@@ -88,7 +90,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
-    using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes>;
+    using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes, Math::kExtraStageBytes>;
+    static_assert(Math::kExtraStageBytes % 16 == 0, "side data moves in 16-byte units");
     static_assert(Smem::kMerge >= 4 * plan_scratch_ints((W + 1) * 32),
                   "the plan's scratch lives in the merge area");
 
@@ -104,6 +107,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
         reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
     uint8_t* qbuf = reinterpret_cast<uint8_t*>(ids_buf + 2 * kMaxItemBlocks);   // [2][kQBufBytes]
+    // [STAGES][kExtraStageBytes]: per-row scales of a stage's K and V tiles
+    const uint32_t xring = smem_addr(qbuf + Smem::kQBuf);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -194,7 +199,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     } else {
                         stage_bad[stage] = cur_bad;
                         if (data)
-                            mbar_arrive_expect_tx(fb, Geom::kStageBytes);
+                            mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
                         else
                             mbar_arrive(fb);          // no data: consumers skip the slot
                         issued = t + 1;
@@ -213,6 +218,23 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     tma_load_3d(dst, lane ? static_cast<const void*>(&tmap_v)
                                           : static_cast<const void*>(&tmap_k),
                                 fb, 0, row, 0);
+                }
+                if constexpr (Math::kExtraStageBytes > 0) {
+                    // Lanes 2 and 3: the tile's 16 K and 16 V row scales (64 bytes
+                    // each, 64-byte aligned: the tile's first row is a multiple of
+                    // 16 within its block).
+                    if (data && (lane == 2 || lane == 3)) {
+                        const int id = ids[tok / bs - b0];
+                        const size_t r = (static_cast<size_t>(id) * p.num_kv_heads + cur.y) * bs + (tok % bs);
+                        const float* src = (lane == 2 ? p.k_row_scales : p.v_row_scales) + r;
+                        const uint32_t dst = xring + stage * Math::kExtraStageBytes +
+                                             (lane - 2) * (Math::kExtraStageBytes / 2);
+                        asm volatile(
+                            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
+                            " [%0], [%1], %2, [%3];" ::"r"(dst), "l"(src),
+                            "r"(Math::kExtraStageBytes / 2), "r"(fb)
+                            : "memory");
+                    }
                 }
             }
             cur = nxt;
@@ -300,7 +322,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     // Rows of the tile before a sliding window (<= 0: none).
                     const int skip = p.window > 0 ? n - p.window - row0 : 0;
                     math.tile(kb, kb + Geom::kTileBytes, valid, p.scale_log2, lane, row0, limit0,
-                              grp, skip);
+                              grp, skip, xring + stage * Math::kExtraStageBytes);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
@@ -367,7 +389,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
 cudaError_t launch_stream_instance(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecodeParams& p, int sm_count, cudaStream_t stream) {
-    using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D, Math::kQBufBytes>;
+    using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D, Math::kQBufBytes,
+                            Math::kExtraStageBytes>;
     auto kernel = decode_stream_kernel<Math, D, G, W, STAGES, MIN_CTAS>;
     const int smem = static_cast<int>(Smem::kBytes);
     // The shared-memory attribute and the resulting CTAs per SM are set up

@@ -26,6 +26,8 @@ struct DecodeParams {
     float scale_log2;              // scale * log2(e): scores are kept in base 2
     float k_scale;                 // FP8 caches: K value = k_scale * e4m3(code) (else 1)
     float v_scale;                 // FP8 caches: V value = v_scale * e4m3(code) (else 1)
+    const float* k_row_scales;     // INT8 caches: [num_blocks][num_kv_heads][block_size] (else null)
+    const float* v_row_scales;
     int num_seqs;
     int num_queries;               // query tokens per sequence, the last rows of each (>= 1)
     int window;                    // sliding window: attend to the last `window` rows (0 = all)
@@ -66,6 +68,18 @@ bool has_tma_instance(pa_kernel kernel, pa_dtype dtype, int head_dim, int group,
 cudaError_t launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, int sm_count, cudaStream_t stream);
 bool has_fp8_instance(int head_dim, int group);
+
+// INT8 cache with per-row scales, bf16 q/out (head dim 128; 1, 2, 4 or 8
+// query heads per KV head).
+cudaError_t launch_decode_int8(const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, int sm_count, cudaStream_t stream);
+
+// Quantising append into an INT8 cache: one scale per (row, KV head).
+cudaError_t launch_append_int8(const void* k_new, const void* v_new, pa_dtype new_dtype,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               float* k_scales, float* v_scales, int num_tokens,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int32_t* error_word, cudaStream_t stream);
 
 // Quantising append into an FP8 cache (new rows fp32 or bf16).
 cudaError_t launch_append_fp8(const void* k_new, const void* v_new, pa_dtype new_dtype,

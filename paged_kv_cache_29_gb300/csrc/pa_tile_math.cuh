@@ -126,6 +126,7 @@ template <int D, int G, bool CAUSAL = false>
 struct MmaMath {
     using T = __nv_bfloat16;
     static constexpr bool kCausal = CAUSAL;
+    static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<T, D>;
     static constexpr int kSteps = D / 16;
     // G: query columns the state holds (a capacity: an item uses ncols <= G).
@@ -181,7 +182,7 @@ struct MmaMath {
     // holds a visible row for one query per sequence.
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float scale_log2, int lane, int row0, int limit0,
-                                         int grp, int skip) {
+                                         int grp, int skip, uint32_t /*xb: none*/) {
         const int mi = lane >> 3;
         const int lr = lane & 7;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -329,6 +330,7 @@ template <typename TT, int D, int G>
 struct SimtMath {
     using T = TT;
     static constexpr bool kCausal = false;
+    static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<T, D>;
     using E = ElemTraits<T>;
     static constexpr int kEpc = E::kPerChunk;               // elements per 16-byte chunk
@@ -402,7 +404,8 @@ struct SimtMath {
     // rows (a sliding window starting inside this tile).
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float /*scale_log2*/, int /*lane*/, int /*row0*/,
-                                         int /*limit0*/, int /*grp*/, int skip) {
+                                         int /*limit0*/, int /*grp*/, int skip,
+                                         uint32_t /*xb: none*/) {
         const uint32_t kbox = kbase + (ch >> 3) * kBoxBytes;
         const uint32_t vbox = vbase + (ch >> 3) * kBoxBytes;
         const int cc = ch & 7;

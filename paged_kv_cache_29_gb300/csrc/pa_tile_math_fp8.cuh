@@ -65,6 +65,7 @@ template <int D, int G>
 struct Fp8MmaMath {
     using T = __nv_bfloat16;                    // q and out
     static constexpr bool kCausal = false;
+    static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<uint8_t, D>;
     static_assert(D == 128, "one 128-byte row of codes per token");
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
@@ -207,7 +208,8 @@ struct Fp8MmaMath {
     // sliding window) are masked; a tile always holds a visible row.
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float /*scale_log2: folded into q'*/, int /*lane*/,
-                                         int /*row0*/, int /*limit0*/, int /*grp*/, int skip) {
+                                         int /*row0*/, int /*limit0*/, int /*grp*/, int skip,
+                                         uint32_t /*xb: none*/) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         qk(kbase, valid, skip, c);
         float mx0 = fmaxf(c[0], c[2]);

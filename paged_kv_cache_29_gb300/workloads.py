@@ -27,11 +27,16 @@ workloads:
                  together (multi-query decode: each query attends causally)
   8b_gqa_win1024 the 8b_gqa batch under a 1,024-row sliding window (a local
                  attention layer)
+  8b_gqa_int8    the 8b_gqa batch over an INT8 cache with one fp32 scale per
+                 (row, KV head); q and the new K/V rows stay bf16 and the
+                 append quantises them
 
 Every value of q, of the new K/V rows and of the whole pool (used or not) is
 drawn N(0, 1) in fp32 and stored in the cache dtype (bf16 by round to nearest
 even). An FP8 pool holds e4m3 codes of N(0, 1) draws, made by PyTorch's
-float8_e4m3fn conversion; q and the new rows of an FP8 step are bf16. The pool holds 1.25x the blocks the batch needs (the tiny workload: 32)
+float8_e4m3fn conversion; q and the new rows of an FP8 step are bf16. An
+INT8 pool holds codes drawn uniformly from [-127, 127] with per-row scales
+drawn uniformly from [0.01, 0.03] (values of about unit size). The pool holds 1.25x the blocks the batch needs (the tiny workload: 32)
 and hands them out in a seeded random order, so a sequence's blocks are
 scattered. Lengths count the token appended by this step: the cache holds
 n - 1 rows before the step and n after it. Unused block-table entries hold -1.
@@ -50,7 +55,7 @@ from .block_manager import BlockManager
 # Seeds of the five named workloads, in the order listed above.
 WORKLOAD_SEEDS = {"tiny": 0, "7b_mha": 1, "8b_gqa": 2, "long_skew": 3, "prefix_shared": 4,
                   "8b_gqa_fp8": 2, "8b_gqa_mq2": 2,
-                  "8b_gqa_win1024": 2}                # variants of the 8b_gqa batch
+                  "8b_gqa_win1024": 2, "8b_gqa_int8": 2}   # variants of the 8b_gqa batch
 PAD_BLOCK = -1
 
 
@@ -93,11 +98,25 @@ def as_f32(x: np.ndarray, cache_dtype: str) -> np.ndarray:
     return np.asarray(x, dtype=np.float32)
 
 
-_STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8}
-_BYTES = {"f32": 4, "bf16": 2, "fp8": 1}
+_STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8": np.uint8, "int8": np.int8}
+_BYTES = {"f32": 4, "bf16": 2, "fp8": 1, "int8": 1}
 
 
 _CHUNK = 1 << 22
+
+
+def _int8_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Codes uniform in [-127, 127], drawn in the same fixed chunks as
+    _normal."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.int8)
+    root = np.random.SeedSequence(int(rng.integers(0, 2**63 - 1)))
+    chunks = list(range(0, n, _CHUNK))
+    for i, seed in enumerate(root.spawn(len(chunks))):
+        lo = chunks[i]
+        hi = min(n, lo + _CHUNK)
+        out[lo:hi] = np.random.default_rng(seed).integers(-127, 128, hi - lo, dtype=np.int8)
+    return out.reshape(shape)
 
 
 def _normal(rng: np.random.Generator, shape, cache_dtype: str) -> np.ndarray:
@@ -134,7 +153,7 @@ class DecodeStep:
     append (k_new/v_new into slot_mapping) and then attending over
     context_lens tokens per sequence is the step."""
     name: str
-    cache_dtype: str                  # "f32", "bf16" or "fp8" (e4m3 codes)
+    cache_dtype: str                  # "f32", "bf16", "fp8" (e4m3 codes) or "int8" (codes)
     num_heads: int
     num_kv_heads: int
     head_dim: int
@@ -153,6 +172,8 @@ class DecodeStep:
     act_dtype: str = ""               # dtype of q, out, k_new, v_new ("" = cache_dtype)
     num_queries: int = 1              # new tokens per sequence, the last rows of each
     window: int = 0                   # sliding window: attend to the last `window` rows
+    k_row_scales: np.ndarray | None = None   # INT8 caches: fp32 [NB][Hkv][bs], value = scale * code
+    v_row_scales: np.ndarray | None = None
     k_scale: float = 1.0              # FP8 caches: value = scale * e4m3(code)
     v_scale: float = 1.0
 
@@ -233,12 +254,22 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
     for s, t in enumerate(tables):
         bt[s, :len(t)] = t
     pool_shape = (num_blocks, num_kv_heads, block_size, head_dim)
-    k_cache = _normal(rng, pool_shape, cache_dtype)
-    v_cache = _normal(rng, pool_shape, cache_dtype)
+    k_rs = v_rs = None
+    if cache_dtype == "int8":
+        k_cache = _int8_codes(rng, pool_shape)
+        v_cache = _int8_codes(rng, pool_shape)
+        k_rs = rng.uniform(0.01, 0.03, pool_shape[:3]).astype(np.float32)
+        v_rs = rng.uniform(0.01, 0.03, pool_shape[:3]).astype(np.float32)
+    else:
+        k_cache = _normal(rng, pool_shape, cache_dtype)
+        v_cache = _normal(rng, pool_shape, cache_dtype)
     for src, dst in cow_pairs:           # copy-on-write copies made while building
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
-    act = "bf16" if cache_dtype == "fp8" else cache_dtype
+        if k_rs is not None:
+            k_rs[dst] = k_rs[src]
+            v_rs[dst] = v_rs[src]
+    act = "bf16" if cache_dtype in ("fp8", "int8") else cache_dtype
     Q = num_queries
     q = _normal(rng, (B, num_heads, head_dim) if Q == 1 else (B, Q, num_heads, head_dim), act)
     k_new = _normal(rng, (B * Q, num_kv_heads, head_dim), act)
@@ -251,7 +282,8 @@ def _materialise(name, cache_dtype, num_heads, num_kv_heads, head_dim, block_siz
                       k_cache=k_cache, v_cache=v_cache, block_tables=bt,
                       context_lens=np.asarray(lens, dtype=np.int32),
                       scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale),
-                      seed=seed, meta=meta, act_dtype=act, num_queries=Q)
+                      seed=seed, meta=meta, act_dtype=act, num_queries=Q,
+                      k_row_scales=k_rs, v_row_scales=v_rs)
 
 
 # ---- the five named workloads ------------------------------------------------
@@ -306,6 +338,13 @@ def gqa_8b_win1024(seed: int = WORKLOAD_SEEDS["8b_gqa_win1024"], batch: int = 12
     return step
 
 
+def gqa_8b_int8(seed: int = WORKLOAD_SEEDS["8b_gqa_int8"], batch: int = 128) -> DecodeStep:
+    rng = np.random.default_rng(seed)
+    lens = gqa_8b_lengths(rng, batch)
+    return build_step("8b_gqa_int8", lens, num_heads=32, num_kv_heads=8, head_dim=128,
+                      cache_dtype="int8", seed=seed, rng=rng)
+
+
 def long_skew(seed: int = WORKLOAD_SEEDS["long_skew"]) -> DecodeStep:
     return build_step("long_skew", [100_000] + [1_500] * 7, num_heads=32, num_kv_heads=8,
                       head_dim=128, seed=seed)
@@ -357,6 +396,7 @@ WORKLOADS = {
     "8b_gqa_fp8": gqa_8b_fp8,
     "8b_gqa_mq2": gqa_8b_mq2,
     "8b_gqa_win1024": gqa_8b_win1024,
+    "8b_gqa_int8": gqa_8b_int8,
 }
 
 
