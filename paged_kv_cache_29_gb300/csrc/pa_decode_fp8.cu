@@ -2,7 +2,7 @@
 // (e4m3) cache with bf16 q and output (head dim 128; 1, 2, 4 or 8 query heads
 // per KV head).
 #include "pa_decode_stream.cuh"
-#include "pa_tile_math_fp8.cuh"
+#include "pa_tile_math_quant.cuh"
 
 namespace pa {
 

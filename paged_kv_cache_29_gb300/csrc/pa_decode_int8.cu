@@ -2,7 +2,7 @@
 // cache with per-row scales and bf16 q and output (head dim 128; 1, 2, 4 or 8
 // query heads per KV head).
 #include "pa_decode_stream.cuh"
-#include "pa_tile_math_int8.cuh"
+#include "pa_tile_math_quant.cuh"
 
 namespace pa {
 

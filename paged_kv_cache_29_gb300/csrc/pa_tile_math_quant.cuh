@@ -1,18 +1,31 @@
-// pa_tile_math_fp8.cuh -- per-tile math for an FP8 (e4m3) KV cache with bf16 q
-// and output.
+// pa_tile_math_quant.cuh -- per-tile math for quantised KV caches (8-bit codes)
+// with bf16 q and output: FP8 (e4m3) with one scale per tensor, and INT8 with
+// one scale per (row, KV head).
 //
-// Each cached element is an e4m3 code with one scale per tensor: value =
-// k_scale * e4m3(code) for K, v_scale * e4m3(code) for V (an FP8 cache halves
-// the bytes per token; scales are per tensor: "Forward Deployed Engineering
-// Interview", Chapter 2 "Batching and the KV Cache"). The codes are widened to
-// f16 in registers (cvt.rn.f16x2.e4m3x2, exact: every e4m3 value is an f16
-// value) and multiplied with m16n8k16 f16 MMAs accumulating in fp32; the
-// online softmax is that of MmaMath. The scales never touch the tile:
-//   scores  S = (q * scale * log2(e) * k_scale) . code(K): q is scaled and
-//           rounded to f16 once per item, so the accumulators are base-2
-//           scores;
-//   output  O = v_scale * sum_i p_i code(V_i): v_scale is applied when the
-//           warp state is written.
+//   FP8   value = k_scale * e4m3(code) (V: v_scale); an FP8 cache halves the
+//         bytes per token, scales per tensor ("Forward Deployed Engineering
+//         Interview", Chapter 2 "Batching and the KV Cache").
+//   INT8  value = scale_row * code with scale_row = max|row| / 127
+//         ("MLSys Engineer -- Inference Systems Q&A", Q3: INT8 KV with
+//         per-token scaling, dequantised before the softmax).
+//
+// The codes are widened to f16 in registers (exact for both formats: every
+// e4m3 value and every int8 is an f16 value) and multiplied with m16n8k16 f16
+// MMAs accumulating in fp32; the online softmax is that of MmaMath. The
+// scales never touch the products:
+//   FP8   S = (q * scale * log2(e) * k_scale) . code(K): q is scaled and
+//         rounded to f16 once per item, so the accumulators are base-2
+//         scores; O = v_scale * sum_i p_i code(V_i), v_scale applied when the
+//         warp state is written.
+//   INT8  S_row = k_scale_row * (q * scale * log2(e)) . code(K_row): each
+//         accumulator row is multiplied by its K scale; O = sum_row (p_row *
+//         v_scale_row) code(V_row): the V scale folds into the probability
+//         before it becomes an MMA operand, while the softmax sum keeps p_row.
+//         The 16 K and 16 V scales of a tile arrive with it, in a small
+//         per-stage array (extra stage bytes).
+//
+// Widening: e4m3 with cvt.rn.f16x2.e4m3x2; int8 code c as the f16 bit pattern
+// 0x6400 | (c ^ 0x80), the value 1024 + 128 + c, minus 1152.
 //
 // Fragment assignment (lane = 4 * gid + t4; the dot products and the output
 // rows are sums and rows, so any fixed assignment of dims works when A, B and
@@ -35,17 +48,6 @@
 
 namespace pa {
 
-// Two e4m3 codes in each 16-bit half of w -> two f16x2 registers (the low
-// byte of each pair becomes the low half).
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 l, h;\n\t"
-        "mov.b32 {l, h}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -61,15 +63,50 @@ __device__ __forceinline__ void mma_16816_f16(float* c, uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int D, int G>
-struct Fp8MmaMath {
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// e4m3 codes with one scale per tensor.
+struct E4m3Codes {
+    static constexpr bool kRowScales = false;
+    // Four codes -> two f16x2 registers (the low byte of each pair becomes
+    // the low half).
+    __device__ static __forceinline__ void widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
+        asm("{\n\t.reg .b16 l, h;\n\t"
+            "mov.b32 {l, h}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    }
+};
+
+// int8 codes with one scale per (row, KV head).
+struct S8Codes {
+    static constexpr bool kRowScales = true;
+    __device__ static __forceinline__ void widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
+        const uint32_t t = w ^ 0x80808080u;
+        const uint32_t a = prmt(t, 0x64646464u, 0x4140u);   // (t.b0, 0x64, t.b1, 0x64)
+        const uint32_t b = prmt(t, 0x64646464u, 0x4342u);   // (t.b2, 0x64, t.b3, 0x64)
+        const uint32_t bias = 0x64806480u;                  // f16x2 {1152, 1152}
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+    }
+};
+
+template <int D, int G, class Codes>
+struct QuantMmaMath {
     using T = __nv_bfloat16;                    // q and out
-    static constexpr bool kCausal = false;
-    static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<uint8_t, D>;
+    static constexpr bool kCausal = false;
     static_assert(D == 128, "one 128-byte row of codes per token");
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
     static constexpr int kSteps = D / 16;
+    // Row scales: 16 K then 16 V scales (fp32) beside each stage.
+    static constexpr int kExtraStageBytes = Codes::kRowScales ? 2 * kTileRows * 4 : 0;
 
     static constexpr bool kQInSmem = true;
     static constexpr int kQRowBytes = D * 2 + 16;
@@ -85,8 +122,8 @@ struct Fp8MmaMath {
     __device__ __forceinline__ void setup(int lane, const DecodeParams& p) {
         gid = lane >> 2;
         t4 = lane & 3;
-        qscale = p.scale_log2 * p.k_scale;
-        vscale = p.v_scale;
+        qscale = Codes::kRowScales ? p.scale_log2 : p.scale_log2 * p.k_scale;
+        vscale = Codes::kRowScales ? 1.f : p.v_scale;
     }
 
     __device__ __forceinline__ void stage_q(const DecodeParams& p, int s, int h, int ncols,
@@ -94,9 +131,9 @@ struct Fp8MmaMath {
         stage_q_rows<D, kQRowBytes>(p, s, h, ncols, grp, qbuf, lane);
     }
 
-    // q' = q * scale * log2(e) * k_scale in f16, dealt as the k-steps deal
-    // the dims; the softmax state is cleared. Lanes of heads gid >= G read
-    // nothing (the buffer holds G rows) and hold zeros.
+    // q' = q * qscale in f16, dealt as the k-steps deal the dims; the softmax
+    // state is cleared. Lanes of heads gid >= G read nothing (the buffer holds
+    // G rows) and hold zeros.
     __device__ __forceinline__ void begin_staged(const uint8_t* qbuf, int /*ncols: G*/) {
         const uint8_t* row = qbuf + gid * kQRowBytes;
 #pragma unroll
@@ -116,9 +153,8 @@ struct Fp8MmaMath {
         l[0] = l[1] = 0.f;
     }
 
-    // S^T of one 16-row tile: c = S^T[token gid, gid + 8][heads 2 t4, 2 t4 + 1].
-    // Rows past `valid` or before `skip` (a sliding window) are masked.
-    __device__ __forceinline__ void qk(uint32_t kbase, int valid, int skip, float* c) const {
+    // c += code(K tile) . q'^T: c = S^T[token gid, gid + 8][heads 2 t4, 2 t4 + 1].
+    __device__ __forceinline__ void qk(uint32_t kbase, float* c) const {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const uint4 r0 = lds128(swizzled(kbase, gid, 2 * t4 + half));
@@ -129,23 +165,15 @@ struct Fp8MmaMath {
             for (int jj = 0; jj < 4; ++jj) {
                 const int j = 4 * half + jj;
                 uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(w0[jj], a0, a2);
-                e4m3x4_to_f16x2x2(w1[jj], a1, a3);
+                Codes::widen(w0[jj], a0, a2);
+                Codes::widen(w1[jj], a1, a3);
                 mma_16816_f16(c, a0, a1, a2, a3, qb[j][0], qb[j][1]);
             }
         }
-        if (valid < kTileRows) {
-            if (gid >= valid) c[0] = c[1] = -INFINITY;
-            if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
-        }
-        if (skip > 0) {
-            if (gid < skip) c[0] = c[1] = -INFINITY;
-            if (gid + 8 < skip) c[2] = c[3] = -INFINITY;
-        }
     }
 
-    // P^T B fragments of one tile from its probabilities (as in MmaMath):
-    // lane (gid, t4) gets P[tokens 2t4, 2t4+1][head gid] and P[tokens 2t4+8,
+    // P^T B fragments from this lane's probabilities (as in MmaMath): lane
+    // (gid, t4) gets P[tokens 2t4, 2t4+1][head gid] and P[tokens 2t4+8,
     // 2t4+9][head gid].
     __device__ __forceinline__ void p_fragments(float p0, float p1, float p2, float p3,
                                                 uint32_t& b0, uint32_t& b1) const {
@@ -161,10 +189,10 @@ struct Fp8MmaMath {
         b1 = prmt(u0, u1, sel);
     }
 
-    // O^T += V^T . P^T over one 16-row tile: V rows 2t4, 2t4+1, 2t4+8, 2t4+9,
-    // chunk gid (dims 16 gid .. 16 gid + 15). Rows past the sequence hold
-    // whatever the pool holds (possibly NaN codes): their V values are zeroed
-    // so that 0 * V stays 0.
+    // O^T += code(V)^T . P^T over one 16-row tile: V rows 2t4, 2t4+1, 2t4+8,
+    // 2t4+9, chunk gid. MASK zeroes the V values of rows past `valid`, whose
+    // codes may be NaN (e4m3) so that 0 * V stays 0; int8 codes are finite.
+    template <bool MASK>
     __device__ __forceinline__ void pv(uint32_t vbase, int valid, uint32_t b0, uint32_t b1) {
         const uint4 x0 = lds128(swizzled(vbase, 2 * t4, gid));
         const uint4 x1 = lds128(swizzled(vbase, 2 * t4 + 1, gid));
@@ -174,44 +202,65 @@ struct Fp8MmaMath {
         const uint32_t e1[4] = {x1.x, x1.y, x1.z, x1.w};
         const uint32_t e2[4] = {x2.x, x2.y, x2.z, x2.w};
         const uint32_t e3[4] = {x3.x, x3.y, x3.z, x3.w};
-        if (valid == kTileRows) {
-#pragma unroll
-            for (int mt = 0; mt < kSteps; ++mt) {
-                // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
-                const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
-                const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
-                uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(lo, a0, a1);
-                e4m3x4_to_f16x2x2(hi, a2, a3);
-                mma_16816_f16(o[mt], a0, a1, a2, a3, b0, b1);
-            }
-        } else {
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if constexpr (MASK) {
             const int tk = 2 * t4;
-            const uint32_t mlo = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
-            const uint32_t mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+            mlo = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+            mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+        }
 #pragma unroll
-            for (int mt = 0; mt < kSteps; ++mt) {
-                const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
-                const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
-                uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(lo, a0, a1);
-                e4m3x4_to_f16x2x2(hi, a2, a3);
-                mma_16816_f16(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+        for (int mt = 0; mt < kSteps; ++mt) {
+            // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
+            const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
+            const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
+            uint32_t a0, a1, a2, a3;
+            Codes::widen(lo, a0, a1);
+            Codes::widen(hi, a2, a3);
+            if constexpr (MASK) {
+                a0 &= mlo;
+                a1 &= mlo;
+                a2 &= mhi;
+                a3 &= mhi;
             }
+            mma_16816_f16(o[mt], a0, a1, a2, a3, b0, b1);
         }
     }
 
-    // One 16-row tile per step.
     // One query per sequence: rows past `valid` and the first `skip` rows (a
-    // sliding window) are masked; a tile always holds a visible row.
+    // sliding window) are masked; a tile always holds a visible row. xb: the
+    // stage's row scales (INT8).
     __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int valid,
                                          float /*scale_log2: folded into q'*/, int /*lane*/,
                                          int /*row0*/, int /*limit0*/, int /*grp*/, int skip,
-                                         uint32_t /*xb: none*/) {
+                                         uint32_t xb) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
-        qk(kbase, valid, skip, c);
+        qk(kbase, c);
+        float vs0 = 1.f, vs1 = 1.f;
+        if constexpr (Codes::kRowScales) {
+            const bool ok0 = gid < valid && gid >= skip;
+            const bool ok1 = gid + 8 < valid && gid + 8 >= skip;
+            // Scales of rows past the sequence are whatever memory holds: only
+            // visible rows read theirs.
+            const float ks0 = ok0 ? lds_f32(xb + 4 * gid) : 0.f;
+            const float ks1 = ok1 ? lds_f32(xb + 4 * (gid + 8)) : 0.f;
+            vs0 = ok0 ? lds_f32(xb + 4 * (kTileRows + gid)) : 0.f;
+            vs1 = ok1 ? lds_f32(xb + 4 * (kTileRows + gid + 8)) : 0.f;
+            c[0] = ok0 ? c[0] * ks0 : -INFINITY;
+            c[1] = ok0 ? c[1] * ks0 : -INFINITY;
+            c[2] = ok1 ? c[2] * ks1 : -INFINITY;
+            c[3] = ok1 ? c[3] * ks1 : -INFINITY;
+        } else {
+            (void)xb;
+            if (valid < kTileRows) {
+                if (gid >= valid) c[0] = c[1] = -INFINITY;
+                if (gid + 8 >= valid) c[2] = c[3] = -INFINITY;
+            }
+            if (skip > 0) {
+                if (gid < skip) c[0] = c[1] = -INFINITY;
+                if (gid + 8 < skip) c[2] = c[3] = -INFINITY;
+            }
+        }
         float mx0 = fmaxf(c[0], c[2]);
         float mx1 = fmaxf(c[1], c[3]);
 #pragma unroll
@@ -244,11 +293,19 @@ struct Fp8MmaMath {
             }
         }
         uint32_t b0, b1;
-        p_fragments(p0, p1, p2, p3, b0, b1);
-        pv(vbase, valid, b0, b1);
+        if constexpr (Codes::kRowScales) {
+            p_fragments(p0 * vs0, p1 * vs0, p2 * vs1, p3 * vs1, b0, b1);
+            pv<false>(vbase, valid, b0, b1);
+        } else {
+            p_fragments(p0, p1, p2, p3, b0, b1);
+            if (valid == kTileRows)
+                pv<false>(vbase, valid, b0, b1);
+            else
+                pv<true>(vbase, valid, b0, b1);
+        }
     }
 
-    // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o scaled by v_scale.
+    // State layout: m[G], l[G], o[G][D] (fp32, base-2 max), o times vscale.
     __device__ __forceinline__ void write_state(float* st, int /*lane*/, int /*ncols: G*/) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -269,5 +326,10 @@ struct Fp8MmaMath {
         }
     }
 };
+
+template <int D, int G>
+using Fp8MmaMath = QuantMmaMath<D, G, E4m3Codes>;
+template <int D, int G>
+using Int8MmaMath = QuantMmaMath<D, G, S8Codes>;
 
 }  // namespace pa
