@@ -168,7 +168,10 @@ pa_status pa_decode_int8(const void* q, const void* k_cache, const void* v_cache
  * Destinations must be distinct and no destination may be a source of
  * another pair in the same call (such pairs race). head_dim * sizeof(T) must
  * be a multiple of 16 and the pools 16-byte aligned. Returns PA_OK or an
- * error; never blocks.
+ * error; never blocks. For an INT8 cache (dtype PA_DTYPE_INT8) this copies
+ * the codes; copy the row scales with a second call on the two scale arrays
+ * viewed as fp32 pools of one KV head, one row and num_kv_heads * block_size
+ * values per block (num_kv_heads * block_size a multiple of 4).
  */
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
                          int num_pairs, int num_kv_heads, int head_dim, int block_size,

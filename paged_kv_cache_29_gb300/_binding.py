@@ -126,6 +126,8 @@ def _dtype_code(t) -> int:
         return 1
     if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
         return 2
+    if t.dtype == torch.int8:
+        return 3
     raise TypeError(f"dtype must be float32, bfloat16 or e4m3 codes, got {t.dtype}")
 
 
@@ -374,7 +376,9 @@ def pa_decode_int8(q, k_cache, v_cache, k_scales, v_scales, block_tables, contex
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None) -> None:
     """Copy-on-write: block dst := block src of both pools for each (src, dst)
-    row of block_mapping (int64 [n][2]); negative entries skip a pair."""
+    row of block_mapping (int64 [n][2]); negative entries skip a pair. The
+    pools are [NB][Hkv][bs][D]; for an INT8 cache call it again on the row
+    scales viewed as [NB][1][1][Hkv * bs]."""
     import torch
     _check_cuda("k_cache", k_cache, ndim=4)
     _check_cuda("v_cache", v_cache, k_cache.dtype, 4)

@@ -330,7 +330,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
                          int num_blocks, pa_dtype dtype, int32_t* error_word,
                          struct CUstream_st* stream) {
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks <= 0 || !valid_cache_dtype(dtype))
+        num_blocks <= 0 || !valid_decode_cache_dtype(dtype))
         return PA_ERR_INVALID_ARG;
     const int row_bytes = head_dim * elem_bytes(dtype);
     if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;

@@ -128,3 +128,30 @@ def test_int8_unsupported():
     with pytest.raises(pa.PagedAttentionError) as e:
         _gpu_step(step, append=False)                         # head_dim 64
     assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+def test_int8_copy_on_write_copies_codes_and_scales():
+    """pa_copy_blocks on the codes, then on the row scales viewed as a pool of
+    one head and one row: the copied blocks decode like the oracle's copy."""
+    step = wl.build_step("i8cow", [40, 600, 17], 32, 8, 128, cache_dtype="int8", seed=21)
+    nb = step.num_blocks
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(nb)
+    used = sorted({int(b) for b in step.block_tables.ravel() if b >= 0})
+    free = [int(b) for b in perm if int(b) not in used]
+    mapping = np.array([[used[i], free[i]] for i in range(min(6, len(free)))], np.int64)
+    kc, vc = _dev(step.k_cache), _dev(step.v_cache)
+    ks, vs = _dev(step.k_row_scales), _dev(step.v_row_scales)
+    md = _dev(mapping)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(kc, vc, md, error_word=err)
+    hkv, bs = step.num_kv_heads, step.block_size
+    pa.pa_copy_blocks(ks.view(nb, 1, 1, hkv * bs), vs.view(nb, 1, 1, hkv * bs), md, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    wk, wv = step.k_cache.copy(), step.v_cache.copy()
+    wks, wvs = step.k_row_scales.copy(), step.v_row_scales.copy()
+    for src, dst in mapping:
+        wk[dst], wv[dst], wks[dst], wvs[dst] = wk[src], wv[src], wks[src], wvs[src]
+    for dv, want in zip((kc, vc, ks, vs), (wk, wv, wks, wvs)):
+        np.testing.assert_array_equal(dv.cpu().numpy(), want)
