@@ -14,7 +14,7 @@ constexpr int kMinCtasPerSm = 4;   // four rings per SM (register budget 96 per 
 template <int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                 int sm_count, cudaStream_t stream) {
-    return launch_stream_instance<Fp8MmaMath<128, G>, 128, G, kWarps, kStages, kMinCtasPerSm>(
+    return launch_stream_instance<Fp8MmaMath<128, G>, 128, G, kWarps, kStages, kMinCtasPerSm, true>(
         tk, tv, p, sm_count, stream);
 }
 }  // namespace

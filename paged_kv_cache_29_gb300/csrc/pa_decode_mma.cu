@@ -17,9 +17,9 @@ cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams
     if constexpr (G > 1) {   // several query tokens fill at least two columns
         if (p.num_queries > 1)
             return launch_stream_instance<MmaMath<D, G, true>, D, G, kWarps, kStages,
-                                          kMinCtasPerSm>(tk, tv, p, sm_count, stream);
+                                          kMinCtasPerSm, false>(tk, tv, p, sm_count, stream);
     }
-    return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages, kMinCtasPerSm>(
+    return launch_stream_instance<MmaMath<D, G>, D, G, kWarps, kStages, kMinCtasPerSm, false>(
         tk, tv, p, sm_count, stream);
 }
 

@@ -17,7 +17,7 @@ constexpr int stages_for() {
 template <typename T, int D, int G>
 cudaError_t run(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                 int sm_count, cudaStream_t stream) {
-    return launch_stream_instance<SimtMath<T, D, G>, D, G, kWarps, stages_for<T, D>(), 1>(
+    return launch_stream_instance<SimtMath<T, D, G>, D, G, kWarps, stages_for<T, D>(), 1, false>(
         tk, tv, p, sm_count, stream);
 }
 

@@ -36,6 +36,7 @@
 #pragma once
 
 #include <atomic>
+#include <climits>
 
 #include "pa_plan.cuh"
 #include "pa_tile_math.cuh"
@@ -73,7 +74,8 @@ struct StreamSmem {
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
     static constexpr int kMerge = 2 * W * kState * 4;   // double-buffered warp states
     static constexpr int kBarriers = 2 * STAGES * 8;
-    static constexpr int kFlags = (STAGES + 2 * W + 8) * 4;
+    // stage_bad[STAGES], warp_bad[2 W], abort flag, last_t[STAGES], imeta[16]
+    static constexpr int kFlags = ((2 * STAGES + 2 * W + 8 + 16) * 4 + 15) / 16 * 16;
     static constexpr int kIds = 2 * kMaxItemBlocks * 4;
     static constexpr size_t kQBuf = 2 * Math_kQBufBytes;
     static constexpr size_t kExtra = static_cast<size_t>(STAGES) * XBYTES;   // per-stage side data
@@ -82,8 +84,11 @@ struct StreamSmem {
 };
 
 // MIN_CTAS: resident CTAs per SM the register budget is sized for (see
-// "Sizing" above).
-template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
+// "Sizing" above). PER_WARP_ISSUE: the producer refills each consumer warp's
+// stages independently (instead of in stream order), which pays where the
+// consumers' per-tile math is long (8-bit caches) and costs ~1 % where the
+// kernel streams at the bandwidth limit (bf16).
+template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS, bool PER_WARP_ISSUE>
 __global__ void __launch_bounds__((W + 1) * 32, MIN_CTAS)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -104,6 +109,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     volatile int32_t* stage_bad = reinterpret_cast<volatile int32_t*>(empty + STAGES);
     volatile int32_t* warp_bad = stage_bad + STAGES;          // [2][W]: per item parity
     volatile int32_t* abort_flag = warp_bad + 2 * W;
+    volatile int32_t* last_t = abort_flag + 8;                 // [STAGES]: producer's last tile per stage
+    volatile int32_t* imeta = last_t + STAGES;                 // [2][8]: producer's item meta
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
         reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
     uint8_t* qbuf = reinterpret_cast<uint8_t*>(ids_buf + 2 * kMaxItemBlocks);   // [2][kQBufBytes]
@@ -141,115 +148,317 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == W) {
         // ------------------------------ producer ------------------------------
-        // Item info and block ids are loaded one item ahead of their use.
-        auto load_item = [&](int j) -> int4 {
-            const int k = snake_item(c, j, C);
-            return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
-        };
-        // Block ids of an item are copied into a double-buffered shared array
-        // with cp.async one item ahead of their use.
-        auto prefetch_ids = [&](const int4& it, int32_t* buf) {
-            if (it.x >= 0) {
+        if constexpr (PER_WARP_ISSUE) {
+            // Consumer warp w takes tiles w, w + W, ... of every item, in ring
+            // stages w, w + W, ... . Lane w < W of this warp issues warp w's tiles
+            // in order; the W streams are independent, so a stage is refilled as
+            // soon as its own consumer frees it, whatever the other consumer warps
+            // are doing. The lanes stay converged: in every round each lane whose
+            // next stage is free issues its tile (arrive.expect_tx, then the K and
+            // V boxes); a round in which nothing moved sleeps on the empty barrier
+            // of the oldest outstanding tile.
+            //
+            // Items: the consumer warps meet at the end of every item, so no lane
+            // runs more than one item ahead of the slowest one. The block ids of
+            // item j (one coalesced cp.async, checked against the pool) live in
+            // buffer j & 1; those of item j + 1 are fetched once every lane has
+            // entered item j. Item descriptors are read two items ahead.
+            const int n_items = own_item_count(c, C, total);
+            auto load_item = [&](int j) -> int4 {
+                return j < n_items ? p.items[snake_item(c, j, C)] : make_int4(-1, 0, 0, 0);
+            };
+            if (lane < STAGES) last_t[lane] = -1;
+            int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
+            int4 d_req2 = load_item(1);
+            int jl = 0;                     // items whose ids were requested
+            int ready = 0;                  // items whose ids landed and were checked
+            int t_req = 0;                  // stream index of item jl's first tile
+            // Item meta in shared memory, slot j & 1: blocks, KV head, first row,
+            // first block, tiles, tiles per consumer warp, first stream index, bad.
+            auto request = [&]() {
+                const int4 it = d_req;
                 const int lo = seq_row_base(it.w, p.window) + it.z * P;
                 const int hi = min(it.w, lo + P);
                 const int b0 = lo / bs;
                 const int nblk = (hi - 1) / bs - b0 + 1;
+                const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
+                const int share = (ntiles + W - 1) / W;
+                int32_t* buf = ids_buf + (jl & 1) * kMaxItemBlocks;
                 const int32_t* bt = p.block_tables + static_cast<size_t>(it.x) * p.max_blocks_per_seq + b0;
                 for (int i = lane; i < nblk; i += 32) cp_async_4(smem_addr(buf + i), bt + i);
-            }
-            cp_async_commit();
-        };
-        int4 cur = load_item(0);
-        int4 nxt = load_item(1);
-        prefetch_ids(cur, ids_buf);
-        int t = 0;              // stream tile counter
-        int issued = 0;
-        bool ok = true;
-        for (int j = 0; cur.x >= 0 && ok; ++j) {
-            const int4 nxt2 = load_item(j + 2);     // used two items from now
-            int32_t* ids = ids_buf + (j & 1) * kMaxItemBlocks;
-            prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
-            cp_async_wait_group_1();                // this item's ids have landed
-            __syncwarp();
-            const int lo = seq_row_base(cur.w, p.window) + cur.z * P;
-            const int hi = min(cur.w, lo + P);
-            const int b0 = lo / bs;
-            const int nblk = (hi - 1) / bs - b0 + 1;
-            bool bad_lane = false;
-            for (int i = lane; i < nblk; i += 32) bad_lane |= (ids[i] < 0) | (ids[i] >= p.num_blocks);
-            const int cur_bad = __any_sync(0xffffffffu, bad_lane) ? 1 : 0;
-            const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
-            if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
-            // The item's tiles are padded with data-less slots up to a multiple
-            // of W, so that every item starts at a stream index divisible by W
-            // and warp w always takes tiles w, w + W, ... of the item: the
-            // rounding of an item's result never depends on what the CTA
-            // streamed before it.
-            const int span = ((ntiles + W - 1) / W) * W;
-            for (int tt = 0; tt < span; ++tt, ++t) {
-                const int tok = lo + kTileRows * tt;
-                const bool data = tt < ntiles && !cur_bad;
-                const int stage = t % STAGES;
-                const uint32_t fb = smem_addr(&full[stage]);
+                cp_async_commit();
                 if (lane == 0) {
-                    if (t >= STAGES && !mbar_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
+                    volatile int32_t* m = imeta + (jl & 1) * 8;
+                    m[0] = nblk; m[1] = it.y; m[2] = lo; m[3] = b0;
+                    m[4] = ntiles; m[5] = share; m[6] = t_req; m[7] = 0;
+                }
+                __syncwarp();
+                t_req += share * W;
+                ++jl;
+                d_req = d_req2;
+                d_req2 = load_item(jl + 1);
+            };
+            auto validate = [&](int j) {
+                cp_async_wait_all();
+                __syncwarp();
+                volatile int32_t* m = imeta + (j & 1) * 8;
+                const int nblk = m[0];
+                const int32_t* ids = ids_buf + (j & 1) * kMaxItemBlocks;
+                bool bad_lane = false;
+                for (int i = lane; i < nblk; i += 32) bad_lane |= (ids[i] < 0) | (ids[i] >= p.num_blocks);
+                const bool bad = __any_sync(0xffffffffu, bad_lane);
+                if (lane == 0) {
+                    m[7] = bad ? 1 : 0;
+                    if (bad) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
+                }
+                __syncwarp();
+                ready = j + 1;
+            };
+            bool ok = true;
+            if (n_items > 0) {
+                request();
+                validate(0);
+                if (jl < n_items) request();
+                // lane w < W: warp w's item and next tile within it, and that item's meta
+                int cj = 0, ci = 0;
+                int h = 0, lo = 0, b0 = 0, ntiles = 0, share = 0, t0 = 0, bad = 0;
+                auto enter = [&]() {
+                    const volatile int32_t* m = imeta + (cj & 1) * 8;
+                    h = m[1]; lo = m[2]; b0 = m[3]; ntiles = m[4]; share = m[5]; t0 = m[6]; bad = m[7];
+                };
+                if (lane < W) enter();
+                uint32_t idle_rounds = 0;
+                uint64_t idle_since = 0;
+                while (true) {
+                    // Issue first (a lane woken by its stage's release refills it
+                    // at once), then the item bookkeeping.
+                    bool moved = false;
+                    int t_wait = INT_MAX;                       // this lane's blocked tile, if any
+                    if (lane < W && cj < n_items && ci < share) {
+                        const int tt = lane + W * ci;           // tile within the item
+                        const int t = t0 + tt;
+                        const int stage = t % STAGES;
+                        if (t < STAGES || mbar_test_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
+                            const bool data = tt < ntiles && !bad;
+                            const uint32_t fb = smem_addr(&full[stage]);
+                            stage_bad[stage] = bad;
+                            last_t[stage] = t;
+                            if (data) {
+                                mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
+                                const int tok = lo + kTileRows * tt;
+                                const int id = ids_buf[(cj & 1) * kMaxItemBlocks + tok / bs - b0];
+                                const int row = (id * p.num_kv_heads + h) * bs + (tok % bs);
+                                const uint32_t dst = ring_addr + stage * Geom::kStageBytes;
+                                // One 3D box each (all 128-byte column halves of 16 rows).
+                                tma_load_3d(dst, &tmap_k, fb, 0, row, 0);
+                                tma_load_3d(dst + Geom::kTileBytes, &tmap_v, fb, 0, row, 0);
+                                if constexpr (Math::kExtraStageBytes > 0) {
+                                    // The tile's 16 K and 16 V row scales (64 bytes each,
+                                    // 64-byte aligned: the tile's first row is a multiple
+                                    // of 16 within its block).
+                                    const size_t r = static_cast<size_t>(row);
+                                    const uint32_t xd = xring + stage * Math::kExtraStageBytes;
+                                    constexpr int kHalf = Math::kExtraStageBytes / 2;
+                                    asm volatile(
+                                        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
+                                        " [%0], [%1], %2, [%3];" ::"r"(xd), "l"(p.k_row_scales + r),
+                                        "r"(kHalf), "r"(fb)
+                                        : "memory");
+                                    asm volatile(
+                                        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
+                                        " [%0], [%1], %2, [%3];" ::"r"(xd + kHalf),
+                                        "l"(p.v_row_scales + r), "r"(kHalf), "r"(fb)
+                                        : "memory");
+                                }
+                            } else {
+                                mbar_arrive(fb);                // no data: consumers skip the slot
+                            }
+                            ++ci;
+                            moved = true;
+                        } else {
+                            t_wait = t;
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, abort_flag[0] != 0)) {
                         ok = false;
-                    } else if (abort_flag[0]) {
-                        ok = false;
+                        break;
+                    }
+                    const bool live = lane < W && cj < n_items;
+                    const int jmin = __reduce_min_sync(0xffffffffu, live ? cj : INT_MAX);
+                    if (jmin == INT_MAX) break;                 // every tile issued
+                    // The ids of the next item: buffer jl & 1 last held item jl - 2,
+                    // which every lane has left.
+                    if (jl < n_items && jl == ready && jl <= jmin + 1) {
+                        request();
+                        moved = true;
+                    }
+                    const bool wants_next = live && ci == share && cj == jmin && cj + 1 < n_items;
+                    if (__any_sync(0xffffffffu, wants_next) && ready == jmin + 1 && jl > jmin + 1) {
+                        validate(jmin + 1);
+                        moved = true;
+                    }
+                    if (live && ci == share) {
+                        if (cj + 1 == n_items) {
+                            cj = n_items;                       // this warp's tiles are all issued
+                            moved = true;
+                        } else if (cj == jmin && cj + 1 < ready) {
+                            ++cj;
+                            ci = 0;
+                            enter();
+                            moved = true;
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, moved)) {
+                        idle_rounds = 0;
+                        continue;
+                    }
+                    // Nothing moved: sleep on the oldest blocked tile's empty barrier
+                    // (a hardware-suspended wait that returns when it completes or
+                    // after the system's time limit), then look at every lane again.
+                    const int t_old = __reduce_min_sync(0xffffffffu, t_wait);
+                    if (t_old != INT_MAX) {
+                        if (lane == 0)
+                            (void)mbar_try_wait(smem_addr(&empty[t_old % STAGES]),
+                                                ((t_old / STAGES) - 1) & 1);
+                        __syncwarp();
                     } else {
-                        stage_bad[stage] = cur_bad;
-                        if (data)
-                            mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
-                        else
-                            mbar_arrive(fb);          // no data: consumers skip the slot
-                        issued = t + 1;
+                        __nanosleep(64);
                     }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                // Lane 0 copies the K tile, lane 1 the V tile: one 3D box each
-                // (all 128-byte column halves of 16 rows), issued after lane
-                // 0's expect_tx (ordered by the shuffle above).
-                if (data && lane < 2) {
-                    const int id = ids[tok / bs - b0];
-                    const int row = (id * p.num_kv_heads + cur.y) * bs + (tok % bs);
-                    const uint32_t dst = ring_addr + stage * Geom::kStageBytes +
-                                         (lane ? Geom::kTileBytes : 0);
-                    tma_load_3d(dst, lane ? static_cast<const void*>(&tmap_v)
-                                          : static_cast<const void*>(&tmap_k),
-                                fb, 0, row, 0);
-                }
-                if constexpr (Math::kExtraStageBytes > 0) {
-                    // Lanes 2 and 3: the tile's 16 K and 16 V row scales (64 bytes
-                    // each, 64-byte aligned: the tile's first row is a multiple of
-                    // 16 within its block).
-                    if (data && (lane == 2 || lane == 3)) {
-                        const int id = ids[tok / bs - b0];
-                        const size_t r = (static_cast<size_t>(id) * p.num_kv_heads + cur.y) * bs + (tok % bs);
-                        const float* src = (lane == 2 ? p.k_row_scales : p.v_row_scales) + r;
-                        const uint32_t dst = xring + stage * Math::kExtraStageBytes +
-                                             (lane - 2) * (Math::kExtraStageBytes / 2);
-                        asm volatile(
-                            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
-                            " [%0], [%1], %2, [%3];" ::"r"(dst), "l"(src),
-                            "r"(Math::kExtraStageBytes / 2), "r"(fb)
-                            : "memory");
+                    if ((idle_rounds++ & 15u) == 0) {
+                        const uint64_t now = global_timer_ns();
+                        if (idle_rounds == 1) {
+                            idle_since = now;
+                        } else if (now - idle_since > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
                     }
                 }
             }
-            cur = nxt;
-            nxt = nxt2;
-        }
-        cp_async_wait_all();
-        if (lane == 0) {
+            cp_async_wait_all();
+            __syncwarp();
             if (!ok) {
-                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
-                abort_flag[0] = 1;
+                if (lane == 0 && !abort_flag[0]) {
+                    raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                    abort_flag[0] = 1;
+                }
+                // Copies still in flight must land before the CTA's shared memory
+                // is released: wait (bounded) for each stage's last issued tile.
+                if (lane < STAGES && last_t[lane] >= 0)
+                    (void)mbar_wait(smem_addr(&full[lane]), (last_t[lane] / STAGES) & 1);
             }
-            // Copies still in flight must land before the CTA's shared memory
-            // is released: wait (bounded) for the last issued stages.
-            for (int u = issued > STAGES ? issued - STAGES : 0; u < issued; ++u)
-                (void)mbar_wait(smem_addr(&full[u % STAGES]), (u / STAGES) & 1);
+        } else {
+            // In stream order: one lane waits for each stage in turn.
+            // Item info and block ids are loaded one item ahead of their use.
+            auto load_item = [&](int j) -> int4 {
+                const int k = snake_item(c, j, C);
+                return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
+            };
+            // Block ids of an item are copied into a double-buffered shared array
+            // with cp.async one item ahead of their use.
+            auto prefetch_ids = [&](const int4& it, int32_t* buf) {
+                if (it.x >= 0) {
+                    const int lo = seq_row_base(it.w, p.window) + it.z * P;
+                    const int hi = min(it.w, lo + P);
+                    const int b0 = lo / bs;
+                    const int nblk = (hi - 1) / bs - b0 + 1;
+                    const int32_t* bt = p.block_tables + static_cast<size_t>(it.x) * p.max_blocks_per_seq + b0;
+                    for (int i = lane; i < nblk; i += 32) cp_async_4(smem_addr(buf + i), bt + i);
+                }
+                cp_async_commit();
+            };
+            int4 cur = load_item(0);
+            int4 nxt = load_item(1);
+            prefetch_ids(cur, ids_buf);
+            int t = 0;              // stream tile counter
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; cur.x >= 0 && ok; ++j) {
+                const int4 nxt2 = load_item(j + 2);     // used two items from now
+                int32_t* ids = ids_buf + (j & 1) * kMaxItemBlocks;
+                prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
+                cp_async_wait_group_1();                // this item's ids have landed
+                __syncwarp();
+                const int lo = seq_row_base(cur.w, p.window) + cur.z * P;
+                const int hi = min(cur.w, lo + P);
+                const int b0 = lo / bs;
+                const int nblk = (hi - 1) / bs - b0 + 1;
+                bool bad_lane = false;
+                for (int i = lane; i < nblk; i += 32) bad_lane |= (ids[i] < 0) | (ids[i] >= p.num_blocks);
+                const int cur_bad = __any_sync(0xffffffffu, bad_lane) ? 1 : 0;
+                const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
+                if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
+                // The item's tiles are padded with data-less slots up to a multiple
+                // of W, so that every item starts at a stream index divisible by W
+                // and warp w always takes tiles w, w + W, ... of the item: the
+                // rounding of an item's result never depends on what the CTA
+                // streamed before it.
+                const int span = ((ntiles + W - 1) / W) * W;
+                for (int tt = 0; tt < span; ++tt, ++t) {
+                    const int tok = lo + kTileRows * tt;
+                    const bool data = tt < ntiles && !cur_bad;
+                    const int stage = t % STAGES;
+                    const uint32_t fb = smem_addr(&full[stage]);
+                    if (lane == 0) {
+                        if (t >= STAGES && !mbar_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
+                            ok = false;
+                        } else if (abort_flag[0]) {
+                            ok = false;
+                        } else {
+                            stage_bad[stage] = cur_bad;
+                            if (data)
+                                mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
+                            else
+                                mbar_arrive(fb);          // no data: consumers skip the slot
+                            issued = t + 1;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    // Lane 0 copies the K tile, lane 1 the V tile: one 3D box each
+                    // (all 128-byte column halves of 16 rows), issued after lane
+                    // 0's expect_tx (ordered by the shuffle above).
+                    if (data && lane < 2) {
+                        const int id = ids[tok / bs - b0];
+                        const int row = (id * p.num_kv_heads + cur.y) * bs + (tok % bs);
+                        const uint32_t dst = ring_addr + stage * Geom::kStageBytes +
+                                             (lane ? Geom::kTileBytes : 0);
+                        tma_load_3d(dst, lane ? static_cast<const void*>(&tmap_v)
+                                              : static_cast<const void*>(&tmap_k),
+                                    fb, 0, row, 0);
+                    }
+                    if constexpr (Math::kExtraStageBytes > 0) {
+                        // Lanes 2 and 3: the tile's 16 K and 16 V row scales (64 bytes
+                        // each, 64-byte aligned: the tile's first row is a multiple of
+                        // 16 within its block).
+                        if (data && (lane == 2 || lane == 3)) {
+                            const int id = ids[tok / bs - b0];
+                            const size_t r = (static_cast<size_t>(id) * p.num_kv_heads + cur.y) * bs + (tok % bs);
+                            const float* src = (lane == 2 ? p.k_row_scales : p.v_row_scales) + r;
+                            const uint32_t dst = xring + stage * Math::kExtraStageBytes +
+                                                 (lane - 2) * (Math::kExtraStageBytes / 2);
+                            asm volatile(
+                                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes"
+                                " [%0], [%1], %2, [%3];" ::"r"(dst), "l"(src),
+                                "r"(Math::kExtraStageBytes / 2), "r"(fb)
+                                : "memory");
+                        }
+                    }
+                }
+                cur = nxt;
+                nxt = nxt2;
+            }
+            cp_async_wait_all();
+            if (lane == 0) {
+                if (!ok) {
+                    raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                    abort_flag[0] = 1;
+                }
+                // Copies still in flight must land before the CTA's shared memory
+                // is released: wait (bounded) for the last issued stages.
+                for (int u = issued > STAGES ? issued - STAGES : 0; u < issued; ++u)
+                    (void)mbar_wait(smem_addr(&full[u % STAGES]), (u / STAGES) & 1);
+            }
         }
         return;
     }
@@ -386,12 +595,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
 // Host-side launch of one persistent instance: as many CTAs as fit on
 // sm_count SMs, programmatic dependent launch on the stream.
-template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS>
+template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS, bool PER_WARP_ISSUE>
 cudaError_t launch_stream_instance(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecodeParams& p, int sm_count, cudaStream_t stream) {
     using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D, Math::kQBufBytes,
                             Math::kExtraStageBytes>;
-    auto kernel = decode_stream_kernel<Math, D, G, W, STAGES, MIN_CTAS>;
+    auto kernel = decode_stream_kernel<Math, D, G, W, STAGES, MIN_CTAS, PER_WARP_ISSUE>;
     const int smem = static_cast<int>(Smem::kBytes);
     // The shared-memory attribute and the resulting CTAs per SM are set up
     // once per device and instance.

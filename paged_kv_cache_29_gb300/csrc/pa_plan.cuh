@@ -36,6 +36,14 @@ __device__ __forceinline__ int snake_item(int c, int j, int C) {
     return j * C + ((j & 1) ? (C - 1 - c) : c);
 }
 
+// Number of items CTA c owns when the launch has `total` items.
+__device__ __forceinline__ int own_item_count(int c, int C, int total) {
+    const int rounds = total / C;
+    const int rem = total - rounds * C;
+    const int pos = (rounds & 1) ? (C - 1 - c) : c;   // its slot in the last, partial round
+    return rounds + (pos < rem ? 1 : 0);
+}
+
 // Shared ints plan_cta needs for NT threads.
 __host__ __device__ constexpr int plan_scratch_ints(int nt) {
     return (nt / 32) * (1 + kPlanBuckets) + 3 * kPlanBuckets + 4;
