@@ -171,17 +171,22 @@ __host__ __device__ __forceinline__ int combine_warps(int np) {
 template <typename T, int E>
 __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const DecodeParams p) {
     extern __shared__ float sm[];                // [nw][2 + head_dim]
-    // Launched as a programmatic dependent of the decode kernel: wait for its
-    // partials before reading anything.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int qh = blockIdx.x;
     const int sq = blockIdx.y;                 // s * num_queries + query token
     const int s = sq / p.num_queries;
+    // Launched as a programmatic dependent of the decode kernel, which starts
+    // this grid only after its own griddepcontrol.wait (every kernel before it
+    // has completed) and never writes the context lengths: they are final and
+    // visible here, and a sequence of one partition (written directly by the
+    // decode kernel) leaves at once. CTA (0, 0) always waits, so that this
+    // grid never completes before the decode kernel does.
     const int n = __ldg(p.context_lens + s);
     const int P = p.partition_size;
-    if (n > p.context_cap || n < p.num_queries) return;   // flagged
     const int span = n - seq_row_base(n, p.window);       // rows of the partitions
-    if (span <= P) return;                     // one partition (written directly)
+    const bool merge = n <= p.context_cap && n >= p.num_queries && span > P;   // else flagged or one partition
+    if (!merge && (blockIdx.x | blockIdx.y) != 0) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");    // the partials are the decode kernel's output
+    if (!merge) return;
     const int np = (span + P - 1) / P;
     const int nw = combine_warps(np);
     const int D = p.head_dim;
@@ -197,6 +202,15 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
         for (int c0 = warp * kCombineChunk; c0 < np; c0 += nw * kCombineChunk) {
             const int cnt = min(kCombineChunk, np - c0);
             const float2 v = lane < cnt ? ml[c0 + lane] : make_float2(-INFINITY, 0.f);
+            // The first o rows are loaded together with the maxima.
+            float ov[kCombineBatch][E];
+#pragma unroll
+            for (int k = 0; k < kCombineBatch; ++k)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int d = lane + 32 * e;
+                    ov[k][e] = (k < cnt && d < D) ? o[static_cast<size_t>(c0 + k) * D + d] : 0.f;
+                }
             const float Mc = fmaxf(M, warp_max(v.x));
             // Partitions a query token does not reach (several tokens per
             // sequence) hold m = -inf, l = 0: weight 0, never NaN.
@@ -208,15 +222,16 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
             for (int e = 0; e < E; ++e) acc[e] *= rescale;
             M = Mc;
             for (int i = 0; i < cnt; i += kCombineBatch) {
-                float ov[kCombineBatch][E];
+                if (i > 0) {
 #pragma unroll
-                for (int k = 0; k < kCombineBatch; ++k)
+                    for (int k = 0; k < kCombineBatch; ++k)
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const int d = lane + 32 * e;
-                        ov[k][e] = (i + k < cnt && d < D)
-                                       ? o[static_cast<size_t>(c0 + i + k) * D + d] : 0.f;
-                    }
+                        for (int e = 0; e < E; ++e) {
+                            const int d = lane + 32 * e;
+                            ov[k][e] = (i + k < cnt && d < D)
+                                           ? o[static_cast<size_t>(c0 + i + k) * D + d] : 0.f;
+                        }
+                }
 #pragma unroll
                 for (int k = 0; k < kCombineBatch; ++k) {
                     const float wk = __shfl_sync(0xffffffffu, w, (i + k) & 31);

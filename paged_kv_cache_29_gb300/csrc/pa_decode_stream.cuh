@@ -74,8 +74,10 @@ struct StreamSmem {
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
     static constexpr int kMerge = 2 * W * kState * 4;   // double-buffered warp states
     static constexpr int kBarriers = 2 * STAGES * 8;
-    // stage_bad[STAGES], warp_bad[2 W], abort flag, last_t[STAGES], imeta[16]
-    static constexpr int kFlags = ((2 * STAGES + 2 * W + 8 + 16) * 4 + 15) / 16 * 16;
+    // stage_bad[STAGES], warp_bad[2 W], abort flag (+7), last_t[STAGES],
+    // imeta[16], then (16-byte aligned) the CTA's first two items
+    static constexpr int kFirstItemsOffset = ((2 * STAGES + 2 * W + 8 + 16) * 4 + 15) / 16 * 16;
+    static constexpr int kFlags = kFirstItemsOffset + 2 * 16;
     static constexpr int kIds = 2 * kMaxItemBlocks * 4;
     static constexpr size_t kQBuf = 2 * Math_kQBufBytes;
     static constexpr size_t kExtra = static_cast<size_t>(STAGES) * XBYTES;   // per-stage side data
@@ -111,6 +113,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     volatile int32_t* abort_flag = warp_bad + 2 * W;
     volatile int32_t* last_t = abort_flag + 8;                 // [STAGES]: producer's last tile per stage
     volatile int32_t* imeta = last_t + STAGES;                 // [2][8]: producer's item meta
+    int4* first_items = reinterpret_cast<int4*>(
+        reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFirstItemsOffset);   // [2]
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
         reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
     uint8_t* qbuf = reinterpret_cast<uint8_t*>(ids_buf + 2 * kMaxItemBlocks);   // [2][kQBufBytes]
@@ -140,8 +144,14 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int c = blockIdx.x;
     // The CTA's work list; its scratch is the merge area, free until the first
     // item ends. The items are read back with plain (coherent) loads.
-    const int total = plan_cta<T, (W + 1) * 32>(p, c, C, reinterpret_cast<int*>(merge));
+    const int total = plan_cta<T, (W + 1) * 32>(p, c, C, reinterpret_cast<int*>(merge), first_items);
     __syncthreads();
+    // The CTA's j-th item (x = -1: none): the first two from shared memory.
+    auto own_item = [&](int j) -> int4 {
+        const int k = snake_item(c, j, C);
+        if (k >= total) return make_int4(-1, 0, 0, 0);
+        return j < 2 ? first_items[j] : p.items[k];
+    };
     const int P = p.partition_size;
     const int bs = p.block_size;
     const uint32_t ring_addr = smem_addr(ring);
@@ -164,9 +174,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // buffer j & 1; those of item j + 1 are fetched once every lane has
             // entered item j. Item descriptors are read two items ahead.
             const int n_items = own_item_count(c, C, total);
-            auto load_item = [&](int j) -> int4 {
-                return j < n_items ? p.items[snake_item(c, j, C)] : make_int4(-1, 0, 0, 0);
-            };
+            auto load_item = own_item;
             if (lane < STAGES) last_t[lane] = -1;
             int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
             int4 d_req2 = load_item(1);
@@ -350,10 +358,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         } else {
             // In stream order: one lane waits for each stage in turn.
             // Item info and block ids are loaded one item ahead of their use.
-            auto load_item = [&](int j) -> int4 {
-                const int k = snake_item(c, j, C);
-                return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
-            };
+            auto load_item = own_item;
             // Block ids of an item are copied into a double-buffered shared array
             // with cp.async one item ahead of their use.
             auto prefetch_ids = [&](const int4& it, int32_t* buf) {
@@ -474,10 +479,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int grp = Math::kCausal ? p.num_heads / p.num_kv_heads : G;
     const int Qn = Math::kCausal ? p.num_queries : 1;
     const int ncols = Math::kCausal ? grp * Qn : G;
-    auto item_at = [&](int j) -> int4 {
-        const int k = snake_item(c, j, C);
-        return k < total ? p.items[k] : make_int4(-1, 0, 0, 0);
-    };
+    auto item_at = own_item;
     int4 it = item_at(0);
     int4 it_next = item_at(1);
     typename Math::QRegs q_next;

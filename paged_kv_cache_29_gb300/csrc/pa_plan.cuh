@@ -74,11 +74,13 @@ __device__ __forceinline__ int plan_bucket(int r, int P) {
     return r > 0 ? min(kPlanBuckets - 1, ((P - r) * kPlanBuckets) / P) : -1;
 }
 
-// Writes CTA c's items and returns the number of items of the launch. All NT
-// threads of the CTA call it; `sm` holds plan_scratch_ints(NT) ints. Row bytes
+// Writes CTA c's items and returns the number of items of the launch; the
+// CTA's first two items also go to `first` (shared memory), so that its work
+// starts without a global-memory round trip. All NT threads of the CTA call
+// it; `sm` holds plan_scratch_ints(NT) ints. Row bytes
 // of the output (num_heads * head_dim * sizeof(T)) are a multiple of 16.
 template <typename T, int NT>
-__device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
+__device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* first) {
     constexpr int NW = NT / 32;
     int* wsum = sm;                          // [NW]
     int* wcnt = wsum + NW;                   // [NW][kPlanBuckets]
@@ -121,7 +123,9 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
         const int pf = base + incl - nf;     // full partitions before sequence s
         for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
             const int unit = k / Hkv;
-            p.items[k] = make_int4(s, k - unit * Hkv, unit - pf, n);
+            const int4 v = make_int4(s, k - unit * Hkv, unit - pf, n);
+            p.items[k] = v;
+            if (k < 2 * C) first[k / C] = v;
         });
         const int b = n > 0 ? plan_bucket(span % P, P) : -1;
         if (b >= 0) atomicAdd(&bcount[b], 1);
@@ -167,7 +171,11 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm) {
             for (int w = 0; w < warp; ++w) j += wcnt[w * kPlanBuckets + b];
             const int a = full_items + j * Hkv;
             const int nf = span / P;
-            for_own_items(a, a + Hkv, c, C, [&](int k) { p.items[k] = make_int4(s, k - a, nf, n); });
+            for_own_items(a, a + Hkv, c, C, [&](int k) {
+                const int4 v = make_int4(s, k - a, nf, n);
+                p.items[k] = v;
+                if (k < 2 * C) first[k / C] = v;
+            });
         }
         __syncthreads();
         if (tid < kPlanBuckets) {
