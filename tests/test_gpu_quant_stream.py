@@ -1,0 +1,94 @@
+"""Work-list edge cases of the FP8 and INT8 decode kernels on the GPU, through
+the C ABI. Their producer refills each consumer warp's ring stages from that
+warp's own issue stream (block ids double-buffered per item), so these cases
+aim at the item bookkeeping: hundreds of one-tile items per CTA (the streams
+constantly one item apart), every tile count, CTAs with no item at all, empty
+sequences and partition edges, and a bad block id in the middle of a CTA's
+stream (flagged, the other sequences still exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from paged_kv_cache_29_gb300 import _binding as pa
+from paged_kv_cache_29_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = ["fp8", "int8"]
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _run(fmt, step, tables=None):
+    """Decode over the step's caches as they are (no append); returns the
+    output (fp64) and the device error word."""
+    q = to_torch(step.q, "bf16")
+    kc, vc = _dev(step.k_cache), _dev(step.v_cache)
+    bt = to_torch(step.block_tables if tables is None else tables)
+    lens = to_torch(step.context_lens)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    if fmt == "fp8":
+        pa.pa_decode_fp8(q, kc, vc, bt, lens, step.scale, out, step.max_context_len,
+                         step.k_scale, step.v_scale, error_word=err)
+    else:
+        pa.pa_decode_int8(q, kc, vc, _dev(step.k_row_scales), _dev(step.v_row_scales), bt, lens,
+                          step.scale, out, step.max_context_len, error_word=err)
+    torch.cuda.synchronize()
+    return wl.as_f32(from_torch(out), "bf16").astype(np.float64), int(err.item())
+
+
+def _reference(fmt, step):
+    if fmt == "fp8":
+        return oracle.decode_kv(step.q, step.k_cache, step.v_cache, step.block_tables,
+                                step.context_lens, step.scale, step.k_scale, step.v_scale)
+    return oracle.decode_int8(step.q, step.k_cache, step.v_cache, step.k_row_scales,
+                              step.v_row_scales, step.block_tables, step.context_lens, step.scale)
+
+
+LENS = {
+    # hundreds of one-tile items: every CTA gets several, each one tile per
+    # consumer warp at most
+    "one_tile_items": [1] * 700 + [17, 33],
+    # every tile count from 1 to 100 (rows 16 k + 1: a one-row ragged tail)
+    "every_tile_count": [16 * k + 1 for k in range(100)],
+    # a single item: nearly every CTA has nothing to do
+    "single_item": [17],
+    # empty sequences, partition edges (511, 512, 513) and a long sequence
+    "empty_and_edges": [0, 9000, 0, 1, 511, 512, 513, 0],
+}
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("case", sorted(LENS))
+def test_work_list_shapes(fmt, case):
+    lens = LENS[case]
+    step = wl.build_step(f"qs_{case}", lens, 32, 8, 128, cache_dtype=fmt, seed=31)
+    got, err = _run(fmt, step)
+    want = _reference(fmt, step)
+    assert err == 0
+    empty = [s for s, n in enumerate(lens) if n == 0]
+    assert np.all(got[empty] == 0.0)
+    assert max_abs(got, want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_bad_block_id_mid_stream_is_flagged(fmt):
+    lens = [40, 1300, 33, 700, 5000, 16]
+    step = wl.build_step("qs_bad", lens, 32, 8, 128, cache_dtype=fmt, seed=32)
+    want = _reference(fmt, step)
+    bad = step.block_tables.copy()
+    bad[1, 40] = step.num_blocks + 3           # a full partition of sequence 1: outside the pool
+    bad[4, 300] = -2                           # the last partition of sequence 4
+    got, err = _run(fmt, step, tables=bad)
+    assert err & pa.PA_DEVERR_BLOCK_ID
+    ok = [0, 2, 3, 5]
+    assert max_abs(got[ok], want[ok]) <= TOL["bf16"]
+    # The next call on a clean table is exact again (no state carried over).
+    got, err = _run(fmt, step)
+    assert err == 0
+    assert max_abs(got, want) <= TOL["bf16"]
