@@ -36,10 +36,14 @@
 //       Each lane reads whole 16-byte chunks 2 t4 and 2 t4 + 1 of rows gid
 //       and gid + 8; with the 128-byte swizzle the 8 lanes of a phase hit 8
 //       different chunks (no bank conflicts).
-//   PV  m-tile mt covers, for lane gid, dims 16 gid + 2 mt (row gid) and
-//       16 gid + 2 mt + 1 (row gid + 8); the A registers pair tokens (2 t4,
-//       2 t4 + 1) and (2 t4 + 8, 2 t4 + 9), read as chunk gid of those four
-//       token rows and interleaved with byte permutes.
+//   PV  m-tile mt covers dims 16 mt + gid (row gid) and 16 mt + gid + 8 (row
+//       gid + 8): the 16-byte chunk mt of the tile's 16 token rows, read with
+//       a transposing 8-bit ldmatrix (m16n16.trans.b8). That load gives lane
+//       (gid, t4) column gid (first word) and column gid + 8 (second word) of
+//       matrix rows 4 t4 .. 4 t4 + 3; matrix row 4 t + j is pointed at token
+//       row 2 t + (j & 1) + 8 (j >> 1), so each word holds the codes of tokens
+//       2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9: the A registers' token pairs,
+//       widened with no byte shuffling.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -61,6 +65,17 @@ __device__ __forceinline__ void mma_16816_f16(float* c, uint32_t a0, uint32_t a1
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two 16 x 16 byte matrices (threads 0-15 give matrix 0's row addresses,
+// threads 16-31 matrix 1's), transposed: lane (gid, t4) receives column gid
+// (w0 / w2) and column gid + 8 (w1 / w3) of rows 4 t4 .. 4 t4 + 3, the lowest
+// row in the lowest byte.
+__device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t& w0, uint32_t& w1,
+                                                 uint32_t& w2, uint32_t& w3) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                 : "r"(addr));
 }
 
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
@@ -189,19 +204,16 @@ struct QuantMmaMath {
         b1 = prmt(u0, u1, sel);
     }
 
-    // O^T += code(V)^T . P^T over one 16-row tile: V rows 2t4, 2t4+1, 2t4+8,
-    // 2t4+9, chunk gid. MASK zeroes the V values of rows past `valid`, whose
-    // codes may be NaN (e4m3) so that 0 * V stays 0; int8 codes are finite.
+    // O^T += code(V)^T . P^T over one 16-row tile (two 16-dim chunks per
+    // ldmatrix). MASK zeroes the V values of rows past `valid`, whose codes may
+    // be NaN (e4m3) so that 0 * V stays 0; int8 codes are finite.
     template <bool MASK>
     __device__ __forceinline__ void pv(uint32_t vbase, int valid, uint32_t b0, uint32_t b1) {
-        const uint4 x0 = lds128(swizzled(vbase, 2 * t4, gid));
-        const uint4 x1 = lds128(swizzled(vbase, 2 * t4 + 1, gid));
-        const uint4 x2 = lds128(swizzled(vbase, 2 * t4 + 8, gid));
-        const uint4 x3 = lds128(swizzled(vbase, 2 * t4 + 9, gid));
-        const uint32_t e0[4] = {x0.x, x0.y, x0.z, x0.w};
-        const uint32_t e1[4] = {x1.x, x1.y, x1.z, x1.w};
-        const uint32_t e2[4] = {x2.x, x2.y, x2.z, x2.w};
-        const uint32_t e3[4] = {x3.x, x3.y, x3.z, x3.w};
+        const int r = (4 * gid + t4) & 15;                 // matrix row this lane points at
+        const int tok = 2 * (r >> 2) + (r & 1) + 8 * ((r >> 1) & 1);
+        const uint32_t row = vbase + static_cast<uint32_t>(tok * 128);
+        const int sw = tok & 7;                            // 128-byte swizzle of that row
+        const int second = gid >> 2;                       // lanes 16-31: the second chunk
         uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
         if constexpr (MASK) {
             const int tk = 2 * t4;
@@ -209,21 +221,24 @@ struct QuantMmaMath {
             mhi = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
         }
 #pragma unroll
-        for (int mt = 0; mt < kSteps; ++mt) {
-            // bytes 2(mt%2), 2(mt%2)+1 of word mt/2: dims 16 gid + 2 mt and + 1
-            const uint32_t sel_v = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t lo = prmt(e0[mt >> 1], e1[mt >> 1], sel_v);
-            const uint32_t hi = prmt(e2[mt >> 1], e3[mt >> 1], sel_v);
-            uint32_t a0, a1, a2, a3;
-            Codes::widen(lo, a0, a1);
-            Codes::widen(hi, a2, a3);
-            if constexpr (MASK) {
-                a0 &= mlo;
-                a1 &= mlo;
-                a2 &= mhi;
-                a3 &= mhi;
+        for (int i = 0; i < kSteps / 2; ++i) {
+            uint32_t w[4];
+            ldsm_x2_trans_b8(row + static_cast<uint32_t>(((2 * i + second) ^ sw) << 4), w[0], w[1],
+                             w[2], w[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int mt = 2 * i + h;
+                uint32_t a0, a1, a2, a3;
+                Codes::widen(w[2 * h], a0, a2);            // dim 16 mt + gid
+                Codes::widen(w[2 * h + 1], a1, a3);        // dim 16 mt + gid + 8
+                if constexpr (MASK) {
+                    a0 &= mlo;
+                    a1 &= mlo;
+                    a2 &= mhi;
+                    a3 &= mhi;
+                }
+                mma_16816_f16(o[mt], a0, a1, a2, a3, b0, b1);
             }
-            mma_16816_f16(o[mt], a0, a1, a2, a3, b0, b1);
         }
     }
 
@@ -320,9 +335,9 @@ struct QuantMmaMath {
         float* so = st + 2 * G;
 #pragma unroll
         for (int mt = 0; mt < kSteps; ++mt) {
-            const int d0 = 16 * gid + 2 * mt;
-            if (h0 < G) { so[h0 * D + d0] = o[mt][0] * vscale; so[h0 * D + d0 + 1] = o[mt][2] * vscale; }
-            if (h1 < G) { so[h1 * D + d0] = o[mt][1] * vscale; so[h1 * D + d0 + 1] = o[mt][3] * vscale; }
+            const int d0 = 16 * mt + gid;
+            if (h0 < G) { so[h0 * D + d0] = o[mt][0] * vscale; so[h0 * D + d0 + 8] = o[mt][2] * vscale; }
+            if (h1 < G) { so[h1 * D + d0] = o[mt][1] * vscale; so[h1 * D + d0 + 8] = o[mt][3] * vscale; }
         }
     }
 };
