@@ -19,10 +19,12 @@
 // Consumer warps: the CTA's tiles are numbered in stream order; tile t lives
 // in stage t % STAGES and is consumed by warp t % W (STAGES is a multiple of
 // W, so every stage has one owner and parity waits stay within one phase).
-// At the end of an item every warp writes its online-softmax state to a
-// double-buffered merge area, the consumer warps meet at a named barrier, and
-// the merged result is written as the final output (one partition) or as the
-// item's partial (max, sum, unnormalised output) for the combine kernel.
+// At the end of an item every warp writes its online-softmax state to the
+// merge area, the consumer warps meet at a named barrier, the merged result is
+// written as the final output (one partition) or as the item's partial (max,
+// sum, unnormalised output) for the combine kernel, and a second barrier frees
+// the area for the next item (one buffer: with 8 query columns a second one
+// would cost a CTA per SM).
 //
 // Sizing: a random 4 KB tile gather streams at about 6.6 TB/s on GB300 only
 // with four or more independent rings per SM (a ring's single producer waits
@@ -68,15 +70,18 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes, int XBYTES = 0>
+template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes, int XBYTES,
+          bool PER_WARP_ISSUE>
 struct StreamSmem {
     static constexpr int kRing = STAGES * Geom::kStageBytes;
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
-    static constexpr int kMerge = 2 * W * kState * 4;   // double-buffered warp states
+    static constexpr int kMerge = W * kState * 4;       // the warps' states at an item's end
     static constexpr int kBarriers = 2 * STAGES * 8;
-    // stage_bad[STAGES], warp_bad[2 W], abort flag (+7), last_t[STAGES],
-    // imeta[16], then (16-byte aligned) the CTA's first two items
-    static constexpr int kFirstItemsOffset = ((2 * STAGES + 2 * W + 8 + 16) * 4 + 15) / 16 * 16;
+    // stage_bad[STAGES], warp_bad[2 W], abort flag (+7), with per-warp issue
+    // last_t[STAGES] and imeta[16]; then (16-byte aligned) the CTA's first two
+    // items
+    static constexpr int kFlagInts = STAGES + 2 * W + 8 + (PER_WARP_ISSUE ? STAGES + 16 : 0);
+    static constexpr int kFirstItemsOffset = (kFlagInts * 4 + 15) / 16 * 16;
     static constexpr int kFlags = kFirstItemsOffset + 2 * 16;
     static constexpr int kIds = 2 * kMaxItemBlocks * 4;
     static constexpr size_t kQBuf = 2 * Math_kQBufBytes;
@@ -97,7 +102,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
-    using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes, Math::kExtraStageBytes>;
+    using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes, Math::kExtraStageBytes,
+                            PER_WARP_ISSUE>;
     static_assert(Math::kExtraStageBytes % 16 == 0, "side data moves in 16-byte units");
     static_assert(Smem::kMerge >= 4 * plan_scratch_ints((W + 1) * 32),
                   "the plan's scratch lives in the merge area");
@@ -111,8 +117,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     volatile int32_t* stage_bad = reinterpret_cast<volatile int32_t*>(empty + STAGES);
     volatile int32_t* warp_bad = stage_bad + STAGES;          // [2][W]: per item parity
     volatile int32_t* abort_flag = warp_bad + 2 * W;
-    volatile int32_t* last_t = abort_flag + 8;                 // [STAGES]: producer's last tile per stage
-    volatile int32_t* imeta = last_t + STAGES;                 // [2][8]: producer's item meta
+    // per-warp issue only: the producer's last tile per stage, item meta [2][8]
+    volatile int32_t* last_t = abort_flag + 8;
+    volatile int32_t* imeta = last_t + STAGES;
     int4* first_items = reinterpret_cast<int4*>(
         reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFirstItemsOffset);   // [2]
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
@@ -542,7 +549,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         it = it_next;
         it_next = it_after;
         t0 += span;
-        float* buf = merge + (j & 1) * (W * Smem::kState);
+        float* buf = merge;
         math.write_state(buf + warp * Smem::kState, lane, ncols);
         if constexpr (Math::kQInSmem) {
             if (warp == 0) cp_async_wait_all();   // next item's q is visible after the barrier
@@ -559,9 +566,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         bool any_bad = false;
 #pragma unroll
         for (int w = 0; w < W; ++w) any_bad |= warp_bad[(j & 1) * W + w] != 0;
-        if (any_bad) continue;              // flagged by the producer; output left unspecified
+        // any_bad: flagged by the producer; output left unspecified
         const int nparts = (n - base + P - 1) / P;
-        for (int idx = threadIdx.x; idx < ncols * D; idx += W * 32) {
+        for (int idx = any_bad ? ncols * D : threadIdx.x; idx < ncols * D; idx += W * 32) {
             const int g = idx / D;            // query column
             const int d = idx - g * D;
             float M = -INFINITY;
@@ -592,6 +599,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
             }
         }
+        // The next item's warp states overwrite the merge area.
+        named_barrier(1, W * 32);
     }
 }
 
@@ -601,7 +610,7 @@ template <class Math, int D, int G, int W, int STAGES, int MIN_CTAS, bool PER_WA
 cudaError_t launch_stream_instance(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecodeParams& p, int sm_count, cudaStream_t stream) {
     using Smem = StreamSmem<W, STAGES, typename Math::Geom, G, D, Math::kQBufBytes,
-                            Math::kExtraStageBytes>;
+                            Math::kExtraStageBytes, PER_WARP_ISSUE>;
     auto kernel = decode_stream_kernel<Math, D, G, W, STAGES, MIN_CTAS, PER_WARP_ISSUE>;
     const int smem = static_cast<int>(Smem::kBytes);
     // The shared-memory attribute and the resulting CTAs per SM are set up
