@@ -309,7 +309,7 @@ def run_native(args) -> dict | None:
     stream = torch.cuda.current_stream(dev)
     # append, decode, and the split-K merge when a sequence spans more than
     # one 512-row partition (batches of at most 4096 sequences: one launch each)
-    launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)
+    launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)   # unfused; see fused_step
 
     def do_append(st):
         if int8:
@@ -340,9 +340,21 @@ def run_native(args) -> dict | None:
             pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                          workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
 
-    def do_step(st=None):
+    # One decode step. bf16/fp32 caches with one query token per sequence and
+    # no window go through pa_append_decode (the decode kernel writes the new
+    # rows itself); the other workloads append, then decode.
+    fused_step = not (int8 or fp8) and Qn == 1 and step.window == 0
+
+    def do_unfused_step(st=None):
         do_append(st)
         do_decode(st)
+
+    def do_step(st=None):
+        if not fused_step:
+            do_unfused_step(st)
+            return
+        pa.pa_append_decode(k_new, v_new, slots, k_cache, v_cache, q, tables, lens, step.scale,
+                            out, mcl, workspace=workspace, error_word=err, stream=st)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -355,10 +367,13 @@ def run_native(args) -> dict | None:
     # (launches replayed without host gaps, as a serving loop replays a decode
     # step); both run the same kernels as the eager calls.
     graph_step, graph_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    graph_unfused = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_step):
         do_step(None)
     with torch.cuda.graph(graph_decode):
         do_decode(None)
+    with torch.cuda.graph(graph_unfused):
+        do_unfused_step(None)
     for _ in range(args.warmup):
         flush_l2()
         graph_step.replay()
@@ -397,6 +412,7 @@ def run_native(args) -> dict | None:
     decode_ms = timed(graph_decode.replay, K)
     decode_avg = sum(decode_ms) / K
     eager_ms = timed(lambda: do_step(stream), K)
+    unfused_ms = timed(graph_unfused.replay, K) if fused_step else step_ms
     append_ms = sum(a - b for a, b in zip(step_ms, decode_ms)) / K
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
@@ -487,6 +503,8 @@ def run_native(args) -> dict | None:
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),
             "max_context_len": mcl, "partition_size": 512, "kernel": kernel_name,
+            "step": ("pa_append_decode (new rows written by the decode kernel)" if fused_step
+                     else "pa_reshape_and_cache + decode call"),
             "l2": "between timed steps a 256 MiB buffer is written, then another 256 MiB read (L2 clean, holding none of the step's data); attended K/V also exceed L2",
             "parallelism": f"replicas x{world} (independent batches per GPU)",
         },
@@ -495,7 +513,8 @@ def run_native(args) -> dict | None:
         "pct_of_measured_hbm": round(100 * value / peak / world, 2),
         "pct_of_nominal_8tbs": round(100 * value / NOMINAL_HBM_GBS / world, 2),
         "step_breakdown_ms": {"append_and_overlap": round(append_ms, 5),
-                              "decode_call": round(decode_avg, 5)},
+                              "decode_call": round(decode_avg, 5),
+                              "unfused_step": round(sum(unfused_ms) / K, 5)},
         "eager_ms_per_step": round(sum(eager_ms) / K, 5),
         "timing": "CUDA graph replay of one step per timed iteration; eager_ms_per_step "
                   "is the same step launched through the Python binding",
@@ -517,7 +536,7 @@ def run_native(args) -> dict | None:
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
         },
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": (launches_per_step - (1 if fused_step else 0)) * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
         "copy_blocks": None if copy_info is None else {
             "pairs": copy_info[0],

@@ -214,6 +214,38 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     size_t workspace_bytes, int32_t* error_word, struct CUstream_st* stream);
 
 /*
+ * pa_append_decode -- one decode step in one call: pa_reshape_and_cache of one
+ * new token per sequence followed by pa_decode (the token is the last of the
+ * context_lens[s] rows attended), as in the naive decoder of "MLSys Engineer
+ * -- Inference Systems Q&A", Q1: append the step's K and V, then attend over
+ * every cached row including them.
+ *
+ * k_new, v_new: [num_seqs][num_kv_heads][head_dim] in `dtype` (device,
+ *   16-byte aligned); slot_mapping: int64 [num_seqs], slot_mapping[s] the slot
+ *   of row context_lens[s] - 1 of sequence s, i.e.
+ *   block_tables[s][(n - 1) / block_size] * block_size + (n - 1) % block_size,
+ *   or negative (nothing appended for s). Every other argument as pa_decode.
+ * The tile-ring kernels write each new row from the CTA that attends to the
+ * sequence's last partition, just before it loads that tile: no separate
+ * append kernel, no extra pass over HBM. Other shapes run pa_reshape_and_cache's
+ * kernel, then pa_decode's plain kernel. Results (cache bytes and output) are
+ * those of the two calls in sequence.
+ * Errors: host checks as pa_reshape_and_cache and pa_decode. A slot that is
+ * non-negative but not the slot of row n - 1 (or of an empty sequence) sets
+ * PA_DEVERR_SLOT in error_word and is not written (fused path; the unfused
+ * path writes any slot inside the pool, as pa_reshape_and_cache does).
+ * Supported dtypes: fp32 and bf16 (one query token per sequence).
+ */
+pa_status pa_append_decode(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           void* k_cache, void* v_cache, const void* q,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, int32_t* error_word,
+                           struct CUstream_st* stream);
+
+/*
  * pa_decode over an FP8 (e4m3) cache with bf16 q and out:
  *   out[s][qh][:] = sum_i softmax_i(scale * <q, k_scale * e4m3(K_i)>) * v_scale * e4m3(V_i)[:]
  * The codes are widened to f16 in registers (exact) and multiplied on tensor

@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.pa_copy_blocks.restype = I
         L.pa_decode.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P, P]
         L.pa_decode.restype = I
+        L.pa_append_decode.argtypes = [P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I,
+                                       P, S, P, P]
+        L.pa_append_decode.restype = I
         L.pa_decode_ex.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
                                    ctypes.POINTER(_Options), P]
         L.pa_decode_ex.restype = I
@@ -439,6 +442,46 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
                             ctypes.byref(opts), _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode")
+
+
+def pa_append_decode(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_tables, context_lens,
+                     scale, out, max_context_len, workspace=None, error_word=None,
+                     stream=None) -> None:
+    """One decode step: append one new K/V row per sequence (k_new/v_new
+    [B][Hkv][D], slot_mapping int64 [B], the slot of each sequence's last row
+    or negative), then decode attention into out ([B][Hq][D])."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    _check_cuda("k_new", k_new, k_cache.dtype, 3)
+    _check_cuda("v_new", v_new, k_cache.dtype, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    _check_cuda("q", q, k_cache.dtype, 3)
+    _check_cuda("out", out, k_cache.dtype, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or tuple(k_new.shape) != (B, hkv, d) or tuple(v_new.shape) != (B, hkv, d) \
+            or slot_mapping.shape[0] != B or block_tables.shape[0] != B \
+            or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between the step's tensors and the caches")
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_append_decode(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(q), _ptr(block_tables), _ptr(context_lens),
+                                float(scale), _ptr(out), B, hq, hkv, d, bs, nb,
+                                int(block_tables.shape[1]), int(max_context_len),
+                                _dtype_code(k_cache), _ptr(workspace), ws_bytes,
+                                _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_append_decode")
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES

@@ -119,7 +119,9 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       pa_dtype act_dtype, void* workspace, size_t workspace_bytes,
                       int32_t* error_word, const pa_decode_options* options,
                       struct CUstream_st* stream, int num_queries = 1, int window = 0,
-                      const float* k_row_scales = nullptr, const float* v_row_scales = nullptr) {
+                      const float* k_row_scales = nullptr, const float* v_row_scales = nullptr,
+                      const void* k_new = nullptr, const void* v_new = nullptr,
+                      const int64_t* slot_mapping = nullptr) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
                                                                : pa::kDefaultPartition;
@@ -196,6 +198,19 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
          pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem))
         return PA_ERR_UNSUPPORTED;
 
+    // Fused append: the in-order tile-ring kernels write each sequence's new
+    // row themselves; the direct-load kernel gets a separate append first.
+    const bool append = k_new != nullptr;
+    const bool fused_append = append && kernel != PA_KERNEL_GENERIC;
+    const int row_bytes = head_dim * elem_bytes(dtype);
+    if (append && !fused_append) {
+        if (pa::launch_append(k_new, v_new, slot_mapping, const_cast<void*>(k_cache),
+                              const_cast<void*>(v_cache), num_seqs, num_kv_heads, row_bytes,
+                              block_size, num_blocks, error_word,
+                              reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeParams base{};
     base.k_cache = k_cache;
@@ -251,6 +266,12 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
         p.context_lens = context_lens + s0;
         p.num_seqs = bs_n;
+        if (fused_append) {
+            const size_t roff = static_cast<size_t>(s0) * num_kv_heads * row_bytes;
+            p.k_new = static_cast<const uint8_t*>(k_new) + roff;
+            p.v_new = static_cast<const uint8_t*>(v_new) + roff;
+            p.slot_mapping = slot_mapping + s0;
+        }
         cudaError_t err;
         if (kernel == PA_KERNEL_GENERIC) {
             err = pa::launch_decode_generic(p, dtype, st);
@@ -468,6 +489,29 @@ pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, pa_dtyp
         head_dim, block_size, num_blocks, k_scale, v_scale, error_word,
         reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_append_decode(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           void* k_cache, void* v_cache, const void* q,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                           void* workspace, size_t workspace_bytes, int32_t* error_word,
+                           struct CUstream_st* stream) {
+    if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0) {
+        if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+        if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+            !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+            return PA_ERR_INVALID_ARG;
+        if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    }
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.f, 1.f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
+                       workspace_bytes, error_word, nullptr, stream, 1, 0, nullptr, nullptr,
+                       k_new, v_new, slot_mapping);
 }
 
 pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -400,6 +400,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int cur_bad = __any_sync(0xffffffffu, bad_lane) ? 1 : 0;
                 const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;
                 if (cur_bad && lane == 0) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
+                // Fused append: the item holding the sequence's last row writes
+                // this KV head's new K and V rows into their slot before the
+                // tile that holds them is loaded (the slot must be that row's).
+                const long long new_slot =
+                    (p.k_new != nullptr && hi == cur.w) ? __ldg(p.slot_mapping + cur.x) : -1;
+                const int new_tile = (cur.w - 1 - lo) / kTileRows;
                 // The item's tiles are padded with data-less slots up to a multiple
                 // of W, so that every item starts at a stream index divisible by W
                 // and warp w always takes tiles w, w + W, ... of the item: the
@@ -411,6 +417,27 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const bool data = tt < ntiles && !cur_bad;
                     const int stage = t % STAGES;
                     const uint32_t fb = smem_addr(&full[stage]);
+                    if (new_slot >= 0 && tt == new_tile && !cur_bad) {
+                        const int r = cur.w - 1;                  // the new row
+                        const int blk = ids[r / bs - b0];
+                        if (new_slot == static_cast<long long>(blk) * bs + r % bs) {
+                            constexpr int kChunks = D * static_cast<int>(sizeof(T)) / 16;
+                            const size_t src = (static_cast<size_t>(cur.x) * p.num_kv_heads + cur.y) * kChunks;
+                            const size_t dst = ((static_cast<size_t>(blk) * p.num_kv_heads + cur.y) * bs + r % bs) * kChunks;
+                            for (int i = lane; i < 2 * kChunks; i += 32) {
+                                const bool v = i >= kChunks;
+                                const int ch = v ? i - kChunks : i;
+                                const uint4 x = __ldg(static_cast<const uint4*>(v ? p.v_new : p.k_new) + src + ch);
+                                static_cast<uint4*>(const_cast<void*>(v ? p.v_cache : p.k_cache))[dst + ch] = x;
+                            }
+                            // The generic-proxy writes are visible to this
+                            // warp's next TMA loads (the async proxy).
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                        } else if (lane == 0) {
+                            raise_error(p.error_word, PA_DEVERR_SLOT);
+                        }
+                        __syncwarp();
+                    }
                     if (lane == 0) {
                         if (t >= STAGES && !mbar_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
                             ok = false;

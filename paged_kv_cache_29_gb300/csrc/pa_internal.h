@@ -22,6 +22,12 @@ struct DecodeParams {
     float* part_o;                 // [B][Hq][max_parts][D] unnormalised partial outputs
     float* part_ml;                // [B][Hq][max_parts][2] (running max in log2 units, sum)
     int4* items;                   // work items (sequence, KV head, partition, context length)
+    // Fused append (pa_append_decode; in-order stream kernels): each
+    // sequence's new K and V rows [B][Hkv][D] (cache dtype) and their slots,
+    // written by the CTA that loads them; null otherwise.
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slot_mapping;
     int32_t* error_word;           // nullable
     float scale_log2;              // scale * log2(e): scores are kept in base 2
     float k_scale;                 // FP8 caches: K value = k_scale * e4m3(code) (else 1)

@@ -130,6 +130,9 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         const int b = n > 0 ? plan_bucket(span % P, P) : -1;
         if (b >= 0) atomicAdd(&bcount[b], 1);
         if (n == 0 && s % C == c) {
+            // A fused append for an empty sequence has no row to go to.
+            if (p.slot_mapping != nullptr && __ldg(p.slot_mapping + s) >= 0)
+                raise_error(p.error_word, PA_DEVERR_SLOT);
             // the sequence's num_queries output rows
             const int chunks =
                 p.num_queries * p.num_heads * p.head_dim * static_cast<int>(sizeof(T)) / 16;
