@@ -340,10 +340,11 @@ def run_native(args) -> dict | None:
             pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
                          workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
 
-    # One decode step. bf16/fp32 caches with one query token per sequence and
-    # no window go through pa_append_decode (the decode kernel writes the new
-    # rows itself); the other workloads append, then decode.
-    fused_step = not (int8 or fp8) and Qn == 1 and step.window == 0
+    # One decode step. Workloads with one query token per sequence and no
+    # window go through the fused call (pa_append_decode and its FP8/INT8
+    # forms: the decode kernel writes, or quantises, the new rows itself); the
+    # others append, then decode.
+    fused_step = Qn == 1 and step.window == 0
 
     def do_unfused_step(st=None):
         do_append(st)
@@ -352,9 +353,18 @@ def run_native(args) -> dict | None:
     def do_step(st=None):
         if not fused_step:
             do_unfused_step(st)
-            return
-        pa.pa_append_decode(k_new, v_new, slots, k_cache, v_cache, q, tables, lens, step.scale,
-                            out, mcl, workspace=workspace, error_word=err, stream=st)
+        elif int8:
+            pa.pa_append_decode_int8(k_new, v_new, slots, k_cache, v_cache, k_rs, v_rs, q, tables,
+                                     lens, step.scale, out, mcl, workspace=workspace,
+                                     error_word=err, stream=st)
+        elif fp8:
+            pa.pa_append_decode_fp8(k_new, v_new, slots, k_cache, v_cache, q, tables, lens,
+                                    step.scale, out, mcl, step.k_scale, step.v_scale,
+                                    workspace=workspace, error_word=err, stream=st)
+        else:
+            pa.pa_append_decode(k_new, v_new, slots, k_cache, v_cache, q, tables, lens,
+                                step.scale, out, mcl, workspace=workspace, error_word=err,
+                                stream=st)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -503,8 +513,8 @@ def run_native(args) -> dict | None:
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),
             "max_context_len": mcl, "partition_size": 512, "kernel": kernel_name,
-            "step": ("pa_append_decode (new rows written by the decode kernel)" if fused_step
-                     else "pa_reshape_and_cache + decode call"),
+            "step": ("fused append + decode call (new rows written by the decode kernel)"
+                     if fused_step else "append call + decode call"),
             "l2": "between timed steps a 256 MiB buffer is written, then another 256 MiB read (L2 clean, holding none of the step's data); attended K/V also exceed L2",
             "parallelism": f"replicas x{world} (independent batches per GPU)",
         },

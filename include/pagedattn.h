@@ -246,6 +246,32 @@ pa_status pa_append_decode(const void* k_new, const void* v_new, const int64_t* 
                            struct CUstream_st* stream);
 
 /*
+ * pa_append_decode over an FP8 (e4m3) cache (pa_reshape_and_cache_fp8 of one
+ * bf16 row per sequence, then pa_decode_fp8) and over an INT8 cache with row
+ * scales (pa_reshape_and_cache_int8, then pa_decode_int8). The rows are
+ * quantised by the decode kernel with the append kernels' arithmetic (codes
+ * and scales bit-identical to theirs) before the tiles that hold them load.
+ * k_new, v_new: bf16 [num_seqs][num_kv_heads][head_dim]; slot_mapping as in
+ * pa_append_decode; every other argument as the decode call.
+ */
+pa_status pa_append_decode_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               void* k_cache, void* v_cache, float k_scale, float v_scale,
+                               const void* q, const int32_t* block_tables,
+                               const int32_t* context_lens, float scale, void* out, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, int max_blocks_per_seq, int max_context_len,
+                               void* workspace, size_t workspace_bytes, int32_t* error_word,
+                               struct CUstream_st* stream);
+pa_status pa_append_decode_int8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                const void* q, const int32_t* block_tables,
+                                const int32_t* context_lens, float scale, void* out, int num_seqs,
+                                int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, int max_blocks_per_seq, int max_context_len,
+                                void* workspace, size_t workspace_bytes, int32_t* error_word,
+                                struct CUstream_st* stream);
+
+/*
  * pa_decode over an FP8 (e4m3) cache with bf16 q and out:
  *   out[s][qh][:] = sum_i softmax_i(scale * <q, k_scale * e4m3(K_i)>) * v_scale * e4m3(V_i)[:]
  * The codes are widened to f16 in registers (exact) and multiplied on tensor

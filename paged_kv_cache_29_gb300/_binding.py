@@ -81,6 +81,12 @@ def lib() -> ctypes.CDLL:
         L.pa_append_decode.argtypes = [P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I,
                                        P, S, P, P]
         L.pa_append_decode.restype = I
+        L.pa_append_decode_fp8.argtypes = [P, P, P, P, P, F, F, P, P, P, F, P, I, I, I, I, I, I, I,
+                                           I, P, S, P, P]
+        L.pa_append_decode_fp8.restype = I
+        L.pa_append_decode_int8.argtypes = [P, P, P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I,
+                                            I, I, P, S, P, P]
+        L.pa_append_decode_int8.restype = I
         L.pa_decode_ex.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
                                    ctypes.POINTER(_Options), P]
         L.pa_decode_ex.restype = I
@@ -482,6 +488,78 @@ def pa_append_decode(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_tabl
                                 _ptr(error_word), _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_append_decode")
+
+
+def _check_step_rows(k_new, v_new, slot_mapping, q, out, block_tables, context_lens, hkv, d):
+    import torch
+    _check_cuda("k_new", k_new, torch.bfloat16, 3)
+    _check_cuda("v_new", v_new, torch.bfloat16, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int64, 1)
+    _check_cuda("q", q, torch.bfloat16, 3)
+    _check_cuda("out", out, torch.bfloat16, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(k_new.shape) != (B, hkv, d) \
+            or tuple(v_new.shape) != (B, hkv, d) or slot_mapping.shape[0] != B \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between the step's tensors and the caches")
+    return B, hq
+
+
+def pa_append_decode_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_tables,
+                         context_lens, scale, out, max_context_len, k_scale=1.0, v_scale=1.0,
+                         workspace=None, error_word=None, stream=None) -> None:
+    """One decode step over FP8 pools: quantise one new bf16 K/V row per
+    sequence into its slot (the sequence's last row), then decode."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    if _dtype_code(k_cache) != 2:
+        raise TypeError("FP8 caches are uint8 (e4m3 codes) or float8_e4m3fn")
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq = _check_step_rows(k_new, v_new, slot_mapping, q, out, block_tables, context_lens, hkv, d)
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_append_decode_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                                    _ptr(v_cache), float(k_scale), float(v_scale), _ptr(q),
+                                    _ptr(block_tables), _ptr(context_lens), float(scale),
+                                    _ptr(out), B, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+                                    int(max_context_len), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_append_decode_fp8")
+
+
+def pa_append_decode_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales, v_scales, q,
+                          block_tables, context_lens, scale, out, max_context_len,
+                          workspace=None, error_word=None, stream=None) -> None:
+    """One decode step over INT8 pools with row scales: quantise one new bf16
+    K/V row per sequence into its slot (the sequence's last row), then decode."""
+    import torch
+    _check_int8_pool(k_cache, v_cache, k_scales, v_scales)
+    if error_word is not None:
+        _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq = _check_step_rows(k_new, v_new, slot_mapping, q, out, block_tables, context_lens, hkv, d)
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_append_decode_int8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(k_scales), _ptr(v_scales), _ptr(q),
+                                     _ptr(block_tables), _ptr(context_lens), float(scale),
+                                     _ptr(out), B, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+                                     int(max_context_len), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _ptr(error_word), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_append_decode_int8")
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES

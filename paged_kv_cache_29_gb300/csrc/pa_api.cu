@@ -396,6 +396,45 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                        workspace, workspace_bytes, error_word, nullptr, stream);
 }
 
+pa_status pa_append_decode_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               void* k_cache, void* v_cache, float k_scale, float v_scale,
+                               const void* q, const int32_t* block_tables,
+                               const int32_t* context_lens, float scale, void* out, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, int max_blocks_per_seq, int max_context_len,
+                               void* workspace, size_t workspace_bytes, int32_t* error_word,
+                               struct CUstream_st* stream) {
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || k_scale == INFINITY || v_scale == INFINITY)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping || !aligned16(k_new) ||
+                         !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0))
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                       out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_DTYPE_FP8_E4M3, PA_DTYPE_BF16,
+                       workspace, workspace_bytes, error_word, nullptr, stream, 1, 0, nullptr,
+                       nullptr, k_new, v_new, slot_mapping);
+}
+
+pa_status pa_append_decode_int8(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                void* k_cache, void* v_cache, float* k_scales, float* v_scales,
+                                const void* q, const int32_t* block_tables,
+                                const int32_t* context_lens, float scale, void* out, int num_seqs,
+                                int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, int max_blocks_per_seq, int max_context_len,
+                                void* workspace, size_t workspace_bytes, int32_t* error_word,
+                                struct CUstream_st* stream) {
+    if (num_seqs > 0 && (!k_scales || !v_scales || !k_new || !v_new || !slot_mapping ||
+                         !aligned16(k_new) || !aligned16(v_new) ||
+                         (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0))
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_DTYPE_INT8, PA_DTYPE_BF16,
+                       workspace, workspace_bytes, error_word, nullptr, stream, 1, 0, k_scales,
+                       v_scales, k_new, v_new, slot_mapping);
+}
+
 pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens, float scale,
                           void* out, int num_seqs, int num_queries, int num_heads,

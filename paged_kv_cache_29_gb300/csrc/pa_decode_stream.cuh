@@ -183,8 +183,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int n_items = own_item_count(c, C, total);
             auto load_item = own_item;
             if (lane < STAGES) last_t[lane] = -1;
-            int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
+                int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
             int4 d_req2 = load_item(1);
+            int4 d_val = make_int4(-1, 0, 0, 0);   // descriptor of the requested, unchecked item
+            // Fused append: this lane's share of that item's new K and V rows,
+            // loaded at the request (used once its block ids are checked).
+            uint2 new_k = make_uint2(0u, 0u), new_v = make_uint2(0u, 0u);
             int jl = 0;                     // items whose ids were requested
             int ready = 0;                  // items whose ids landed and were checked
             int t_req = 0;                  // stream index of item jl's first tile
@@ -210,6 +214,14 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
                 t_req += share * W;
                 ++jl;
+                d_val = it;
+                if constexpr (Math::kQuantAppend) {
+                    if (p.k_new != nullptr && hi == it.w) {
+                        const size_t src = (static_cast<size_t>(it.x) * p.num_kv_heads + it.y) * (D / 4);
+                        new_k = __ldg(static_cast<const uint2*>(p.k_new) + src + lane);
+                        new_v = __ldg(static_cast<const uint2*>(p.v_new) + src + lane);
+                    }
+                }
                 d_req = d_req2;
                 d_req2 = load_item(jl + 1);
             };
@@ -226,7 +238,30 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     m[7] = bad ? 1 : 0;
                     if (bad) raise_error(p.error_word, PA_DEVERR_BLOCK_ID);
                 }
-                __syncwarp();
+                // Fused append: the item holding the sequence's last row
+                // quantises this KV head's new rows into their slot (the slot
+                // must be that row's) before any lane may load its tiles.
+                if constexpr (Math::kQuantAppend) {
+                    const int4 it = d_val;
+                    const int lo = m[2];
+                    if (p.k_new != nullptr && !bad && min(it.w, lo + P) == it.w) {
+                        const long long slot = __ldg(p.slot_mapping + it.x);
+                        if (slot >= 0) {
+                            const int r = it.w - 1;
+                            const int blk = ids[r / bs - m[3]];
+                            if (slot == static_cast<long long>(blk) * bs + r % bs) {
+                                Math::Codes::append_row(p, new_k, new_v,
+                                                        (static_cast<size_t>(blk) * p.num_kv_heads + it.y) * bs + r % bs,
+                                                        lane);
+                                // visible to this warp's next copies (the async proxy)
+                                asm volatile("fence.proxy.async.global;" ::: "memory");
+                            } else if (lane == 0) {
+                                raise_error(p.error_word, PA_DEVERR_SLOT);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
                 ready = j + 1;
             };
             bool ok = true;
@@ -406,6 +441,23 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const long long new_slot =
                     (p.k_new != nullptr && hi == cur.w) ? __ldg(p.slot_mapping + cur.x) : -1;
                 const int new_tile = (cur.w - 1 - lo) / kTileRows;
+                // The new rows, 16-byte chunks dealt over the lanes (K, then V),
+                // loaded now and stored when their tile comes up.
+                constexpr int kChunks = D * static_cast<int>(sizeof(T)) / 16;   // per row
+                constexpr int kNewPerLane = (2 * kChunks + 31) / 32;
+                uint4 new_rows[kNewPerLane];
+                if (new_slot >= 0) {
+                    const size_t src = (static_cast<size_t>(cur.x) * p.num_kv_heads + cur.y) * kChunks;
+#pragma unroll
+                    for (int u = 0; u < kNewPerLane; ++u) {
+                        const int i = lane + 32 * u;
+                        if (i < 2 * kChunks) {
+                            const bool v = i >= kChunks;
+                            new_rows[u] = __ldg(static_cast<const uint4*>(v ? p.v_new : p.k_new) + src +
+                                                (v ? i - kChunks : i));
+                        }
+                    }
+                }
                 // The item's tiles are padded with data-less slots up to a multiple
                 // of W, so that every item starts at a stream index divisible by W
                 // and warp w always takes tiles w, w + W, ... of the item: the
@@ -421,14 +473,15 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const int r = cur.w - 1;                  // the new row
                         const int blk = ids[r / bs - b0];
                         if (new_slot == static_cast<long long>(blk) * bs + r % bs) {
-                            constexpr int kChunks = D * static_cast<int>(sizeof(T)) / 16;
-                            const size_t src = (static_cast<size_t>(cur.x) * p.num_kv_heads + cur.y) * kChunks;
                             const size_t dst = ((static_cast<size_t>(blk) * p.num_kv_heads + cur.y) * bs + r % bs) * kChunks;
-                            for (int i = lane; i < 2 * kChunks; i += 32) {
-                                const bool v = i >= kChunks;
-                                const int ch = v ? i - kChunks : i;
-                                const uint4 x = __ldg(static_cast<const uint4*>(v ? p.v_new : p.k_new) + src + ch);
-                                static_cast<uint4*>(const_cast<void*>(v ? p.v_cache : p.k_cache))[dst + ch] = x;
+#pragma unroll
+                            for (int u = 0; u < kNewPerLane; ++u) {
+                                const int i = lane + 32 * u;
+                                if (i < 2 * kChunks) {
+                                    const bool v = i >= kChunks;
+                                    static_cast<uint4*>(const_cast<void*>(v ? p.v_cache : p.k_cache))
+                                        [dst + (v ? i - kChunks : i)] = new_rows[u];
+                                }
                             }
                             // The generic-proxy writes are visible to this
                             // warp's next TMA loads (the async proxy).

@@ -126,6 +126,7 @@ template <int D, int G, bool CAUSAL = false>
 struct MmaMath {
     using T = __nv_bfloat16;
     static constexpr bool kCausal = CAUSAL;
+    static constexpr bool kQuantAppend = false;   // a fused append copies rows as they are
     static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<T, D>;
     static constexpr int kSteps = D / 16;
@@ -330,6 +331,7 @@ template <typename TT, int D, int G>
 struct SimtMath {
     using T = TT;
     static constexpr bool kCausal = false;
+    static constexpr bool kQuantAppend = false;   // a fused append copies rows as they are
     static constexpr int kExtraStageBytes = 0;
     using Geom = TileGeom<T, D>;
     using E = ElemTraits<T>;

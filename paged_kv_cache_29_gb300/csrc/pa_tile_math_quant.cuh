@@ -47,6 +47,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pa_tile_math.cuh"
 
@@ -87,6 +88,20 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
 // e4m3 codes with one scale per tensor.
 struct E4m3Codes {
     static constexpr bool kRowScales = false;
+    // One new bf16 row of K and of V (D = 128; kx, vx: this lane's 4 values)
+    // quantised into cache row `row`: code = e4m3(x / scale), the division in fp32
+    // (IEEE), round to nearest even, saturating (the append kernel's rule).
+    __device__ static __forceinline__ void append_row(const DecodeParams& p, uint2 kx, uint2 vx,
+                                                      size_t row, int lane) {
+        auto enc = [](uint2 x, float sc) -> uint32_t {
+            const float2 a = make_float2(__fdiv_rn(bf16_lo(x.x), sc), __fdiv_rn(bf16_hi(x.x), sc));
+            const float2 b = make_float2(__fdiv_rn(bf16_lo(x.y), sc), __fdiv_rn(bf16_hi(x.y), sc));
+            return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3)) |
+                   (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3)) << 16);
+        };
+        static_cast<uint32_t*>(const_cast<void*>(p.k_cache))[row * 32 + lane] = enc(kx, p.k_scale);
+        static_cast<uint32_t*>(const_cast<void*>(p.v_cache))[row * 32 + lane] = enc(vx, p.v_scale);
+    }
     // Four codes -> two f16x2 registers (the low byte of each pair becomes
     // the low half).
     __device__ static __forceinline__ void widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -102,6 +117,35 @@ struct E4m3Codes {
 // int8 codes with one scale per (row, KV head).
 struct S8Codes {
     static constexpr bool kRowScales = true;
+    // One new bf16 row of K and of V (D = 128; kx, vx: this lane's 4 values)
+    // quantised into cache row `row` with its scale: scale = max|x| / 127, code = x /
+    // scale rounded to nearest even, clamped to [-127, 127], both divisions
+    // in fp32 (IEEE); an all-zero row gets scale 0 and codes 0 (the append
+    // kernel's rule).
+    __device__ static __forceinline__ void append_row(const DecodeParams& p, uint2 kx, uint2 vx,
+                                                      size_t row, int lane) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint2 w = which ? vx : kx;
+            const float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float scale = __fdiv_rn(amax, 127.0f);
+            uint32_t codes = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int c = 0;
+                if (scale != 0.f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], scale))));
+                codes |= (static_cast<uint32_t>(c) & 0xffu) << (8 * i);
+            }
+            static_cast<uint32_t*>(const_cast<void*>(which ? p.v_cache : p.k_cache))[row * 32 + lane] = codes;
+            if (lane == 0) const_cast<float*>(which ? p.v_row_scales : p.k_row_scales)[row] = scale;
+        }
+    }
     __device__ static __forceinline__ void widen(uint32_t w, uint32_t& lo, uint32_t& hi) {
         const uint32_t t = w ^ 0x80808080u;
         const uint32_t a = prmt(t, 0x64646464u, 0x4140u);   // (t.b0, 0x64, t.b1, 0x64)
@@ -112,11 +156,14 @@ struct S8Codes {
     }
 };
 
-template <int D, int G, class Codes>
+template <int D, int G, class CodesT>
 struct QuantMmaMath {
     using T = __nv_bfloat16;                    // q and out
     using Geom = TileGeom<uint8_t, D>;
+    using Codes = CodesT;
     static constexpr bool kCausal = false;
+    // The fused append quantises new rows with Codes::append_row.
+    static constexpr bool kQuantAppend = true;
     static_assert(D == 128, "one 128-byte row of codes per token");
     static_assert(G >= 1 && G <= 8, "the MMA N dimension holds at most 8 query heads");
     static constexpr int kSteps = D / 16;

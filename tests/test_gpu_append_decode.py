@@ -100,3 +100,89 @@ def test_slot_of_another_row_is_flagged_and_not_written():
     _, _, out_ref = oracle_reference(ok)
     keep = [0, 2, 4]
     assert max_abs(fused.result()[keep], out_ref[keep]) <= TOL["bf16"]
+
+
+def _u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _quant_step_tensors(step):
+    from gpu_helpers import to_torch
+    t = dict(q=to_torch(step.q, "bf16"), k_new=to_torch(step.k_new, "bf16"),
+             v_new=to_torch(step.v_new, "bf16"), slots=to_torch(step.slot_mapping),
+             tables=to_torch(step.block_tables), lens=to_torch(step.context_lens),
+             k=_u8(step.k_cache), v=_u8(step.v_cache),
+             err=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    t["out"] = torch.full_like(t["q"], float("nan"))
+    if step.cache_dtype == "int8":
+        t["ks"], t["vs"] = _u8(step.k_row_scales), _u8(step.v_row_scales)
+    return t
+
+
+def _poison_quant(step):
+    """NaN codes (FP8) or NaN scales (INT8) in the slots the step appends to."""
+    bs = step.block_size
+    k, v = step.k_cache.copy(), step.v_cache.copy()
+    extra = {}
+    if step.cache_dtype == "int8":
+        ks, vs = step.k_row_scales.copy(), step.v_row_scales.copy()
+    for slot in step.slot_mapping:
+        if slot >= 0:
+            if step.cache_dtype == "fp8":
+                k[slot // bs, :, slot % bs, :] = 0x7F
+                v[slot // bs, :, slot % bs, :] = 0xFF
+            else:
+                ks[slot // bs, :, slot % bs] = np.nan
+                vs[slot // bs, :, slot % bs] = np.nan
+    if step.cache_dtype == "int8":
+        extra = dict(k_row_scales=ks, v_row_scales=vs)
+    return dataclasses.replace(step, k_cache=k, v_cache=v, **extra)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2)])
+def test_quantised_fused_step_equals_append_then_decode(fmt, hq, hkv):
+    import oracle
+    step = _poison_quant(wl.build_step(f"q{fmt}", LENS, hq, hkv, 128, cache_dtype=fmt,
+                                       seed=hq + hkv))
+    ksc, vsc = (0.75, 1.5) if fmt == "fp8" else (1.0, 1.0)
+    fused, two = _quant_step_tensors(step), _quant_step_tensors(step)
+    if fmt == "fp8":
+        pa.pa_append_decode_fp8(fused["k_new"], fused["v_new"], fused["slots"], fused["k"],
+                                fused["v"], fused["q"], fused["tables"], fused["lens"],
+                                step.scale, fused["out"], step.max_context_len, ksc, vsc,
+                                error_word=fused["err"])
+        pa.pa_reshape_and_cache_fp8(two["k_new"], two["v_new"], two["slots"], two["k"], two["v"],
+                                    ksc, vsc, error_word=two["err"])
+        pa.pa_decode_fp8(two["q"], two["k"], two["v"], two["tables"], two["lens"], step.scale,
+                         two["out"], step.max_context_len, ksc, vsc, error_word=two["err"])
+        k, v = step.k_cache.copy(), step.v_cache.copy()
+        oracle.append_fp8(step.k_new, step.v_new, step.slot_mapping, k, v, ksc, vsc)
+        want = oracle.decode_kv(step.q, k, v, step.block_tables, step.context_lens, step.scale,
+                                ksc, vsc)
+        refs = [("k", k), ("v", v)]
+    else:
+        pa.pa_append_decode_int8(fused["k_new"], fused["v_new"], fused["slots"], fused["k"],
+                                 fused["v"], fused["ks"], fused["vs"], fused["q"],
+                                 fused["tables"], fused["lens"], step.scale, fused["out"],
+                                 step.max_context_len, error_word=fused["err"])
+        pa.pa_reshape_and_cache_int8(two["k_new"], two["v_new"], two["slots"], two["k"], two["v"],
+                                     two["ks"], two["vs"], error_word=two["err"])
+        pa.pa_decode_int8(two["q"], two["k"], two["v"], two["ks"], two["vs"], two["tables"],
+                          two["lens"], step.scale, two["out"], step.max_context_len,
+                          error_word=two["err"])
+        k, v = step.k_cache.copy(), step.v_cache.copy()
+        ks, vs = step.k_row_scales.copy(), step.v_row_scales.copy()
+        oracle.append_int8(step.k_new, step.v_new, step.slot_mapping, k, v, ks, vs)
+        want = oracle.decode_int8(step.q, k, v, ks, vs, step.block_tables, step.context_lens,
+                                  step.scale)
+        refs = [("k", k), ("v", v), ("ks", ks), ("vs", vs)]
+    torch.cuda.synchronize()
+    assert int(fused["err"].item()) == 0 and int(two["err"].item()) == 0
+    for name, ref in refs:
+        got = fused[name].cpu().numpy()
+        np.testing.assert_array_equal(got.view(np.uint8), two[name].cpu().numpy().view(np.uint8))
+        np.testing.assert_array_equal(got.view(np.uint8), np.ascontiguousarray(ref).view(np.uint8))
+    np.testing.assert_array_equal(from_torch(fused["out"]), from_torch(two["out"]))
+    got = wl.as_f32(from_torch(fused["out"]), "bf16").astype(np.float64)
+    assert max_abs(got, want) <= TOL["bf16"]
