@@ -14,7 +14,10 @@
 // [block][kv_head][block_size][head_dim] pool) into the next ring stage. Row i
 // of a sequence is row (i % block_size) of block block_tables[s][i /
 // block_size]: the paged gather of "MLSys Engineer -- Inference Systems Q&A",
-// Q1.
+// Q1. Stages are refilled in stream order, or per consumer warp
+// (PER_WARP_ISSUE, below). With a fused append (pa_append_decode) the item
+// holding a sequence's last row also writes (or quantises) that KV head's new
+// K/V row into its slot before the tile holding it is loaded.
 //
 // Consumer warps: the CTA's tiles are numbered in stream order; tile t lives
 // in stage t % STAGES and is consumed by warp t % W (STAGES is a multiple of
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__((W + 1) * 32, MIN_CTAS)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     static_assert(STAGES % W == 0, "each ring stage must belong to exactly one consumer warp");
+    static_assert(STAGES <= 32 && W <= 32, "the producer warp keeps one lane per stage and per consumer warp");
     using T = typename Math::T;
     using Geom = typename Math::Geom;
     using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes, Math::kExtraStageBytes,
@@ -183,7 +187,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int n_items = own_item_count(c, C, total);
             auto load_item = own_item;
             if (lane < STAGES) last_t[lane] = -1;
-                int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
+            int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
             int4 d_req2 = load_item(1);
             int4 d_val = make_int4(-1, 0, 0, 0);   // descriptor of the requested, unchecked item
             // Fused append: this lane's share of that item's new K and V rows,
