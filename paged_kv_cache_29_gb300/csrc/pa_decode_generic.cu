@@ -240,17 +240,29 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
                 }
             }
         }
-        float* st = sm + warp * (D + 2);
-        if (lane == 0) {
-            st[0] = M;
-            st[1] = L;
-        }
+        if (nw == 1) {
+            // One warp merged every partition: store from its registers (the
+            // same values the cross-warp merge below would give: 2^0 = 1).
+            T* out = static_cast<T*>(p.out) + row * D;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int d = lane + 32 * e;
-            if (d < D) st[2 + d] = acc[e];
+            for (int e = 0; e < E; ++e) {
+                const int d = lane + 32 * e;
+                if (d < D) ElemTraits<T>::store(out + d, acc[e] / L);
+            }
+        } else {
+            float* st = sm + warp * (D + 2);
+            if (lane == 0) {
+                st[0] = M;
+                st[1] = L;
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int d = lane + 32 * e;
+                if (d < D) st[2 + d] = acc[e];
+            }
         }
     }
+    if (nw == 1) return;                       // the same for every thread of the CTA
     __syncthreads();
     float M = -INFINITY;
     for (int w = 0; w < nw; ++w) M = fmaxf(M, sm[w * (D + 2)]);
