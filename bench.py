@@ -19,9 +19,9 @@ One JSON line is printed by rank 0. `value` is the step's algorithmic bytes
 lengths used, the append's reads and writes) over the step time, in GB/s.
 `roofline` covers the attention call (decode + merge kernels) against the
 measured HBM copy bandwidth. `e2e` repeats the measurement through the same
-public API with the step's per-step inputs copied from pinned host memory and
-the output copied back inside the timed region (the KV pool stays resident:
-it is the cache). `cpu_baseline` times the fp64 oracle on a bounded sample of
+public API with the step's per-step inputs copied from pinned host memory (one
+packed buffer, one copy) and the output copied back inside the timed region
+(the KV pool stays resident: it is the cache). `cpu_baseline` times the fp64 oracle on a bounded sample of
 the same workload on the host's cores.
 
 --impl reference times the oracle itself (the CPU baseline) in the same JSON
@@ -101,6 +101,30 @@ def profiled_traffic(workload: str, kernel: str) -> float | None:
         return float(vals["dram_bytes_per_call"])
     except (KeyError, ValueError):
         return None
+
+
+def packed_buffer(arrays, pin=False, storage=None):
+    """numpy arrays back to back in one byte tensor (each region 256-byte
+    aligned): returns the byte tensor and a typed view per array. With
+    `storage` the views are cut from that tensor (same layout), else a host
+    tensor is made (pinned if asked) holding the arrays' bytes."""
+    import torch
+    offs, off = [], 0
+    for a in arrays:
+        off = (off + 255) // 256 * 256
+        offs.append(off)
+        off += a.nbytes
+    if storage is None:
+        storage = torch.empty(off, dtype=torch.uint8, pin_memory=pin)
+        for a, o in zip(arrays, offs):
+            raw = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+            storage[o:o + raw.size] = torch.from_numpy(raw)
+    views = []
+    for a, o in zip(arrays, offs):
+        tdt = {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.int64): torch.int64,
+               np.dtype(np.int32): torch.int32, np.dtype(np.float32): torch.float32}[a.dtype]
+        views.append(storage[o:o + a.nbytes].view(tdt).view(a.shape))
+    return storage, views
 
 
 def _quick_step_seconds(run, flush) -> float:
@@ -286,11 +310,17 @@ def run_native(args) -> dict | None:
             t = t.view(torch.bfloat16)
         return t.to(dev)
 
-    q, k_new, v_new = up(step.q), up(step.k_new), up(step.v_new)
+    # A step's inputs (q, the new rows, slots, block tables, lengths) live in
+    # one device buffer, 256-byte-aligned regions, so that the end-to-end step
+    # moves them from one pinned host buffer with a single copy.
+    step_inputs = [step.q, step.k_new, step.v_new, step.slot_mapping, step.block_tables,
+                   step.context_lens]
+    in_host, _ = packed_buffer(step_inputs, pin=True)
+    in_dev = in_host.to(dev)
+    _, (q, k_new, v_new, slots, tables, lens) = packed_buffer(step_inputs, storage=in_dev)
     k_cache, v_cache = up(step.k_cache), up(step.v_cache)
     if int8:
         k_rs, v_rs = up(step.k_row_scales), up(step.v_row_scales)
-    slots, tables, lens = up(step.slot_mapping), up(step.block_tables), up(step.context_lens)
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     mcl = step.max_context_len
@@ -428,22 +458,14 @@ def run_native(args) -> dict | None:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
 
     # ---- end to end through the public API with host buffers --------------
-    pin = {name: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-           for name, a in (("q", step.q), ("k_new", step.k_new), ("v_new", step.v_new),
-                           ("slots", step.slot_mapping), ("tables", step.block_tables),
-                           ("lens", step.context_lens))}
-    if step.act_dtype == "bf16":
-        for name in ("q", "k_new", "v_new"):
-            pin[name] = pin[name].view(torch.bfloat16)
+    # The step's inputs come from one pinned host buffer (the packed layout
+    # above), the output goes back to pinned memory.
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dsts = {"q": q, "k_new": k_new, "v_new": v_new, "slots": slots, "tables": tables,
-            "lens": lens}
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    h2d = in_host.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for name, t in pin.items():
-            dsts[name].copy_(t, non_blocking=True)
+        in_dev.copy_(in_host, non_blocking=True)
         do_step()
         out_host.copy_(out, non_blocking=True)
 
@@ -545,6 +567,8 @@ def run_native(args) -> dict | None:
             "ms_per_step": round(e2e_total / K, 5),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "transfers": "inputs: one copy of a packed pinned buffer (q, new K/V rows, slots, "
+                         "block tables, lengths); output: one copy to pinned memory",
         },
         "gpu_launches": (launches_per_step - (1 if fused_step else 0)) * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
