@@ -186,3 +186,97 @@ def test_quantised_fused_step_equals_append_then_decode(fmt, hq, hkv):
     np.testing.assert_array_equal(from_torch(fused["out"]), from_torch(two["out"]))
     got = wl.as_f32(from_torch(fused["out"]), "bf16").astype(np.float64)
     assert max_abs(got, want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["8b_gqa", "7b_mha", "long_skew", "prefix_shared"])
+def test_fused_step_on_full_workloads(name):
+    """The benchmarked workloads at full size: the pools after the fused step
+    equal the oracle's append bit for bit, the output is within tolerance of
+    the oracle and bitwise equal to the two-call step."""
+    step = wl.make(name)
+    k_ref, v_ref, out_ref = oracle_reference(step)
+    fused, two = _fused(step), _two_calls(step)
+    assert fused.error_word() == 0
+    np.testing.assert_array_equal(from_torch(fused.k_cache), k_ref)
+    np.testing.assert_array_equal(from_torch(fused.v_cache), v_ref)
+    np.testing.assert_array_equal(from_torch(fused.out), from_torch(two.out))
+    assert max_abs(fused.result(), out_ref) <= TOL[step.cache_dtype]
+
+
+def test_fused_steps_in_a_row_follow_the_oracle():
+    """Four decode steps in a row through pa_append_decode: every step appends
+    one row per sequence (crossing block boundaries) and attends to all."""
+    import oracle
+    from paged_kv_cache_29_gb300.block_manager import BlockManager
+    rng = np.random.default_rng(11)
+    hq, hkv, d, bs, nb = 32, 8, 128, 16, 160
+    lens0 = [14, 15, 16, 511, 1023]
+    mgr = BlockManager(nb, bs, free_order=rng.permutation(nb), prefix_caching=False)
+    for s, n in enumerate(lens0):
+        mgr.admit(f"s{s}", [0] * n)
+    k = wl.to_cache_dtype(rng.standard_normal((nb, hkv, bs, d), dtype=np.float32), "bf16")
+    v = wl.to_cache_dtype(rng.standard_normal((nb, hkv, bs, d), dtype=np.float32), "bf16")
+    kd = torch.from_numpy(k.copy()).view(torch.bfloat16).cuda()
+    vd = torch.from_numpy(v.copy()).view(torch.bfloat16).cuda()
+    B = len(lens0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(4):
+        slots = np.array([mgr.append(f"s{s}", 0).slot for s in range(B)], np.int64)
+        lens = np.array([mgr.num_tokens(f"s{s}") for s in range(B)], np.int32)
+        bt = np.full((B, 72), -1, np.int32)
+        for s in range(B):
+            t = mgr.block_table(f"s{s}")
+            bt[s, :len(t)] = t
+        q = wl.to_cache_dtype(rng.standard_normal((B, hq, d), dtype=np.float32), "bf16")
+        kn = wl.to_cache_dtype(rng.standard_normal((B, hkv, d), dtype=np.float32), "bf16")
+        vn = wl.to_cache_dtype(rng.standard_normal((B, hkv, d), dtype=np.float32), "bf16")
+        oracle.append(kn, vn, slots, k, v)
+        ref = oracle.decode(q, k, v, bt, lens, 1 / np.sqrt(d))
+        dq = torch.from_numpy(q).view(torch.bfloat16).cuda()
+        out = torch.empty_like(dq)
+        pa.pa_append_decode(torch.from_numpy(kn).view(torch.bfloat16).cuda(),
+                            torch.from_numpy(vn).view(torch.bfloat16).cuda(),
+                            torch.from_numpy(slots).cuda(), kd, vd, dq,
+                            torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda(),
+                            1 / np.sqrt(d), out, int(lens.max()), error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
+        assert max_abs(got, ref) <= TOL["bf16"]
+        assert np.array_equal(from_torch(kd), k) and np.array_equal(from_torch(vd), v)
+
+
+@pytest.mark.parametrize("name", ["8b_gqa_fp8", "8b_gqa_int8"])
+def test_quantised_fused_step_on_full_workloads(name):
+    """The benchmarked 8-bit workloads at full size: codes (and row scales)
+    after the fused step equal the two-call step's bit for bit, and so does
+    the output."""
+    step = wl.make(name)
+    fused, two = _quant_step_tensors(step), _quant_step_tensors(step)
+    if step.cache_dtype == "fp8":
+        pa.pa_append_decode_fp8(fused["k_new"], fused["v_new"], fused["slots"], fused["k"],
+                                fused["v"], fused["q"], fused["tables"], fused["lens"],
+                                step.scale, fused["out"], step.max_context_len, step.k_scale,
+                                step.v_scale, error_word=fused["err"])
+        pa.pa_reshape_and_cache_fp8(two["k_new"], two["v_new"], two["slots"], two["k"], two["v"],
+                                    step.k_scale, step.v_scale, error_word=two["err"])
+        pa.pa_decode_fp8(two["q"], two["k"], two["v"], two["tables"], two["lens"], step.scale,
+                         two["out"], step.max_context_len, step.k_scale, step.v_scale,
+                         error_word=two["err"])
+        names = ["k", "v"]
+    else:
+        pa.pa_append_decode_int8(fused["k_new"], fused["v_new"], fused["slots"], fused["k"],
+                                 fused["v"], fused["ks"], fused["vs"], fused["q"],
+                                 fused["tables"], fused["lens"], step.scale, fused["out"],
+                                 step.max_context_len, error_word=fused["err"])
+        pa.pa_reshape_and_cache_int8(two["k_new"], two["v_new"], two["slots"], two["k"], two["v"],
+                                     two["ks"], two["vs"], error_word=two["err"])
+        pa.pa_decode_int8(two["q"], two["k"], two["v"], two["ks"], two["vs"], two["tables"],
+                          two["lens"], step.scale, two["out"], step.max_context_len,
+                          error_word=two["err"])
+        names = ["k", "v", "ks", "vs"]
+    torch.cuda.synchronize()
+    assert int(fused["err"].item()) == 0 and int(two["err"].item()) == 0
+    for n in names:
+        assert torch.equal(fused[n].view(torch.uint8), two[n].view(torch.uint8)), n
+    np.testing.assert_array_equal(from_torch(fused["out"]), from_torch(two["out"]))
