@@ -1,0 +1,34 @@
+"""bench.py's host-side pieces on the CPU: the packed layout of a step's
+inputs (one host buffer, one copy per end-to-end step) holds every array
+unchanged, 256-byte aligned, and the same layout cut from another buffer
+gives the same views."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from paged_kv_cache_29_gb300 import workloads as wl
+
+
+def _host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b_gqa_mq2"])
+def test_packed_inputs_round_trip(name):
+    step = wl.make(name)
+    arrays = [step.q, step.k_new, step.v_new, step.slot_mapping, step.block_tables,
+              step.context_lens]
+    buf, views = bench.packed_buffer(arrays)
+    assert buf.dtype == torch.uint8 and buf.numel() >= sum(a.nbytes for a in arrays)
+    base = buf.data_ptr()
+    for a, v in zip(arrays, views):
+        assert (v.data_ptr() - base) % 256 == 0
+        assert tuple(v.shape) == a.shape
+        np.testing.assert_array_equal(_host(v), a)
+    # The same layout over a copy (as the device buffer is cut) reads the same.
+    _, again = bench.packed_buffer(arrays, storage=buf.clone())
+    for a, v in zip(arrays, again):
+        np.testing.assert_array_equal(_host(v), a)
