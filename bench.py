@@ -548,6 +548,9 @@ def run_native(args) -> dict | None:
                               "decode_call": round(decode_avg, 5),
                               "unfused_step": round(sum(unfused_ms) / K, 5)},
         "eager_ms_per_step": round(sum(eager_ms) / K, 5),
+        "step_ms_spread": {"median": round(float(np.median(step_ms)), 5),
+                           "p10": round(float(np.percentile(step_ms, 10)), 5),
+                           "p90": round(float(np.percentile(step_ms, 90)), 5)},
         "timing": "CUDA graph replay of one step per timed iteration; eager_ms_per_step "
                   "is the same step launched through the Python binding",
         "roofline": {
