@@ -128,3 +128,34 @@ def test_noalloc_rejects_oversize_requests_on_the_host(lib):
     assert rc == pa.PA_ERR_WORKSPACE
     # The 8B GQA decode batch (128 sequences up to ~8K rows) fits.
     assert lib.pa_decode_workspace_size(128, 32, 128, 8192) <= pa.NOALLOC_SCRATCH_BYTES
+
+
+def test_fused_step_calls_reject_bad_arguments_on_the_host(lib):
+    """pa_append_decode and its FP8/INT8 forms check their extra arguments (the
+    new rows, the slots, the scales) before anything is enqueued."""
+    P = FAKE
+    common = (P, P, P, 0.1, P, 4, 8, 2, 128, 16, 10, 4, 64)   # q .. max_context_len
+    tail = (None, 0, None, None)                                # workspace, bytes, error word, stream
+    # pa_append_decode(k_new, v_new, slots, k_cache, v_cache, q, tables, lens, scale, out, B, ...)
+    ok = dict(k_new=P, v_new=P, slots=P, kc=P, vc=P)
+
+    def fused(dtype=1, **kw):
+        a = {**ok, **kw}
+        return lib.pa_append_decode(a["k_new"], a["v_new"], a["slots"], a["kc"], a["vc"],
+                                    *common, dtype, *tail)
+    assert fused(k_new=None) == pa.PA_ERR_INVALID_ARG
+    assert fused(slots=P + 4) == pa.PA_ERR_INVALID_ARG       # int64 slots, 8-byte aligned
+    assert fused(v_new=P + 8) == pa.PA_ERR_INVALID_ARG       # 16-byte aligned rows
+    assert fused(dtype=7) == pa.PA_ERR_INVALID_ARG
+    assert fused() == pa.PA_ERR_WORKSPACE                    # valid, but no workspace given
+    # pa_append_decode_fp8(..., k_scale, v_scale, q, ...): scales must be finite and > 0
+    for ks, vs in [(0.0, 1.0), (1.0, -2.0), (float("inf"), 1.0)]:
+        assert lib.pa_append_decode_fp8(P, P, P, P, P, ks, vs, *common, *tail) == \
+            pa.PA_ERR_INVALID_ARG
+    assert lib.pa_append_decode_fp8(None, P, P, P, P, 1.0, 1.0, *common, *tail) == \
+        pa.PA_ERR_INVALID_ARG
+    # pa_append_decode_int8(..., k_scales, v_scales, q, ...): the row scales are required
+    assert lib.pa_append_decode_int8(P, P, P, P, P, None, P, *common, *tail) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_append_decode_int8(P, P, None, P, P, P, P, *common, *tail) == \
+        pa.PA_ERR_INVALID_ARG
