@@ -108,3 +108,64 @@ def test_incremental_rows_match_naive_decoder():
     for t in range(g["decoded"]):
         m.append("s", 100 + t)
     assert m.num_tokens("s") == g["cache_rows"]
+
+
+def test_prefix_reuse_shares_full_blocks_only():
+    """A second request with the same prompt reuses the unbroken run of full
+    cached blocks from its start (reference counts go up, no new blocks); its
+    partly filled last block is its own."""
+    m = BlockManager(32, 4)
+    prompt = list(range(10))                     # 2 full blocks + 2 tokens
+    assert m.admit("a", prompt) == 0
+    free_before = m.num_free
+    assert m.admit("b", prompt) == 8
+    ta, tb = m.block_table("a"), m.block_table("b")
+    assert ta[:2] == tb[:2] and ta[2] != tb[2]
+    assert [m.refcount(x) for x in tb] == [2, 2, 1]
+    assert m.num_free == free_before - 1         # only the partial block is new
+    m.check()
+
+
+def test_salt_isolates_prefix_caches():
+    m = BlockManager(32, 4)
+    prompt = list(range(12))
+    m.admit("a", prompt, salt="tenant-1")
+    assert m.admit("b", prompt, salt="tenant-2") == 0
+    assert set(m.block_table("a")).isdisjoint(m.block_table("b"))
+    assert m.admit("c", prompt, salt="tenant-1") == 12
+    m.check()
+
+
+def test_chain_key_breaks_at_the_first_differing_block():
+    """Blocks match only as an unbroken run from the start: a prompt that
+    differs in block 1 reuses block 0 and nothing after it, even where a later
+    block's tokens are the same."""
+    m = BlockManager(32, 4)
+    m.admit("a", list(range(12)))
+    other = list(range(12))
+    other[5] = 99                                # block 1 differs, block 2 identical
+    assert m.admit("b", other) == 4
+    ta, tb = m.block_table("a"), m.block_table("b")
+    assert ta[0] == tb[0] and ta[1] != tb[1] and ta[2] != tb[2]
+    m.check()
+
+
+def test_released_blocks_stay_reusable_until_handed_out_again():
+    """A finished request's blocks join the LRU free queue with their keys: a
+    new identical prompt revives them; once the free queue hands a block out
+    to other data, its key is gone."""
+    m = BlockManager(4, 4)
+    prompt = list(range(8))
+    m.admit("a", prompt)
+    blocks = m.block_table("a")
+    m.release("a")
+    assert m.num_free == 4
+    assert m.admit("b", prompt) == 8              # revived from the free queue
+    assert m.block_table("b") == blocks
+    m.release("b")
+    # Allocate every block for other tokens: the cached blocks are reused and
+    # their keys evicted.
+    m.admit("c", list(range(100, 116)))
+    m.release("c")
+    assert m.admit("d", prompt) == 0
+    m.check()
