@@ -49,6 +49,8 @@ class _Options(ctypes.Structure):
 def lib() -> ctypes.CDLL:
     """The loaded library. Raises if it has not been built."""
     global _lib
+    if _lib is not None:            # loaded: no lock needed to read the reference
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -144,10 +146,26 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> int | None:
+def _current_raw_stream():
+    """A function returning torch's current CUDA stream handle as an int: the
+    raw accessor when this torch has it (no Stream object is built, ~3 us less
+    per call), else the public API."""
     import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return lambda: raw(torch.cuda.current_device())
+    return lambda: torch.cuda.current_stream().cuda_stream
+
+
+_raw_stream = None
+
+
+def _stream(stream) -> int | None:
+    global _raw_stream
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream or None
+        if _raw_stream is None:
+            _raw_stream = _current_raw_stream()
+        return _raw_stream() or None
     if isinstance(stream, int):
         return stream or None
     return stream.cuda_stream or None
