@@ -254,7 +254,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
             if (dev < pa::kMaxDevices) cached_sms[dev].store(sm_count, std::memory_order_relaxed);
         }
     }
-    const size_t es = static_cast<size_t>(elem_bytes(act_dtype));   // q and out rows
+    const size_t es = static_cast<size_t>(elem_bytes(act_dtype));   // q, out and new rows
     // Batches above kPlanMaxSeqs sequences run as consecutive launches over
     // slices of the batch; they reuse the workspace in stream order.
     for (int s0 = 0; s0 < num_seqs; s0 += pa::kPlanMaxSeqs) {
@@ -267,7 +267,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         p.context_lens = context_lens + s0;
         p.num_seqs = bs_n;
         if (fused_append) {
-            const size_t roff = static_cast<size_t>(s0) * num_kv_heads * row_bytes;
+            // New rows are in the activation dtype (bf16 over 8-bit pools).
+            const size_t roff = static_cast<size_t>(s0) * num_kv_heads * head_dim * es;
             p.k_new = static_cast<const uint8_t*>(k_new) + roff;
             p.v_new = static_cast<const uint8_t*>(v_new) + roff;
             p.slot_mapping = slot_mapping + s0;
