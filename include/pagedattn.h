@@ -185,7 +185,9 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
  * block_tables[s]), accumulated in fp32, stored in the cache dtype with
  * round-to-nearest-even.
  *
- * Long sequences are split into fixed partitions of 512 rows whose partial
+ * Long sequences are split into fixed partitions of 512 rows (1024 over the
+ * 8-bit caches of pa_decode_fp8 and pa_decode_int8: the same bytes per
+ * partition; pa_default_partition_size) whose partial
  * results (running max, sum and unnormalised output, the online-softmax state
  * of Q4 "How would you write a fused attention kernel?") are merged by a
  * second kernel. Partition boundaries and the merge order depend only on the
@@ -391,7 +393,8 @@ typedef enum pa_kernel {
 
 typedef struct pa_decode_options {
     int kernel;          /* a pa_kernel value */
-    int partition_size;  /* rows per split-K partition: a multiple of 16, 16..4096; 0 = 512 */
+    int partition_size;  /* rows per split-K partition: a multiple of 16, 16..4096;
+                            0 = pa_default_partition_size(dtype) */
 } pa_decode_options;
 
 /* pa_decode with explicit options (NULL = defaults). The workspace must be
@@ -415,6 +418,12 @@ pa_status pa_check_error_word(int32_t error_word_value);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pa_version(void);
+
+/* Rows per split-K partition the decode calls use for a cache of this type
+ * when none is requested: 512 for fp32 and bf16, 1024 for the 1-byte FP8 and
+ * INT8 caches (the same bytes per partition). 0 for a type no cache holds.
+ * pa_decode_workspace_size assumes 512, which covers both. */
+int pa_default_partition_size(pa_dtype cache_dtype);
 
 #ifdef __cplusplus
 }

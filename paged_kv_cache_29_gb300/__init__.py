@@ -28,10 +28,11 @@ from ._binding import (  # noqa: F401
     pa_reshape_and_cache,
     pa_reshape_and_cache_fp8,
     pa_reshape_and_cache_int8,
+    pa_default_partition_size,
     pa_status_string,
     pa_version,
 )
 
 __all__ = ["pa_reshape_and_cache", "pa_reshape_and_cache_int8", "pa_decode_int8", "pa_decode_window", "pa_decode_multi", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_copy_blocks", "pa_decode", "pa_decode_noalloc", "pa_append_decode", "pa_append_decode_fp8", "pa_append_decode_int8", "pa_decode_workspace_size", "pa_decode_workspace_size_multi", "pa_status_string",
-           "pa_version", "PagedAttentionError", "KERNELS", "block_manager", "workloads",
+           "pa_default_partition_size", "pa_version", "PagedAttentionError", "KERNELS", "block_manager", "workloads",
            "accounting"]

@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.pa_check_error_word.restype = I
         L.pa_version.argtypes = []
         L.pa_version.restype = I
+        L.pa_default_partition_size.argtypes = [I]
+        L.pa_default_partition_size.restype = I
         _lib = L
         return L
 
@@ -125,6 +127,15 @@ def pa_status_string(status: int) -> str:
 
 def pa_version() -> int:
     return lib().pa_version()
+
+
+def pa_default_partition_size(cache_dtype: str) -> int:
+    """Rows per split-K partition used when none is requested, for a cache
+    of this type ("f32", "bf16", "fp8" or "int8")."""
+    codes = {"f32": 0, "bf16": 1, "fp8": 2, "int8": 3}
+    if cache_dtype not in codes:
+        raise ValueError(f"unknown cache dtype {cache_dtype!r}")
+    return lib().pa_default_partition_size(codes[cache_dtype])
 
 
 def _dtype_code(t) -> int:

@@ -13,7 +13,7 @@ namespace {
 
 using pa::DecodeParams;
 
-constexpr int kVersion = 10000;   // 1.0.0
+constexpr int kVersion = 10100;   // 1.1.0
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kMaxDynamicSmem = 227 * 1024;
 
@@ -124,6 +124,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       const int64_t* slot_mapping = nullptr) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
+                          : elem_bytes(dtype) == 1             ? pa::kDefaultPartition8
                                                                : pa::kDefaultPartition;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
@@ -313,6 +314,11 @@ pa_status pa_check_error_word(int32_t error_word_value) {
 }
 
 int pa_version(void) { return kVersion; }
+
+int pa_default_partition_size(pa_dtype cache_dtype) {
+    if (!valid_decode_cache_dtype(cache_dtype)) return 0;
+    return elem_bytes(cache_dtype) == 1 ? pa::kDefaultPartition8 : pa::kDefaultPartition;
+}
 
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_heads, int head_dim,
                                    int max_context_len, int partition_size) {

@@ -113,5 +113,8 @@ __host__ __device__ inline int seq_row_base(int n, int window) {
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxDevices = 64;      // devices whose per-kernel launch set-up is cached
 constexpr int kDefaultPartition = 512;
+// 8-bit caches: twice the rows, the same bytes per partition as 512 bf16 rows
+// (fewer items, merges and partials for the same traffic).
+constexpr int kDefaultPartition8 = 1024;
 
 }  // namespace pa

@@ -58,8 +58,9 @@ LENS = {
     "every_tile_count": [16 * k + 1 for k in range(100)],
     # a single item: nearly every CTA has nothing to do
     "single_item": [17],
-    # empty sequences, partition edges (511, 512, 513) and a long sequence
-    "empty_and_edges": [0, 9000, 0, 1, 511, 512, 513, 0],
+    # empty sequences, edges of the 1024-row partitions of 8-bit caches and of
+    # 512 rows, and a long sequence
+    "empty_and_edges": [0, 9000, 0, 1, 511, 512, 513, 1023, 1024, 1025, 2047, 2049, 0],
 }
 
 

@@ -27,9 +27,18 @@ def test_status_strings_and_version(lib):
     for code in range(6):
         assert pa.pa_status_string(code)
     assert pa.pa_status_string(99) == "unknown status"
-    assert pa.pa_version() >= 10000
+    assert pa.pa_version() >= 10100
     assert lib.pa_check_error_word(0) == pa.PA_OK
     assert lib.pa_check_error_word(pa.PA_DEVERR_SLOT) == pa.PA_ERR_DEVICE_BOUNDS
+
+
+def test_default_partition_sizes():
+    # 512 rows of 2- or 4-byte elements; 1024 rows of the 1-byte 8-bit caches
+    assert [pa.pa_default_partition_size(d) for d in ("f32", "bf16", "fp8", "int8")] == \
+        [512, 512, 1024, 1024]
+    assert pa.lib().pa_default_partition_size(7) == 0
+    with pytest.raises(ValueError):
+        pa.pa_default_partition_size("f16")
 
 
 def _decode(lib, **kw):
