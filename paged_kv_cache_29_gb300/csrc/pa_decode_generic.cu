@@ -154,6 +154,9 @@ constexpr int kCombineChunk = 32;          // partitions per warp per pass (one 
 constexpr int kCombineMaxWarps = 16;
 constexpr int kCombineMaxElems = kMaxHeadDim / 32;   // output elements per lane
 constexpr int kCombineBatch = 8;           // partitions whose o rows are loaded before use
+// Query heads per CTA (one warp each) when every sequence fits one warp's
+// chunk of partitions: fewer, larger CTAs for the same per-head work.
+constexpr int kCombineHeadsPerCta = 4;
 
 // Warps used for a sequence of np partitions: warp w takes chunks w, w + nw,
 // ... of 32 consecutive partitions. Depends on np only, so a sequence's
@@ -164,14 +167,16 @@ __host__ __device__ __forceinline__ int combine_warps(int np) {
 }
 
 // One CTA per (sequence, query token, query head) of a sequence longer than
-// one partition (one query token per sequence for plain decode).
+// one partition (one query token per sequence for plain decode), or with
+// HPB > 1 (every sequence within one warp's chunk of partitions) one CTA per
+// HPB query heads, a warp each.
 // Each warp merges its chunks (lane q holds partition q's max and sum; the o
 // rows are loaded kCombineBatch partitions at a time), then the warp results
 // are merged in warp order.
-template <typename T, int E>
+template <typename T, int E, int HPB>
 __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const DecodeParams p) {
     extern __shared__ float sm[];                // [nw][2 + head_dim]
-    const int qh = blockIdx.x;
+    const int qh = HPB > 1 ? blockIdx.x * HPB + (threadIdx.x >> 5) : blockIdx.x;
     const int sq = blockIdx.y;                 // s * num_queries + query token
     const int s = sq / p.num_queries;
     // Launched as a programmatic dependent of the decode kernel, which starts
@@ -188,12 +193,12 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
     asm volatile("griddepcontrol.wait;" ::: "memory");    // the partials are the decode kernel's output
     if (!merge) return;
     const int np = (span + P - 1) / P;
-    const int nw = combine_warps(np);
+    const int nw = HPB > 1 ? 1 : combine_warps(np);
     const int D = p.head_dim;
     const size_t row = static_cast<size_t>(sq) * p.num_heads + qh;
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + row * p.max_parts;
     const float* o = p.part_o + row * p.max_parts * static_cast<size_t>(D);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = HPB > 1 ? 0 : threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < nw) {
         float M = -INFINITY, L = 0.f;
         float acc[E];
@@ -311,10 +316,14 @@ cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStr
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
     if (p.max_parts <= 1 || p.num_seqs == 0) return cudaSuccess;
     const int warps = combine_warps(p.max_parts);   // enough for the longest sequence
-    const size_t smem = static_cast<size_t>(warps) * (p.head_dim + 2) * sizeof(float);
+    // One warp per head merges every partition: several heads per CTA.
+    const bool packed = warps == 1 && kCombineHeadsPerCta > 1 &&
+                        p.num_heads % kCombineHeadsPerCta == 0;
+    const size_t smem = packed ? 0 : static_cast<size_t>(warps) * (p.head_dim + 2) * sizeof(float);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_heads, p.num_seqs * p.num_queries);
-    cfg.blockDim = dim3(32 * warps);
+    cfg.gridDim = dim3(packed ? p.num_heads / kCombineHeadsPerCta : p.num_heads,
+                       p.num_seqs * p.num_queries);
+    cfg.blockDim = dim3(packed ? 32 * kCombineHeadsPerCta : 32 * warps);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -327,9 +336,11 @@ cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t s
         using T = decltype(tag);
         // At most 16 warps x (256 + 2) floats: within the default shared-memory limit.
         auto run = [&](auto kernel) -> cudaError_t { return cudaLaunchKernelEx(&cfg, kernel, p); };
-        if (p.head_dim == 128) return run(combine_kernel<T, 4>);
-        if (p.head_dim == 64) return run(combine_kernel<T, 2>);
-        return run(combine_kernel<T, kCombineMaxElems>);
+        constexpr int H = kCombineHeadsPerCta;
+        if (p.head_dim == 128) return packed ? run(combine_kernel<T, 4, H>) : run(combine_kernel<T, 4, 1>);
+        if (p.head_dim == 64) return packed ? run(combine_kernel<T, 2, H>) : run(combine_kernel<T, 2, 1>);
+        return packed ? run(combine_kernel<T, kCombineMaxElems, H>)
+                      : run(combine_kernel<T, kCombineMaxElems, 1>);
     };
     cudaError_t err = dtype == PA_DTYPE_BF16 ? pick(__nv_bfloat16{}) : pick(float{});
     if (err != cudaSuccess) return err;
