@@ -410,6 +410,27 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_heads, int head_dim,
                                    int max_context_len, int partition_size);
 
+/*
+ * Failure test of the bounded waits (not for production use): pa_decode (or,
+ * with dtype PA_DTYPE_FP8_E4M3, pa_decode_fp8 with unit scales) where CTA 0 of
+ * the tile-ring decode kernel announces tile `withhold_tile` (>= 0) of its own
+ * stream to its consumer but neither copies it nor completes its barrier.
+ * Nothing faults and nothing waits without limit: the consumer's wait gives
+ * up after about 2 s, the kernel sets PA_DEVERR_TIMEOUT in error_word
+ * (required, device memory), its warps wind down and the call completes; the
+ * output is unspecified. The CUDA context stays usable, and a following call
+ * is exact. If CTA 0 streams fewer tiles, nothing is withheld. Returns
+ * PA_ERR_INVALID_ARG for a negative withhold_tile or a null error_word, else
+ * as pa_decode.
+ */
+pa_status pa_test_withhold_tile(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, void* out, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                                void* workspace, size_t workspace_bytes, int32_t* error_word,
+                                int withhold_tile, struct CUstream_st* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* pa_status_string(pa_status status);
 

@@ -65,6 +65,9 @@ def lib() -> ctypes.CDLL:
         L.pa_reshape_and_cache_fp8.restype = I
         L.pa_decode_fp8.argtypes = [P, P, P, P, P, F, F, F, P, I, I, I, I, I, I, I, I, P, S, P, P]
         L.pa_decode_fp8.restype = I
+        L.pa_test_withhold_tile.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
+                                            I, P]
+        L.pa_test_withhold_tile.restype = I
         L.pa_decode_multi.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, I, P, S, P, P]
         L.pa_decode_multi.restype = I
         L.pa_decode_workspace_size_multi.argtypes = [I, I, I, I, I]
@@ -277,6 +280,42 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, m
                              _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode_fp8")
+
+
+def pa_test_withhold_tile(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                          max_context_len, withhold_tile, error_word, workspace=None,
+                          stream=None) -> None:
+    """Failure test of the bounded waits: a decode call (fp32/bf16 caches, or
+    FP8 codes with unit scales) whose CTA 0 withholds tile `withhold_tile` of
+    its stream; the waiting consumer gives up after about 2 s and the kernel
+    sets PA_DEVERR_TIMEOUT in error_word. Not for production use."""
+    import torch
+    _check_cuda("k_cache", k_cache, ndim=4)
+    _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
+    code = _dtype_code(k_cache)
+    act = torch.bfloat16 if code == 2 else k_cache.dtype
+    _check_cuda("q", q, act, 3)
+    _check_cuda("out", out, act, 3)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    _check_cuda("error_word", error_word, torch.int32)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, dq = q.shape
+    if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
+            or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    if workspace is None:
+        need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda("workspace", workspace)
+    rc = lib().pa_test_withhold_tile(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d,
+                                     bs, nb, int(block_tables.shape[1]), int(max_context_len),
+                                     code, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _ptr(error_word), int(withhold_tile), _stream(stream))
+    if rc != PA_OK:
+        raise PagedAttentionError(rc, "pa_test_withhold_tile")
 
 
 def pa_decode_workspace_size_multi(num_seqs: int, num_queries: int, num_heads: int,

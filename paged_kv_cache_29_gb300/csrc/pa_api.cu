@@ -121,7 +121,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       struct CUstream_st* stream, int num_queries = 1, int window = 0,
                       const float* k_row_scales = nullptr, const float* v_row_scales = nullptr,
                       const void* k_new = nullptr, const void* v_new = nullptr,
-                      const int64_t* slot_mapping = nullptr) {
+                      const int64_t* slot_mapping = nullptr, int withhold_tile = -1) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
                           : elem_bytes(dtype) == 1             ? pa::kDefaultPartition8
@@ -225,6 +225,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     base.v_scale = v_scale;
     base.num_queries = num_queries;
     base.window = window;
+    base.withhold_tile = withhold_tile;
     base.k_row_scales = k_row_scales;
     base.v_row_scales = v_row_scales;
     base.num_heads = num_heads;
@@ -386,6 +387,23 @@ pa_status pa_decode_ex(const void* q, const void* k_cache, const void* v_cache,
                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, dtype, dtype, workspace,
                        workspace_bytes, error_word, options, stream);
+}
+
+pa_status pa_test_withhold_tile(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, void* out, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                                void* workspace, size_t workspace_bytes, int32_t* error_word,
+                                int withhold_tile, struct CUstream_st* stream) {
+    const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
+    if (withhold_tile < 0 || error_word == nullptr || (!fp8 && !valid_dtype(dtype)))
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, 1.0f, 1.0f, out,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, fp8 ? PA_DTYPE_BF16 : dtype,
+                       workspace, workspace_bytes, error_word, nullptr, stream, 1, 0, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, withhold_tile);
 }
 
 pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,

@@ -293,10 +293,13 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const int t = t0 + tt;
                         const int stage = t % STAGES;
                         if (t < STAGES || mbar_test_wait(smem_addr(&empty[stage]), ((t / STAGES) - 1) & 1)) {
-                            const bool data = tt < ntiles && !bad;
+                            // A withheld tile (failure test) gets neither copies nor
+                            // an arrival, and no wait for its copies at the end.
+                            const bool withheld = c == 0 && t == p.withhold_tile;
+                            const bool data = tt < ntiles && !bad && !withheld;
                             const uint32_t fb = smem_addr(&full[stage]);
                             stage_bad[stage] = bad;
-                            last_t[stage] = t;
+                            last_t[stage] = withheld ? -1 : t;
                             if (data) {
                                 mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
                                 const int tok = lo + kTileRows * tt;
@@ -324,7 +327,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                         "l"(p.v_row_scales + r), "r"(kHalf), "r"(fb)
                                         : "memory");
                                 }
-                            } else {
+                            } else if (!withheld) {
                                 mbar_arrive(fb);                // no data: consumers skip the slot
                             }
                             ++ci;
@@ -470,7 +473,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int span = ((ntiles + W - 1) / W) * W;
                 for (int tt = 0; tt < span; ++tt, ++t) {
                     const int tok = lo + kTileRows * tt;
-                    const bool data = tt < ntiles && !cur_bad;
+                    // A withheld tile (failure test) gets neither copies nor an
+                    // arrival, and no wait for its copies at the end.
+                    const bool withheld = c == 0 && t == p.withhold_tile;
+                    const bool data = tt < ntiles && !cur_bad && !withheld;
                     const int stage = t % STAGES;
                     const uint32_t fb = smem_addr(&full[stage]);
                     if (new_slot >= 0 && tt == new_tile && !cur_bad) {
@@ -504,7 +510,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             stage_bad[stage] = cur_bad;
                             if (data)
                                 mbar_arrive_expect_tx(fb, Geom::kStageBytes + Math::kExtraStageBytes);
-                            else
+                            else if (!withheld)
                                 mbar_arrive(fb);          // no data: consumers skip the slot
                             issued = t + 1;
                         }
@@ -553,7 +559,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // Copies still in flight must land before the CTA's shared memory
                 // is released: wait (bounded) for the last issued stages.
                 for (int u = issued > STAGES ? issued - STAGES : 0; u < issued; ++u)
-                    (void)mbar_wait(smem_addr(&full[u % STAGES]), (u / STAGES) & 1);
+                    if (!(c == 0 && u == p.withhold_tile))
+                        (void)mbar_wait(smem_addr(&full[u % STAGES]), (u / STAGES) & 1);
             }
         }
         return;

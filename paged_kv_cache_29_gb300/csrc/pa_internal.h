@@ -46,6 +46,10 @@ struct DecodeParams {
     int context_cap;               // min(max_context_len, max_blocks_per_seq * block_size)
     int partition_size;
     int max_parts;                 // ceil(max_context_len / partition_size), >= 1
+    // Failure test only (-1 otherwise): the tile-ring kernels' CTA 0 announces
+    // its stream tile withhold_tile without copying it or completing its
+    // barrier, so the consumer's bounded wait expires.
+    int withhold_tile = -1;
 };
 
 // Launch result: cudaSuccess or the launch error.

@@ -32,6 +32,14 @@ def test_status_strings_and_version(lib):
     assert lib.pa_check_error_word(pa.PA_DEVERR_SLOT) == pa.PA_ERR_DEVICE_BOUNDS
 
 
+def test_withhold_hook_argument_checks(lib):
+    # Checked on the host before anything is enqueued (no GPU needed).
+    P = None
+    args = [P, P, P, P, P, 1.0, P, 1, 1, 1, 16, 16, 1, 1, 16, 1, P, 0]   # bf16
+    assert lib.pa_test_withhold_tile(*args, P, -1, P) == pa.PA_ERR_INVALID_ARG   # negative tile
+    assert lib.pa_test_withhold_tile(*args, P, 3, P) == pa.PA_ERR_INVALID_ARG    # no error word
+
+
 def test_default_partition_sizes():
     # 512 rows of 2- or 4-byte elements; 1024 rows of the 1-byte 8-bit caches
     assert [pa.pa_default_partition_size(d) for d in ("f32", "bf16", "fp8", "int8")] == \
