@@ -55,6 +55,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 COPY_PAIRS = 4096
+# Bound on every collective of a multi-rank run (the final barrier and the
+# max/sum over ranks): a rank that died makes the others fail, not wait.
+PG_TIMEOUT_S = 300
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "pa_decode_8b_gqa_ncu.md")
 CSRC = os.path.join(ROOT, "paged_kv_cache_29_gb300", "csrc")
 
@@ -293,7 +296,9 @@ def run_native(args) -> dict | None:
     world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        import datetime
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local),
+                                timeout=datetime.timedelta(seconds=PG_TIMEOUT_S))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     step = wl.make(args.workload, seed=wl.WORKLOAD_SEEDS[args.workload] + 1000 * rank)

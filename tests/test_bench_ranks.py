@@ -1,8 +1,11 @@
 """bench.py's whole-job aggregation over ranks, on two gloo processes (CPU):
 timings take the max over ranks, work counts the sum; the reference arm runs
-on rank 0 only."""
+on rank 0 only; a rank that dies between steps makes the other's reduction
+fail within the process-group timeout instead of waiting."""
+import datetime
 import os
 import socket
+import time
 
 import pytest
 import torch
@@ -61,3 +64,37 @@ def test_reduce_without_process_group_is_identity():
     import bench
     assert not dist.is_initialized()
     assert bench.reduce_over_ranks([1, 2], [3], torch.device("cpu")) == ([1.0, 2.0], [3.0])
+
+
+def _dying_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=20))
+    if rank == 1:
+        os._exit(3)                             # dies between steps, without a goodbye
+    t0 = time.monotonic()
+    try:
+        bench.reduce_over_ranks([1.0], [1.0], torch.device("cpu"))
+        out.put((rank, "no error", time.monotonic() - t0))
+    except Exception as e:                      # the backend's error type varies by version
+        out.put((rank, type(e).__name__, time.monotonic() - t0))
+
+
+def test_dead_rank_fails_the_reduction_instead_of_hanging():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dying_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    rank, outcome, waited = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.kill()
+    assert rank == 0
+    assert outcome != "no error"                # the survivor learns of it on the host
+    assert waited < 60.0                        # within the timeout, not a hang
+    assert procs[1].exitcode == 3
