@@ -93,3 +93,49 @@ def test_bad_block_id_mid_stream_is_flagged(fmt):
     got, err = _run(fmt, step)
     assert err == 0
     assert max_abs(got, want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mcl", [0, 16])
+def test_all_empty_batch(mcl):
+    """No sequence has a row: the plan yields no work item at all; every output
+    row is zero and nothing is flagged, for every kernel family (max_context_len
+    0, or an upper bound no sequence reaches)."""
+    from gpu_helpers import DeviceStep
+    lens = [0] * 5
+    step = wl.build_step("all_empty", lens, 8, 2, 128, cache_dtype="bf16", seed=33)
+    for kernel in ["mma", "simt", "generic"]:
+        dev = DeviceStep(step)
+        dev.out.fill_(7.0)
+        dev.decode(kernel, max_context_len=mcl)
+        torch.cuda.synchronize()
+        assert dev.error_word() == 0, kernel
+        assert np.all(dev.result() == 0.0), kernel
+    for fmt in FORMATS:
+        st = wl.build_step(f"all_empty_{fmt}", lens, 32, 8, 128, cache_dtype=fmt, seed=34)
+        q = to_torch(st.q, "bf16")
+        kc, vc = _dev(st.k_cache), _dev(st.v_cache)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full_like(q, 7.0)
+        if fmt == "fp8":
+            pa.pa_decode_fp8(q, kc, vc, to_torch(st.block_tables), to_torch(st.context_lens),
+                             st.scale, out, mcl, 1.0, 1.0, error_word=err)
+        else:
+            pa.pa_decode_int8(q, kc, vc, _dev(st.k_row_scales), _dev(st.v_row_scales),
+                              to_torch(st.block_tables), to_torch(st.context_lens), st.scale,
+                              out, mcl, error_word=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, fmt
+        assert torch.all(out == 0).item(), fmt
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("bs", [32, 64])
+def test_larger_blocks(fmt, bs):
+    """Blocks of 32 and 64 rows: several tiles per block (and, for INT8, the
+    row scales of each tile inside the block's scale rows)."""
+    lens = [1, 31, 32, 33, 64, 65, 700, 2100]
+    step = wl.build_step(f"qs_bs{bs}", lens, 32, 8, 128, cache_dtype=fmt, block_size=bs,
+                         seed=35 + bs)
+    got, err = _run(fmt, step)
+    assert err == 0
+    assert max_abs(got, _reference(fmt, step)) <= TOL["bf16"]
