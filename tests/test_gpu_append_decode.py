@@ -142,9 +142,21 @@ def _poison_quant(step):
 @pytest.mark.parametrize("fmt", ["fp8", "int8"])
 @pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2)])
 def test_quantised_fused_step_equals_append_then_decode(fmt, hq, hkv):
+    _check_quantised_fused(fmt, _poison_quant(wl.build_step(f"q{fmt}", LENS, hq, hkv, 128,
+                                                            cache_dtype=fmt, seed=hq + hkv)))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+@pytest.mark.parametrize("bs", [32, 64])
+def test_quantised_fused_step_larger_blocks(fmt, bs):
+    """The new row lands in a block of several tiles (and INT8 scale rows)."""
+    _check_quantised_fused(fmt, _poison_quant(wl.build_step(f"q{fmt}{bs}", LENS, 32, 8, 128,
+                                                            cache_dtype=fmt, block_size=bs,
+                                                            seed=bs)))
+
+
+def _check_quantised_fused(fmt, step):
     import oracle
-    step = _poison_quant(wl.build_step(f"q{fmt}", LENS, hq, hkv, 128, cache_dtype=fmt,
-                                       seed=hq + hkv))
     ksc, vsc = (0.75, 1.5) if fmt == "fp8" else (1.0, 1.0)
     fused, two = _quant_step_tensors(step), _quant_step_tensors(step)
     if fmt == "fp8":
