@@ -98,3 +98,40 @@ def test_random_shape_8bit(i):
                                       np.ascontiguousarray(ref).view(np.uint8))
     got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
     assert max_abs(got, want) <= TOL["bf16"], (i, fmt, g, hkv, bs, lens)
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_window(i):
+    import test_gpu_window as tw
+    rng = np.random.default_rng(3000 + i)
+    dtype = ["f32", "bf16"][i % 2]
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    hq = hkv * int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([16, 32]))
+    lens = rng.integers(0, 4000, size=int(rng.integers(1, 9)))
+    lens[rng.random(len(lens)) < 0.2] = 0
+    window = int(rng.integers(1, 3000))
+    step = wl.build_step(f"rwin{i}", [int(x) for x in lens], hq, hkv, d, cache_dtype=dtype,
+                         block_size=bs, seed=int(rng.integers(1 << 30)))
+    got, err = tw._gpu(step, window)
+    assert err == 0, (i, dtype, hq, hkv, d, bs, window, list(lens))
+    assert max_abs(got, tw._oracle(step, window)) <= TOL[dtype], (i, window)
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_multi_query(i):
+    import test_gpu_multi as tm
+    rng = np.random.default_rng(4000 + i)
+    Q = int(rng.choice([1, 2, 3, 4, 8]))
+    g = int(rng.choice([g for g in (1, 2, 4, 8) if g * Q <= 8]))
+    hkv = int(rng.choice([1, 2, 8]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([16, 32]))
+    lens = rng.integers(Q, 4000, size=int(rng.integers(1, 9)))
+    lens[rng.random(len(lens)) < 0.2] = 0
+    step = wl.build_step(f"rmq{i}", [int(x) for x in lens], g * hkv, hkv, d, block_size=bs,
+                         seed=int(rng.integers(1 << 30)), num_queries=Q)
+    got, err = tm._gpu(step)
+    assert err == 0, (i, Q, g, hkv, d, bs, list(lens))
+    assert max_abs(got, tm._oracle(step)) <= TOL["bf16"], (i, Q, g)
