@@ -118,7 +118,9 @@ constexpr int kMaxHeadDim = 256;
 constexpr int kMaxDevices = 64;      // devices whose per-kernel launch set-up is cached
 constexpr int kDefaultPartition = 512;
 // 8-bit caches: twice the rows, the same bytes per partition as 512 bf16 rows
-// (fewer items, merges and partials for the same traffic).
+// (fewer items, merges and partials for the same traffic). Calls with several
+// query tokens per sequence use it too: their items carry twice the query
+// columns or more, so the per-item merge and partials weigh as much.
 constexpr int kDefaultPartition8 = 1024;
 
 }  // namespace pa
