@@ -539,7 +539,7 @@ def run_native(args) -> dict | None:
             "num_kv_heads": step.num_kv_heads, "head_dim": step.head_dim,
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),
-            "max_context_len": mcl, "partition_size": pa.pa_default_partition_size(cd) if step.num_queries == 1 else 1024, "kernel": kernel_name,
+            "max_context_len": mcl, "partition_size": pa.pa_default_partition_size(cd), "kernel": kernel_name,
             "step": ("fused append + decode call (new rows written by the decode kernel)"
                      if fused_step else "append call + decode call"),
             "l2": "between timed steps a 256 MiB buffer is written, then another 256 MiB read (L2 clean, holding none of the step's data); attended K/V also exceed L2",

@@ -186,8 +186,8 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapp
  * round-to-nearest-even.
  *
  * Long sequences are split into fixed partitions of 512 rows (1024 over the
- * 8-bit caches of pa_decode_fp8 and pa_decode_int8: the same bytes per
- * partition; pa_default_partition_size) whose partial
+ * FP8 caches of pa_decode_fp8: the same bytes per partition;
+ * pa_default_partition_size) whose partial
  * results (running max, sum and unnormalised output, the online-softmax state
  * of Q4 "How would you write a fused attention kernel?") are merged by a
  * second kernel. Partition boundaries and the merge order depend only on the
@@ -308,8 +308,7 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * pa_decode_workspace_size_multi. Supported: head_dim 64 or 128, block_size a
  * multiple of 16, (num_heads / num_kv_heads) * num_queries <= 8 (else
  * PA_ERR_UNSUPPORTED); 1 <= num_queries <= 8. Same merge order and batch
- * invariance as pa_decode; with num_queries > 1 the partitions hold 1024 rows
- * (an item carries num_queries times the query columns), else 512.
+ * invariance as pa_decode.
  */
 pa_status pa_decode_multi(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens, float scale,
@@ -441,11 +440,10 @@ pa_status pa_check_error_word(int32_t error_word_value);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pa_version(void);
 
-/* Rows per split-K partition the single-query decode calls use for a cache
- * of this type when none is requested: 512 for fp32 and bf16, 1024 for the
- * 1-byte FP8 and INT8 caches (the same bytes per partition). 0 for a type no
- * cache holds. pa_decode_multi with num_queries > 1 uses 1024. The workspace
- * size functions assume 512, which covers every case. */
+/* Rows per split-K partition the decode calls use for a cache of this type
+ * when none is requested: 512 for fp32, bf16 and INT8, 1024 for FP8 (the same
+ * bytes per partition as 512 bf16 rows). 0 for a type no cache holds. The
+ * workspace size functions assume 512, which covers every case. */
 int pa_default_partition_size(pa_dtype cache_dtype);
 
 #ifdef __cplusplus

@@ -124,8 +124,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                       const int64_t* slot_mapping = nullptr, int withhold_tile = -1) {
     const int kernel_req = options ? options->kernel : PA_KERNEL_AUTO;
     const int partition = (options && options->partition_size) ? options->partition_size
-                          : (elem_bytes(dtype) == 1 || num_queries > 1) ? pa::kDefaultPartition8
-                                                                        : pa::kDefaultPartition;
+                          : dtype == PA_DTYPE_FP8_E4M3          ? pa::kDefaultPartition8
+                                                               : pa::kDefaultPartition;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
         !valid_decode_cache_dtype(dtype) || !valid_dtype(act_dtype) ||
@@ -318,7 +318,7 @@ int pa_version(void) { return kVersion; }
 
 int pa_default_partition_size(pa_dtype cache_dtype) {
     if (!valid_decode_cache_dtype(cache_dtype)) return 0;
-    return elem_bytes(cache_dtype) == 1 ? pa::kDefaultPartition8 : pa::kDefaultPartition;
+    return cache_dtype == PA_DTYPE_FP8_E4M3 ? pa::kDefaultPartition8 : pa::kDefaultPartition;
 }
 
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_heads, int head_dim,

@@ -117,10 +117,11 @@ __host__ __device__ inline int seq_row_base(int n, int window) {
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxDevices = 64;      // devices whose per-kernel launch set-up is cached
 constexpr int kDefaultPartition = 512;
-// 8-bit caches: twice the rows, the same bytes per partition as 512 bf16 rows
-// (fewer items, merges and partials for the same traffic). Calls with several
-// query tokens per sequence use it too: their items carry twice the query
-// columns or more, so the per-item merge and partials weigh as much.
+// FP8 caches: twice the rows, the same bytes per partition as 512 bf16 rows
+// (fewer items, merges and partials for the same traffic; faster on large and
+// small batches alike). INT8 and multi-token calls keep 512: with fewer items
+// than CTAs a small batch waits for its largest item, and there 1024 rows
+// measured slower.
 constexpr int kDefaultPartition8 = 1024;
 
 }  // namespace pa

@@ -41,9 +41,9 @@ def test_withhold_hook_argument_checks(lib):
 
 
 def test_default_partition_sizes():
-    # 512 rows of 2- or 4-byte elements; 1024 rows of the 1-byte 8-bit caches
+    # 512 rows, 1024 of FP8 codes (the same bytes per partition as 512 bf16 rows)
     assert [pa.pa_default_partition_size(d) for d in ("f32", "bf16", "fp8", "int8")] == \
-        [512, 512, 1024, 1024]
+        [512, 512, 1024, 512]
     assert pa.lib().pa_default_partition_size(7) == 0
     with pytest.raises(ValueError):
         pa.pa_default_partition_size("f16")
