@@ -2,6 +2,7 @@
 the header declares, and rejects bad arguments on the host before touching
 CUDA."""
 import ctypes
+import os
 
 import pytest
 
@@ -176,3 +177,21 @@ def test_fused_step_calls_reject_bad_arguments_on_the_host(lib):
         pa.PA_ERR_INVALID_ARG
     assert lib.pa_append_decode_int8(P, P, None, P, P, P, P, *common, *tail) == \
         pa.PA_ERR_INVALID_ARG
+
+
+def test_c99_program_builds_links_and_runs(lib, tmp_path):
+    """The header is plain C99 and the library links into a C program."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    here = os.path.dirname(os.path.abspath(__file__))
+    lib = pa.LIB_PATH
+    exe = str(tmp_path / "abi_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(here, "..", "include"), os.path.join(here, "c", "abi_check.c"),
+                    "-L", os.path.dirname(lib), "-l:" + os.path.basename(lib),
+                    "-Wl,-rpath," + os.path.dirname(lib), "-o", exe], check=True)
+    run = subprocess.run([exe], capture_output=True, text=True)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stdout)
