@@ -366,7 +366,9 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int m
  *     caller-provided workspace for those.
  *   - The first call on a device looks up the scratch's address there (with
  *     that device current) and caches it: make that first call before any
- *     stream capture on that device.
+ *     stream capture on that device. The cached address is that of the
+ *     device's context at the time: no call may follow a cudaDeviceReset of
+ *     that device in the same process.
  *   - There is ONE scratch per device. Calls whose work may overlap on the
  *     GPU (other streams, other host threads, or another pa_decode_noalloc
  *     call on a stream not ordered after this one) race on it and give wrong

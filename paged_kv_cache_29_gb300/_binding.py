@@ -198,6 +198,23 @@ def _check_cuda(name, t, dtype=None, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
 
 
+def _check_device(stream, *tensors):
+    """Every tensor (and an explicit torch stream) on torch's current CUDA
+    device. The library launches on the current device and takes the SM count,
+    the tensor maps, the fixed scratch of pa_decode_noalloc and the default
+    stream from it, so a tensor on another GPU would hand that GPU's pointers
+    to kernels running here."""
+    import torch
+    cur = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.device.index != cur:
+            raise ValueError(f"a tensor is on {t.device} but the current CUDA device is cuda:{cur}:"
+                             f" run the call under torch.cuda.device({t.device.index})")
+    dev = getattr(stream, "device", None)
+    if dev is not None and getattr(dev, "index", cur) != cur:
+        raise ValueError(f"the stream belongs to {dev} but the current CUDA device is cuda:{cur}")
+
+
 def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, error_word=None,
                          stream=None) -> None:
     """Append new K/V rows ([T][Hkv][D]) into their slots of the paged pools
@@ -214,6 +231,7 @@ def pa_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, error_wor
     if tuple(v_cache.shape) != (nb, hkv, bs, d) or tuple(k_new.shape[1:]) != (hkv, d) \
             or k_new.shape != v_new.shape or slot_mapping.shape[0] != k_new.shape[0]:
         raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    _check_device(stream, k_new, v_new, slot_mapping, k_cache, v_cache, error_word)
     rc = lib().pa_reshape_and_cache(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                                     _ptr(k_cache), _ptr(v_cache), int(k_new.shape[0]), hkv, d,
                                     bs, nb, _dtype_code(k_cache), _ptr(error_word),
@@ -240,6 +258,7 @@ def pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_sca
     if tuple(v_cache.shape) != (nb, hkv, bs, d) or tuple(k_new.shape[1:]) != (hkv, d) \
             or k_new.shape != v_new.shape or slot_mapping.shape[0] != k_new.shape[0]:
         raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    _check_device(stream, k_new, v_new, slot_mapping, k_cache, v_cache, error_word)
     rc = lib().pa_reshape_and_cache_fp8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new),
                                         _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                                         int(k_new.shape[0]), hkv, d, bs, nb, float(k_scale),
@@ -268,6 +287,8 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, m
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word,
+                  workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -304,6 +325,8 @@ def pa_test_withhold_tile(q, k_cache, v_cache, block_tables, context_lens, scale
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word,
+                  workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -342,6 +365,8 @@ def pa_decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out,
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word,
+                  workspace)
     if workspace is None:
         need = pa_decode_workspace_size_multi(B, Q, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -373,6 +398,8 @@ def pa_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale, win
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word,
+                  workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -413,6 +440,8 @@ def pa_reshape_and_cache_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_sc
     if tuple(k_new.shape[1:]) != (hkv, d) or k_new.shape != v_new.shape \
             or slot_mapping.shape[0] != k_new.shape[0]:
         raise ValueError("shape mismatch between k_new/v_new/slot_mapping and the caches")
+    _check_device(stream, k_new, v_new, slot_mapping, k_cache, v_cache, k_scales, v_scales,
+                  error_word)
     rc = lib().pa_reshape_and_cache_int8(_ptr(k_new), _ptr(v_new), _dtype_code(k_new),
                                          _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(k_scales), _ptr(v_scales), int(k_new.shape[0]), hkv,
@@ -437,6 +466,8 @@ def pa_decode_int8(q, k_cache, v_cache, k_scales, v_scales, block_tables, contex
     if dq != d or tuple(out.shape) != tuple(q.shape) or block_tables.shape[0] != B \
             or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, k_scales, v_scales, block_tables,
+                  context_lens, error_word, workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -465,6 +496,7 @@ def pa_copy_blocks(k_cache, v_cache, block_mapping, error_word=None, stream=None
     nb, hkv, bs, d = k_cache.shape
     if tuple(v_cache.shape) != (nb, hkv, bs, d) or block_mapping.shape[1] != 2:
         raise ValueError("v_cache must match k_cache and block_mapping must be [n][2]")
+    _check_device(stream, k_cache, v_cache, block_mapping, error_word)
     rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_mapping),
                               int(block_mapping.shape[0]), hkv, d, bs, nb,
                               _dtype_code(k_cache), _ptr(error_word), _stream(stream))
@@ -501,6 +533,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word,
+                  workspace)
     if workspace is None:
         # The C library allocates nothing; the binding takes the scratch from
         # torch's allocator for callers that do not manage their own.
@@ -543,6 +577,8 @@ def pa_append_decode(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_tabl
             or slot_mapping.shape[0] != B or block_tables.shape[0] != B \
             or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between the step's tensors and the caches")
+    _check_device(stream, k_new, v_new, slot_mapping, q, out, k_cache, v_cache, block_tables,
+                  context_lens, error_word, workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -589,6 +625,8 @@ def pa_append_decode_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, q, block_
         _check_cuda("error_word", error_word, torch.int32)
     nb, hkv, bs, d = k_cache.shape
     B, hq = _check_step_rows(k_new, v_new, slot_mapping, q, out, block_tables, context_lens, hkv, d)
+    _check_device(stream, k_new, v_new, slot_mapping, q, out, k_cache, v_cache, block_tables,
+                  context_lens, error_word, workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -615,6 +653,8 @@ def pa_append_decode_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales
         _check_cuda("error_word", error_word, torch.int32)
     nb, hkv, bs, d = k_cache.shape
     B, hq = _check_step_rows(k_new, v_new, slot_mapping, q, out, block_tables, context_lens, hkv, d)
+    _check_device(stream, k_new, v_new, slot_mapping, q, out, k_cache, v_cache, k_scales,
+                  v_scales, block_tables, context_lens, error_word, workspace)
     if workspace is None:
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -653,6 +693,7 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, ou
     if dq != d or tuple(out.shape) != tuple(q.shape) or tuple(v_cache.shape) != tuple(k_cache.shape) \
             or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch between q/out/block_tables/context_lens and the caches")
+    _check_device(stream, q, out, k_cache, v_cache, block_tables, context_lens, error_word)
     rc = lib().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d, bs,
                                  nb, int(block_tables.shape[1]), int(max_context_len),

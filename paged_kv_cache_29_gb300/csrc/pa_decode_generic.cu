@@ -179,12 +179,16 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
     const int qh = HPB > 1 ? blockIdx.x * HPB + (threadIdx.x >> 5) : blockIdx.x;
     const int sq = blockIdx.y;                 // s * num_queries + query token
     const int s = sq / p.num_queries;
-    // Launched as a programmatic dependent of the decode kernel, which starts
-    // this grid only after its own griddepcontrol.wait (every kernel before it
-    // has completed) and never writes the context lengths: they are final and
-    // visible here, and a sequence of one partition (written directly by the
-    // decode kernel) leaves at once. CTA (0, 0) always waits, so that this
-    // grid never completes before the decode kernel does.
+    // Launched as a programmatic dependent of a decode kernel. The context
+    // lengths are read before griddepcontrol.wait, which is safe because no
+    // decode kernel writes them and every decode kernel either triggers this
+    // grid only after its own griddepcontrol.wait (the tile-ring kernels:
+    // every kernel before them has completed by then) or never triggers it
+    // (the direct-load kernel, which therefore completes first). A decode
+    // kernel that triggered earlier would break this. A sequence of one
+    // partition (written directly by the decode kernel) leaves at once. CTA
+    // (0, 0) always waits, so that this grid never completes before the
+    // decode kernel does.
     const int n = __ldg(p.context_lens + s);
     const int P = p.partition_size;
     const int span = n - seq_row_base(n, p.window);       // rows of the partitions

@@ -8,10 +8,16 @@
 // cudaGetSymbolAddress (with that device current) and cached; after that a
 // call only checks sizes and forwards to pa_decode.
 //
-// Nothing in the scratch has to start at zero: the plan kernel of every
-// launch writes the work-item count and every item before the decode kernel
-// reads them, and the decode kernel writes every partition partial before the
-// merge kernel reads it. So the scratch is never cleared.
+// Nothing in the scratch has to start at zero: each CTA of the persistent
+// decode kernel computes the launch's work list itself and writes every work
+// item it later reads back (no CTA reads another's items), and every partition
+// partial is written by the decode kernel before the merge kernel reads it.
+// So the scratch is never cleared.
+//
+// The cached address belongs to the device's primary context of the moment.
+// cudaDeviceReset (or anything else that destroys that context) unloads the
+// module and may place the array elsewhere when it is loaded again, so no
+// call may follow a device reset in the same process.
 #include <atomic>
 #include <cstdint>
 

@@ -452,6 +452,54 @@ def pin_int8_append():
                     np.testing.assert_array_equal(a[idx], a0[idx])
 
 
+# Rows whose quotients x / scale are exact halves k + 1/2: scale = amax / 127 is
+# exact when amax = 127 * 2^-3, 127 * 3 or 127 * 4, and so is every quotient
+# below. Expected codes written out by hand under round-half-to-even
+# (half-away rounding would give 1, 2, 3, 4, 5, 126, 127, -1, -2, -3, -4, 8,
+# 11, 65 in the first row). The rows with power-of-two scales are exact in
+# bf16 as well as fp32; 127 * 3 needs 9 significant bits, fp32 only.
+INT8_TIE_ROWS = [
+    # (values / scale, scale, expected codes, input types)
+    ([0.5, 1.5, 2.5, 3.5, 4.5, 125.5, 126.5, -0.5, -1.5, -2.5, -3.5, 7.5, 10.5, 64.5, 127.0,
+      0.0], 0.125,
+     [0, 2, 2, 4, 4, 126, 126, 0, -2, -2, -4, 8, 10, 64, 127, 0], ("f32", "bf16")),
+    ([1.5, 2.5, -2.5, 127.0, 0.5, 3.5, -127.0, 5.5, -5.5, 6.5, 8.5, 9.5, -0.5, 11.5, 12.5,
+      13.5], 3.0,
+     [2, 2, -2, 127, 0, 4, -127, 6, -6, 6, 8, 10, 0, 12, 12, 14], ("f32",)),
+    ([-127.0, 21.5, 22.5, -23.5, 0.5, 1.5, 33.5, 34.5, -99.5, 100.5, 101.5, 0.0, 1.0, -1.0,
+      -64.5, 63.5], 4.0,
+     [-127, 22, 22, -24, 0, 2, 34, 34, -100, 100, 102, 0, 1, -1, -64, 64], ("f32", "bf16")),
+]
+
+
+def pin_int8_tie_rounding():
+    """INT8 codes of exact half-way quotients round to the even neighbour
+    ("MLSys Engineer -- Inference Systems Q&A", Q3 gives scale = max|row| / 127
+    and rounding to int8; the tie rule is round-half-to-even, the IEEE default),
+    for fp32 and bf16 input rows."""
+    d = 16
+    for new_dtype in ("f32", "bf16"):
+        cases = [r for r in INT8_TIE_ROWS if new_dtype in r[3]]
+        T = len(cases)
+        rows = np.array([[np.float32(q * sc) for q in qs] for qs, sc, _, _ in cases], np.float32)
+        assert np.all(rows.astype(np.float64) ==
+                      np.array([[q * sc for q in qs] for qs, sc, _, _ in cases]))
+        kn = wl.to_cache_dtype(rows[:, None, :], new_dtype)
+        vn = wl.to_cache_dtype(-rows[:, None, :], new_dtype)
+        assert np.all(wl.as_f32(kn, new_dtype) == rows[:, None, :])   # exact in the input type
+        nb, bs = T, 2
+        kc = np.zeros((nb, 1, bs, d), np.int8)
+        vc = np.zeros_like(kc)
+        ks = np.zeros((nb, 1, bs), np.float32)
+        vs = np.zeros_like(ks)
+        slots = np.array([t * bs + (t % 2) for t in range(T)], np.int64)
+        assert oracle.append_int8(kn, vn, slots, kc, vc, ks, vs) == 0
+        for t, (qs, sc, want, _) in enumerate(cases):
+            b, o = t, t % 2
+            assert ks[b, 0, o] == np.float32(sc) and vs[b, 0, o] == np.float32(sc)
+            assert kc[b, 0, o].tolist() == want, (new_dtype, kc[b, 0, o].tolist(), want)
+            assert vc[b, 0, o].tolist() == [-c for c in want]
+
 def pin_int8_decode():
     """Attention over INT8 codes with per-row scales equals the pure-Python
     brute force over the fp64 values scale * code."""
@@ -619,6 +667,6 @@ def pin_incremental_decoder():
 ALL_PINS = [pin_brute_force, pin_paged_equals_contiguous, pin_block_permutation,
             pin_block_size_invariance, pin_softmax_weights_and_hull, pin_copy_on_write,
             pin_copy_blocks, pin_e4m3_format, pin_fp8_append, pin_fp8_decode, pin_multi_query,
-            pin_sliding_window, pin_int8_append, pin_int8_decode,
+            pin_sliding_window, pin_int8_append, pin_int8_tie_rounding, pin_int8_decode,
             pin_closed_forms, pin_split_invariance, pin_gqa_grouping, pin_append_slots,
             pin_incremental_decoder]

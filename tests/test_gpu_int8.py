@@ -155,3 +155,66 @@ def test_int8_copy_on_write_copies_codes_and_scales():
         wk[dst], wv[dst], wks[dst], wvs[dst] = wk[src], wv[src], wks[src], wvs[src]
     for dv, want in zip((kc, vc, ks, vs), (wk, wv, wks, wvs)):
         np.testing.assert_array_equal(dv.cpu().numpy(), want)
+
+
+def _tie_rows(d, dtype):
+    """The hand-checked half-way rows of the oracle pin, zero-padded to d
+    elements (the row maximum, hence the scale, is unchanged)."""
+    import pins
+    cases = [r for r in pins.INT8_TIE_ROWS if dtype in r[3]]
+    rows = np.zeros((len(cases), d), np.float32)
+    want = np.zeros((len(cases), d), np.int8)
+    for t, (qs, sc, codes, _) in enumerate(cases):
+        rows[t, :16] = [q * sc for q in qs]
+        want[t, :16] = codes
+    return rows, want, np.array([c[1] for c in cases], np.float32)
+
+
+@pytest.mark.parametrize("new_dtype", ["bf16", "f32"])
+def test_int8_append_rounds_exact_halves_to_even(new_dtype):
+    d, hkv = 128, 1
+    rows, want, scales = _tie_rows(d, new_dtype)
+    T = rows.shape[0]
+    nb, bs = T, 16
+    kn = wl.to_cache_dtype(rows[:, None, :], new_dtype)
+    vn = wl.to_cache_dtype(-rows[:, None, :], new_dtype)
+    kc = torch.zeros(nb, hkv, bs, d, dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros(nb, hkv, bs, dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    slots = np.array([t * bs + 5 for t in range(T)], np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_reshape_and_cache_int8(to_torch(kn, new_dtype), to_torch(vn, new_dtype),
+                                 to_torch(slots), kc, vc, ks, vs, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    k, v = kc.cpu().numpy(), vc.cpu().numpy()
+    for t in range(T):
+        np.testing.assert_array_equal(k[t, 0, 5], want[t])
+        np.testing.assert_array_equal(v[t, 0, 5], -want[t])
+    np.testing.assert_array_equal(ks.cpu().numpy()[:, 0, 5], scales)
+
+
+def test_int8_fused_append_rounds_exact_halves_to_even():
+    """The decode kernel's own quantisation of the new rows (pa_append_decode_int8)."""
+    rows, want, _ = _tie_rows(128, "bf16")
+    T = rows.shape[0]
+    step = wl.build_step("ties", [40] * T, 4, 1, 128, cache_dtype="int8", seed=9)
+    kn = wl.to_cache_dtype(rows[:, None, :], "bf16")
+    vn = wl.to_cache_dtype(-rows[:, None, :], "bf16")
+    kc, vc = _dev(step.k_cache), _dev(step.v_cache)
+    ks, vs = _dev(step.k_row_scales), _dev(step.v_row_scales)
+    q = to_torch(step.q, "bf16")
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_append_decode_int8(to_torch(kn, "bf16"), to_torch(vn, "bf16"),
+                             to_torch(step.slot_mapping), kc, vc, ks, vs, q,
+                             to_torch(step.block_tables), to_torch(step.context_lens),
+                             step.scale, out, step.max_context_len, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    k, v = kc.cpu().numpy(), vc.cpu().numpy()
+    for t, slot in enumerate(step.slot_mapping):
+        b, o = int(slot) // 16, int(slot) % 16
+        np.testing.assert_array_equal(k[b, 0, o], want[t])
+        np.testing.assert_array_equal(v[b, 0, o], -want[t])

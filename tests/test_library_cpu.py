@@ -195,3 +195,74 @@ def test_c99_program_builds_links_and_runs(lib, tmp_path):
                     "-Wl,-rpath," + os.path.dirname(lib), "-o", exe], check=True)
     run = subprocess.run([exe], capture_output=True, text=True)
     assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stdout)
+
+
+class _OnDevice:
+    """A stand-in for a CUDA tensor on device `index` (no GPU needed): the
+    binding reads only these attributes before it calls the library."""
+
+    def __init__(self, shape, dtype, index):
+        import torch
+        self._t = torch.empty(shape, dtype=dtype)
+        self.shape, self.dtype = self._t.shape, dtype
+        self.device = torch.device("cuda", index)
+        self.is_cuda = True
+
+    def is_contiguous(self):
+        return True
+
+    def dim(self):
+        return self._t.dim()
+
+    def numel(self):
+        return self._t.numel()
+
+    def element_size(self):
+        return self._t.element_size()
+
+    def data_ptr(self):
+        return FAKE
+
+
+def test_binding_refuses_tensors_on_another_device_before_any_call(monkeypatch):
+    import torch
+
+    def no_library():
+        raise AssertionError("the library was reached")
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(pa, "lib", no_library)
+    B, hq, hkv, d, nb, bs = 2, 8, 2, 128, 8, 16
+
+    def tensors(q_dev=0, cache_dev=0, ws_dev=0):
+        bf = torch.bfloat16
+        return dict(q=_OnDevice((B, hq, d), bf, q_dev),
+                    k_cache=_OnDevice((nb, hkv, bs, d), bf, cache_dev),
+                    v_cache=_OnDevice((nb, hkv, bs, d), bf, cache_dev),
+                    block_tables=_OnDevice((B, 4), torch.int32, 0),
+                    context_lens=_OnDevice((B,), torch.int32, 0),
+                    out=_OnDevice((B, hq, d), bf, 0),
+                    workspace=_OnDevice((4096,), torch.uint8, ws_dev))
+
+    for kw in (dict(q_dev=1), dict(cache_dev=1), dict(ws_dev=1)):
+        t = tensors(**kw)
+        with pytest.raises(ValueError, match="current CUDA device"):
+            pa.pa_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                         t["context_lens"], 0.1, t["out"], 64, workspace=t["workspace"])
+    t = tensors(q_dev=1)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        pa.pa_decode_noalloc(t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                             t["context_lens"], 0.1, t["out"], 64)
+    k_new = _OnDevice((B, hkv, d), torch.bfloat16, 1)
+    slots = _OnDevice((B,), torch.int64, 1)
+    t = tensors()
+    with pytest.raises(ValueError, match="current CUDA device"):
+        pa.pa_reshape_and_cache(k_new, k_new, slots, t["k_cache"], t["v_cache"])
+    with pytest.raises(ValueError, match="current CUDA device"):
+        pa.pa_copy_blocks(t["k_cache"], t["v_cache"], _OnDevice((3, 2), torch.int64, 1))
+    # everything on the current device: the checks pass and the call reaches
+    # the library (here the stub)
+    t = tensors()
+    with pytest.raises(AssertionError, match="library was reached"):
+        pa.pa_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                     0.1, t["out"], 64, workspace=t["workspace"])

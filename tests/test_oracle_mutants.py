@@ -45,6 +45,8 @@ MUTANTS = [
      "const size_t qrow = ((size_t)s * num_heads + qh) * Q + j;"),
     ("int8_scale_128", "const float scale = amax / 127.0f;", "const float scale = amax / 128.0f;"),
     ("int8_truncates", "float c = nearbyintf(x[d] / scale);", "float c = truncf(x[d] / scale);"),
+    ("int8_round_half_away", "float c = nearbyintf(x[d] / scale);",
+     "float c = roundf(x[d] / scale);"),
     ("int8_v_unscaled", "Vc[(size_t)i * head_dim + d] = (double)v_scales[r] * (double)v_cache[r * head_dim + d];",
      "Vc[(size_t)i * head_dim + d] = (double)v_cache[r * head_dim + d];"),
     ("window_off_by_one", "const int first = n > window ? n - window : 0;",
