@@ -222,21 +222,40 @@ def dist_env():
 
 def sample_step(step: wl.DecodeStep, seqs: list[int]) -> wl.DecodeStep:
     idx = np.array(seqs, dtype=np.int64)
-    return wl.DecodeStep(**{**step.__dict__, "q": step.q[idx], "k_new": step.k_new[idx],
-                            "v_new": step.v_new[idx], "slot_mapping": step.slot_mapping[idx],
+    Q = step.num_queries
+    tok = (idx[:, None] * Q + np.arange(Q)[None, :]).reshape(-1)
+    return wl.DecodeStep(**{**step.__dict__, "q": step.q[idx], "k_new": step.k_new[tok],
+                            "v_new": step.v_new[tok], "slot_mapping": step.slot_mapping[tok],
                             "block_tables": step.block_tables[idx],
                             "context_lens": step.context_lens[idx]})
+
+
+def oracle_decode(step: wl.DecodeStep, sub: wl.DecodeStep, threads: int):
+    """The oracle's attention for the sequences of `sub` over `step`'s pool,
+    with the oracle function of the step's kind."""
+    import oracle
+    args = (sub.block_tables, sub.context_lens, step.scale)
+    if step.cache_dtype == "int8":
+        return oracle.decode_int8(sub.q, step.k_cache, step.v_cache, step.k_row_scales,
+                                  step.v_row_scales, *args, num_threads=threads)
+    if step.cache_dtype == "fp8":
+        return oracle.decode_kv(sub.q, step.k_cache, step.v_cache, *args, step.k_scale,
+                                step.v_scale, num_threads=threads)
+    if step.num_queries > 1:
+        return oracle.decode_multi(sub.q, step.k_cache, step.v_cache, *args, num_threads=threads)
+    if step.window > 0:
+        return oracle.decode_window(sub.q, step.k_cache, step.v_cache, *args, step.window,
+                                    num_threads=threads)
+    return oracle.decode(sub.q, step.k_cache, step.v_cache, *args, num_threads=threads)
 
 
 def oracle_sample_plan(step: wl.DecodeStep, target_s: float, threads: int):
     """Pick a sample of sequences that keeps the oracle busy about target_s
     seconds; the rate is probed on one short sequence first."""
-    import oracle
     order = list(np.argsort(step.context_lens, kind="stable"))
     probe = sample_step(step, [order[len(order) // 2]])
     t0 = time.perf_counter()
-    oracle.decode(probe.q, step.k_cache, step.v_cache, probe.block_tables, probe.context_lens,
-                  step.scale, num_threads=1)
+    oracle_decode(step, probe, 1)
     per_token = (time.perf_counter() - t0) / max(int(probe.context_lens.sum()), 1)
     budget_tokens = target_s * max(threads, 1) / max(per_token, 1e-12)
     chosen, tokens = [], 0
@@ -253,16 +272,13 @@ def oracle_sample_plan(step: wl.DecodeStep, target_s: float, threads: int):
 
 
 def time_oracle(step: wl.DecodeStep, seqs: list[int], threads: int) -> tuple[float, int]:
-    """Seconds for one oracle decode over the sampled sequences, and its bytes."""
-    import oracle
+    """Seconds for one oracle decode over the sampled sequences, and their
+    algorithmic attention bytes."""
     sub = sample_step(step, seqs)
     t0 = time.perf_counter()
-    oracle.decode(sub.q, step.k_cache, step.v_cache, sub.block_tables, sub.context_lens,
-                  step.scale, num_threads=threads)
+    oracle_decode(step, sub, threads)
     dt = time.perf_counter() - t0
-    b = accounting.step_bytes(sub.context_lens, step.num_heads, step.num_kv_heads,
-                              step.head_dim, step.elem_bytes, step.block_size)
-    return dt, b.decode
+    return dt, accounting.step_bytes_for(sub).decode
 
 
 def cpu_baseline(step: wl.DecodeStep, target_s: float = 12.0) -> dict:
@@ -285,9 +301,222 @@ def cpu_baseline(step: wl.DecodeStep, target_s: float = 12.0) -> dict:
             "seconds": round(total_s, 3)}
 
 
+def oracle_rates(step: wl.DecodeStep, seconds: float) -> dict:
+    """The oracle's rate on a bounded sample of the workload at every host
+    core and at one thread (about `seconds` of host time each), with the time
+    a whole step's attention would take at that rate."""
+    full = accounting.step_bytes_for(step).decode
+    out = {}
+    for key, threads in (("all_cores", os.cpu_count() or 1), ("one_thread", 1)):
+        seqs = oracle_sample_plan(step, seconds, threads)
+        dt, nbytes = time_oracle(step, seqs, threads)
+        rate = nbytes / dt
+        out[key] = {"threads": threads, "gbs": round(rate / 1e9, 4),
+                    "step_ms_at_this_rate": round(full / rate * 1e3, 1),
+                    "sample": f"{len(seqs)} of {step.num_seqs} sequences, "
+                              f"{int(step.context_lens[seqs].sum())} rows, {dt:.2f} s"}
+    return out
+
+
 # ---------------------------------------------------------------------------
 # the native (CUDA) arm
 # ---------------------------------------------------------------------------
+
+class DeviceWorkload:
+    """One workload resident on the GPU with its step and attention-call
+    closures. A step is one fused append + decode call for workloads with one
+    query token per sequence and no window (pa_append_decode and its FP8/INT8
+    forms: the decode kernel writes, or quantises, the new rows itself), else
+    the append call followed by the decode call."""
+
+    def __init__(self, pa, step: wl.DecodeStep, dev, kernel: str = "auto"):
+        import torch
+        self.step, self.kernel = step, kernel
+        cd = step.cache_dtype
+        self.fp8, self.int8 = cd == "fp8", cd == "int8"
+
+        def up(a):
+            # bf16 arrays are uint16 bit patterns; FP8 pools stay uint8 codes
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            if a.dtype == np.uint16:
+                t = t.view(torch.bfloat16)
+            return t.to(dev)
+
+        # A step's inputs (q, the new rows, slots, block tables, lengths) live
+        # in one device buffer, 256-byte-aligned regions, so that the
+        # end-to-end step moves them from one pinned host buffer with a single
+        # copy.
+        step_inputs = [step.q, step.k_new, step.v_new, step.slot_mapping, step.block_tables,
+                       step.context_lens]
+        self.in_host, _ = packed_buffer(step_inputs, pin=True)
+        self.in_dev = self.in_host.to(dev)
+        _, (self.q, self.k_new, self.v_new, self.slots, self.tables, self.lens) = \
+            packed_buffer(step_inputs, storage=self.in_dev)
+        self.k_cache, self.v_cache = up(step.k_cache), up(step.v_cache)
+        if self.int8:
+            self.k_rs, self.v_rs = up(step.k_row_scales), up(step.v_row_scales)
+        self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pa.pa_decode_workspace_size_multi(step.num_seqs, step.num_queries, step.num_heads,
+                                               step.head_dim, step.max_context_len)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.pa = pa
+        self.fused = step.num_queries == 1 and step.window == 0
+        # append (not in the fused step), decode, and the split-K merge when a
+        # sequence can span more than one partition (at most 4096 sequences:
+        # one launch each)
+        part = pa.pa_default_partition_size(cd)
+        self.launches_per_step = (1 if self.fused else 2) + \
+            (1 if math.ceil(step.max_context_len / part) > 1 else 0)
+
+    def append(self, st=None):
+        pa, s = self.pa, self.step
+        if self.int8:
+            pa.pa_reshape_and_cache_int8(self.k_new, self.v_new, self.slots, self.k_cache,
+                                         self.v_cache, self.k_rs, self.v_rs,
+                                         error_word=self.err, stream=st)
+        elif self.fp8:
+            pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.slots, self.k_cache,
+                                        self.v_cache, s.k_scale, s.v_scale, error_word=self.err,
+                                        stream=st)
+        else:
+            pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slots, self.k_cache,
+                                    self.v_cache, error_word=self.err, stream=st)
+
+    def decode(self, st=None):
+        pa, s = self.pa, self.step
+        common = dict(workspace=self.workspace, error_word=self.err, stream=st)
+        mcl = s.max_context_len
+        if self.int8:
+            pa.pa_decode_int8(self.q, self.k_cache, self.v_cache, self.k_rs, self.v_rs,
+                              self.tables, self.lens, s.scale, self.out, mcl, **common)
+        elif self.fp8:
+            pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.tables, self.lens, s.scale,
+                             self.out, mcl, s.k_scale, s.v_scale, **common)
+        elif s.num_queries > 1:
+            pa.pa_decode_multi(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
+                               s.scale, self.out, mcl, **common)
+        elif s.window > 0:
+            pa.pa_decode_window(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
+                                s.scale, s.window, self.out, mcl, **common)
+        else:
+            pa.pa_decode(self.q, self.k_cache, self.v_cache, self.tables, self.lens, s.scale,
+                         self.out, mcl, kernel=self.kernel, **common)
+
+    def unfused_step(self, st=None):
+        self.append(st)
+        self.decode(st)
+
+    def run_step(self, st=None):
+        pa, s = self.pa, self.step
+        if not self.fused:
+            return self.unfused_step(st)
+        common = dict(workspace=self.workspace, error_word=self.err, stream=st)
+        args = (self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache)
+        if self.int8:
+            pa.pa_append_decode_int8(*args, self.k_rs, self.v_rs, self.q, self.tables, self.lens,
+                                     s.scale, self.out, s.max_context_len, **common)
+        elif self.fp8:
+            pa.pa_append_decode_fp8(*args, self.q, self.tables, self.lens, s.scale, self.out,
+                                    s.max_context_len, s.k_scale, s.v_scale, **common)
+        else:
+            pa.pa_append_decode(*args, self.q, self.tables, self.lens, s.scale, self.out,
+                                s.max_context_len, **common)
+
+    def capture(self):
+        """CUDA graphs of the step, the attention call alone and the two-call
+        step (launches replayed without host gaps, as a serving loop replays a
+        decode step); they run the same kernels as the eager calls."""
+        import torch
+        self.graph_step, self.graph_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.graph_unfused = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_step):
+            self.run_step(None)
+        with torch.cuda.graph(self.graph_decode):
+            self.decode(None)
+        with torch.cuda.graph(self.graph_unfused):
+            self.unfused_step(None)
+
+    def check_error_word(self, where: str):
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error word {int(self.err.item()):#x} {where}")
+
+
+class L2Flusher:
+    """Between timed steps: evict the step's data (write a buffer larger than
+    L2), then replace the dirty lines with clean ones (read another), so that
+    every timed step starts with an L2 holding none of its data and nothing
+    to write back."""
+
+    def __init__(self, dev):
+        import torch
+        self.dirty = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.clean = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev).view(torch.int32)
+
+    def __call__(self, i: int = 1):
+        self.dirty.fill_(i & 0xff)
+        self.clean.max()
+
+
+def timed_runs(run, reps, flush, stream) -> list[float]:
+    """Milliseconds of `run` per repetition: CUDA events on the launching
+    stream around each one, the L2 flushed before each (outside the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i in range(reps):
+        flush(i)
+        evs[i][0].record(stream)
+        run()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def workload_summary(pa, name: str, args, dev, flush, stream, peak: float,
+                     oracle_seconds: float) -> dict:
+    """Step and attention-call timings of one more workload (graph replays,
+    L2 flushed between them) and the oracle's rate on it."""
+    import torch
+    step = wl.make(name)
+    b = accounting.step_bytes_for(step)
+    w = DeviceWorkload(pa, step, dev)
+    for _ in range(args.warmup):
+        flush()
+        w.run_step(stream)
+    torch.cuda.synchronize()
+    w.check_error_word("during warm-up")
+    w.capture()
+    step_ms = timed_runs(w.graph_step.replay, args.steps, flush, stream)
+    decode_ms = timed_runs(w.graph_decode.replay, args.steps, flush, stream)
+    w.check_error_word("in the timed region")
+    st, dc = sum(step_ms) / len(step_ms), sum(decode_ms) / len(decode_ms)
+    decode_gbs = b.decode / (dc * 1e-3) / 1e9
+    res = {
+        "cache_dtype": step.cache_dtype, "num_seqs": step.num_seqs,
+        "num_queries": step.num_queries, "window": step.window,
+        "total_context_rows": int(step.context_lens.sum()),
+        "step": "fused append + decode call" if w.fused else "append call + decode call",
+        "step_us": round(st * 1e3, 2),
+        "decode_call_us": round(dc * 1e3, 2),
+        "seqs_per_s": round(step.num_seqs / (st * 1e-3), 1),
+        "step_gbs": round(b.total / (st * 1e-3) / 1e9, 2),
+        "kv_gbs": round(b.kv / (st * 1e-3) / 1e9, 2),
+        "decode_call_gbs": round(decode_gbs, 2),
+        "frac_of_measured_hbm": round(decode_gbs / peak, 4),
+        "frac_of_nominal_8tbs": round(decode_gbs / NOMINAL_HBM_GBS, 4),
+        "algorithmic_bytes_per_call": b.decode,
+    }
+    if b.kv_unique != b.kv:
+        res["kv_unique_gbs"] = round(b.kv_unique / (st * 1e-3) / 1e9, 2)
+        res["kv_note"] = "kv_gbs counts each sequence's reads of shared blocks; " \
+                         "kv_unique_gbs counts each physical row once"
+    del w
+    torch.cuda.empty_cache()
+    if oracle_seconds > 0:
+        res["oracle"] = oracle_rates(step, oracle_seconds)
+    return res
+
 
 def run_native(args) -> dict | None:
     import torch
@@ -304,175 +533,60 @@ def run_native(args) -> dict | None:
     step = wl.make(args.workload, seed=wl.WORKLOAD_SEEDS[args.workload] + 1000 * rank)
     bytes_ = accounting.step_bytes_for(step)
     cd = step.cache_dtype
-
-    fp8 = cd == "fp8"
-    int8 = cd == "int8"
-
-    def up(a):
-        # bf16 arrays are uint16 bit patterns; FP8 pools stay uint8 codes
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        if a.dtype == np.uint16:
-            t = t.view(torch.bfloat16)
-        return t.to(dev)
-
-    # A step's inputs (q, the new rows, slots, block tables, lengths) live in
-    # one device buffer, 256-byte-aligned regions, so that the end-to-end step
-    # moves them from one pinned host buffer with a single copy.
-    step_inputs = [step.q, step.k_new, step.v_new, step.slot_mapping, step.block_tables,
-                   step.context_lens]
-    in_host, _ = packed_buffer(step_inputs, pin=True)
-    in_dev = in_host.to(dev)
-    _, (q, k_new, v_new, slots, tables, lens) = packed_buffer(step_inputs, storage=in_dev)
-    k_cache, v_cache = up(step.k_cache), up(step.v_cache)
-    if int8:
-        k_rs, v_rs = up(step.k_row_scales), up(step.v_row_scales)
-    out = torch.empty_like(q)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
     mcl = step.max_context_len
-    Qn = step.num_queries
-    ws_bytes = pa.pa_decode_workspace_size_multi(step.num_seqs, Qn, step.num_heads,
-                                                 step.head_dim, mcl)
-    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_clean = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def flush_l2(i: int = 1):
-        # Evict the step's data (write), then replace the dirty lines with
-        # clean ones (read), outside the timed region.
-        flush.fill_(i & 0xff)
-        flush_clean.view(torch.int32).max()
+    w = DeviceWorkload(pa, step, dev, args.kernel)
+    flush_l2 = L2Flusher(dev)
     stream = torch.cuda.current_stream(dev)
-    # append, decode, and the split-K merge when a sequence spans more than
-    # one 512-row partition (batches of at most 4096 sequences: one launch each)
-    launches_per_step = 2 + (1 if math.ceil(mcl / 512) > 1 else 0)   # unfused; see fused_step
-
-    def do_append(st):
-        if int8:
-            pa.pa_reshape_and_cache_int8(k_new, v_new, slots, k_cache, v_cache, k_rs, v_rs,
-                                         error_word=err, stream=st)
-        elif fp8:
-            pa.pa_reshape_and_cache_fp8(k_new, v_new, slots, k_cache, v_cache, step.k_scale,
-                                        step.v_scale, error_word=err, stream=st)
-        else:
-            pa.pa_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache, error_word=err,
-                                    stream=st)
-
-    def do_decode(st):
-        if int8:
-            pa.pa_decode_int8(q, k_cache, v_cache, k_rs, v_rs, tables, lens, step.scale, out,
-                              mcl, workspace=workspace, error_word=err, stream=st)
-        elif fp8:
-            pa.pa_decode_fp8(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
-                             step.k_scale, step.v_scale, workspace=workspace, error_word=err,
-                             stream=st)
-        elif Qn > 1:
-            pa.pa_decode_multi(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
-                               workspace=workspace, error_word=err, stream=st)
-        elif step.window > 0:
-            pa.pa_decode_window(q, k_cache, v_cache, tables, lens, step.scale, step.window, out,
-                                mcl, workspace=workspace, error_word=err, stream=st)
-        else:
-            pa.pa_decode(q, k_cache, v_cache, tables, lens, step.scale, out, mcl,
-                         workspace=workspace, error_word=err, stream=st, kernel=args.kernel)
-
-    # One decode step. Workloads with one query token per sequence and no
-    # window go through the fused call (pa_append_decode and its FP8/INT8
-    # forms: the decode kernel writes, or quantises, the new rows itself); the
-    # others append, then decode.
-    fused_step = Qn == 1 and step.window == 0
-
-    def do_unfused_step(st=None):
-        do_append(st)
-        do_decode(st)
-
-    def do_step(st=None):
-        if not fused_step:
-            do_unfused_step(st)
-        elif int8:
-            pa.pa_append_decode_int8(k_new, v_new, slots, k_cache, v_cache, k_rs, v_rs, q, tables,
-                                     lens, step.scale, out, mcl, workspace=workspace,
-                                     error_word=err, stream=st)
-        elif fp8:
-            pa.pa_append_decode_fp8(k_new, v_new, slots, k_cache, v_cache, q, tables, lens,
-                                    step.scale, out, mcl, step.k_scale, step.v_scale,
-                                    workspace=workspace, error_word=err, stream=st)
-        else:
-            pa.pa_append_decode(k_new, v_new, slots, k_cache, v_cache, q, tables, lens,
-                                step.scale, out, mcl, workspace=workspace, error_word=err,
-                                stream=st)
 
     for _ in range(args.warmup):
         flush_l2()
-        do_step(stream)
+        w.run_step(stream)
     torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item()):#x} during warm-up")
-
-    # The step and the attention call alone, each captured once as a CUDA graph
-    # (launches replayed without host gaps, as a serving loop replays a decode
-    # step); both run the same kernels as the eager calls.
-    graph_step, graph_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    graph_unfused = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_step):
-        do_step(None)
-    with torch.cuda.graph(graph_decode):
-        do_decode(None)
-    with torch.cuda.graph(graph_unfused):
-        do_unfused_step(None)
+    w.check_error_word("during warm-up")
+    w.capture()
     for _ in range(args.warmup):
         flush_l2()
-        graph_step.replay()
+        w.graph_step.replay()
     torch.cuda.synchronize()
-
-    def timed(run, reps):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(reps)]
-        for i in range(reps):
-            flush_l2(i)
-            evs[i][0].record(stream)
-            run()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
 
     K = args.steps
     # Clock soak: untimed back-to-back steps under the clock sampler, so the
     # clocks reported describe this load, then the timed region.
     soak_steps = 0
     if args.clock_soak_s > 0:
-        soak_steps = max(1, int(args.clock_soak_s / max(1e-4, _quick_step_seconds(graph_step.replay, flush))))
+        soak_steps = max(1, int(args.clock_soak_s /
+                                max(1e-4, _quick_step_seconds(w.graph_step.replay, flush_l2))))
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for _ in range(soak_steps):
-            graph_step.replay()
+            w.graph_step.replay()
         # Timed region: K whole steps (append + attention), graph replays.
-        step_ms = timed(graph_step.replay, K)
+        step_ms = timed_runs(w.graph_step.replay, K, flush_l2, stream)
     if world > 1:
         torch.distributed.barrier()
     total_ms = sum(step_ms)
     # The attention call alone (roofline of the dominant kernel) and the eager
     # step through the Python binding, for reference.
-    decode_ms = timed(graph_decode.replay, K)
+    decode_ms = timed_runs(w.graph_decode.replay, K, flush_l2, stream)
     decode_avg = sum(decode_ms) / K
-    eager_ms = timed(lambda: do_step(stream), K)
-    unfused_ms = timed(graph_unfused.replay, K) if fused_step else step_ms
+    eager_ms = timed_runs(lambda: w.run_step(stream), K, flush_l2, stream)
+    unfused_ms = timed_runs(w.graph_unfused.replay, K, flush_l2, stream) if w.fused else step_ms
     append_ms = sum(a - b for a, b in zip(step_ms, decode_ms)) / K
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
+    w.check_error_word("in the timed region")
 
     # ---- end to end through the public API with host buffers --------------
     # The step's inputs come from one pinned host buffer (the packed layout
     # above), the output goes back to pinned memory.
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = in_host.numel()
+    out_host = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
+    h2d = w.in_host.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        in_dev.copy_(in_host, non_blocking=True)
-        do_step()
-        out_host.copy_(out, non_blocking=True)
+        w.in_dev.copy_(w.in_host, non_blocking=True)
+        w.run_step()
+        out_host.copy_(w.out, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -493,20 +607,21 @@ def run_native(args) -> dict | None:
     # overwrites pool blocks). INT8 pools carry row scales pa_copy_blocks
     # does not move: not measured there.
     copy_info = None
-    if not int8:
+    if not w.int8:
         pairs = min(COPY_PAIRS, step.num_blocks // 2)
         perm = torch.randperm(step.num_blocks, generator=torch.Generator().manual_seed(7))
         mapping = torch.stack([perm[:pairs], perm[pairs:2 * pairs]], dim=1).to(dev)
+
+        def copy():
+            pa.pa_copy_blocks(w.k_cache, w.v_cache, mapping, error_word=w.err, stream=stream)
         for _ in range(args.warmup):
-            pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err, stream=stream)
-        copy_ms = timed(lambda: pa.pa_copy_blocks(k_cache, v_cache, mapping, error_word=err,
-                                                  stream=stream), K)
+            copy()
+        copy_ms = timed_runs(copy, K, flush_l2, stream)
         block_bytes = step.num_kv_heads * step.block_size * step.head_dim * step.elem_bytes
         copy_bytes = pairs * 2 * 2 * block_bytes + pairs * 16   # K and V read + written, pairs
         copy_info = (pairs, copy_bytes, sum(copy_ms) / K)
     torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
+    w.check_error_word("in the timed region")
 
     (total_ms, e2e_total, decode_avg), (all_bytes, all_seqs) = reduce_over_ranks(
         [total_ms, e2e_total, decode_avg], [float(bytes_.total), float(step.num_seqs)], dev)
@@ -518,7 +633,6 @@ def run_native(args) -> dict | None:
     value = all_bytes / (ms_per_step * 1e-3) / 1e9
     decode_gbs = bytes_.decode / (decode_avg * 1e-3) / 1e9
     traffic = profiled_traffic(args.workload, args.kernel)
-    kernel_name = {"auto": "auto", "mma": "mma", "simt": "simt", "generic": "generic"}[args.kernel]
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -530,7 +644,7 @@ def run_native(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3" if fp8 else ("int8 codes, fp32 row scales" if int8 else cd),
+        "dtype": "fp8_e4m3" if w.fp8 else ("int8 codes, fp32 row scales" if w.int8 else cd),
         "data": "synthetic (seeded N(0,1) K/V/q; lengths per the workload recipe)",
         "config": {
             "workload": args.workload,
@@ -539,9 +653,10 @@ def run_native(args) -> dict | None:
             "num_kv_heads": step.num_kv_heads, "head_dim": step.head_dim,
             "block_size": step.block_size, "cache_dtype": cd,
             "total_context_rows": int(step.context_lens.sum()),
-            "max_context_len": mcl, "partition_size": pa.pa_default_partition_size(cd), "kernel": kernel_name,
+            "max_context_len": mcl, "partition_size": pa.pa_default_partition_size(cd),
+            "kernel": args.kernel,
             "step": ("fused append + decode call (new rows written by the decode kernel)"
-                     if fused_step else "append call + decode call"),
+                     if w.fused else "append call + decode call"),
             "l2": "between timed steps a 256 MiB buffer is written, then another 256 MiB read (L2 clean, holding none of the step's data); attended K/V also exceed L2",
             "parallelism": f"replicas x{world} (independent batches per GPU)",
         },
@@ -565,6 +680,7 @@ def run_native(args) -> dict | None:
             "peak": peak,
             "unit": "GB/s",
             "frac": round(decode_gbs / peak, 4),
+            "frac_of_nominal_8tbs": round(decode_gbs / NOMINAL_HBM_GBS, 4),
             "traffic": traffic,
             "algorithmic_bytes_per_call": bytes_.decode,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
@@ -578,7 +694,7 @@ def run_native(args) -> dict | None:
             "transfers": "inputs: one copy of a packed pinned buffer (q, new K/V rows, slots, "
                          "block tables, lengths); output: one copy to pinned memory",
         },
-        "gpu_launches": (launches_per_step - (1 if fused_step else 0)) * K,
+        "gpu_launches": w.launches_per_step * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
         "copy_blocks": None if copy_info is None else {
             "pairs": copy_info[0],
@@ -592,10 +708,28 @@ def run_native(args) -> dict | None:
         },
         "clocks": clocks.summary(),
     }
-    if step.meta.get("unique_blocks") and bytes_.kv_unique != bytes_.kv:
+    if bytes_.kv_unique != bytes_.kv:
         res["kv_unique_gbs"] = round(bytes_.kv_unique / (ms_per_step * 1e-3) / 1e9, 2)
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(step, args.cpu_seconds)
+        res["oracle_one_thread"] = oracle_rates(step, args.workload_oracle_seconds)["one_thread"]
+    if world == 1 and args.all_workloads:
+        del w
+        torch.cuda.empty_cache()
+        table = {}
+        for name in wl.WORKLOADS:
+            if name == args.workload:
+                continue
+            table[name] = workload_summary(
+                pa, name, args, dev, flush_l2, stream, peak,
+                0.0 if args.no_cpu_baseline else args.workload_oracle_seconds)
+        res["workloads"] = table
+        res["workloads_note"] = (
+            "the other workloads, measured after the headline in the same process the same "
+            "way (CUDA-graph replays of the step and of the attention call alone, L2 flushed "
+            "between replays); decode_call_gbs = algorithmic attention bytes / attention call "
+            "time; oracle: the fp64 C oracle's rate on a bounded sample of each workload at "
+            "every host core and at one thread")
     return res
 
 
@@ -657,6 +791,10 @@ def main() -> None:
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle time of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload-oracle-seconds", type=float, default=1.5,
+                    help="host seconds of each per-workload oracle sample (all cores, 1 thread)")
+    ap.add_argument("--all-workloads", action=argparse.BooleanOptionalAction, default=True,
+                    help="also measure every other workload (N=1 only) into `workloads`")
     ap.add_argument("--clock-soak-s", type=float, default=1.0,
                     help="seconds of untimed back-to-back steps under the clock sampler "
                          "before the timed region (0 = none)")

@@ -387,6 +387,68 @@ def prefix_shared(seed: int = WORKLOAD_SEEDS["prefix_shared"], samples: int = 64
                               "blocks_needed": need})
 
 
+# ---- structured inputs for parity at long contexts ------------------------------
+
+def tile_signs(num_tiles: int, head_dim: int) -> np.ndarray:
+    """[num_tiles][head_dim] of +-1: element d of every row of logical tile t
+    (16 rows) is (-1)^popcount(t & (d + 1)), a Walsh function of the tile
+    index. Tiles 2k and 2k + 1 cancel in every odd-mask column and aligned
+    runs of 2^(b+1) tiles cancel in the columns whose mask has lowest bit b,
+    so the mean over a whole sequence is small or exactly zero, while one
+    missing, repeated or re-weighted tile (or run of tiles) moves it by a
+    large multiple of its own size."""
+    t = np.arange(num_tiles, dtype=np.int64)[:, None]
+    m = np.arange(1, head_dim + 1, dtype=np.int64)[None, :]
+    odd = np.bitwise_count(t & m) & 1
+    return (1 - 2 * odd).astype(np.int8)
+
+
+_BF16_ONE, _BF16_MINUS_ONE = np.uint16(0x3F80), np.uint16(0xBF80)
+
+
+def structured_long(variant: str = "uniform", lens=(100_000,) + (1_500,) * 7,
+                    seed: int = WORKLOAD_SEEDS["long_skew"],
+                    partition_rows: int = 512) -> DecodeStep:
+    """long_skew's shape (bf16, Hq=32, Hkv=8, d=128) with structured K and V
+    in every attended row (the rest of the pool stays random):
+      V  row i of sequence s, KV head h: (-1)^(s + h) * tile_signs[i // 16]
+      K  "uniform": all zero, so every row gets the same softmax weight;
+         "weighted": zero except element 0, which is 0.5 * ((5 p + s) mod 4)
+         for the rows of chunk p = i // partition_rows, with q's element 0
+         set to 8 and its others to 0, so the weight is constant within a
+         chunk and differs between chunks (up to e^1.06 apart).
+    The step's new rows (k_new, v_new) carry the same pattern for row n - 1."""
+    if variant not in ("uniform", "weighted"):
+        raise ValueError(f"unknown variant {variant!r}")
+    step = build_step(f"structured_{variant}", list(lens), num_heads=32, num_kv_heads=8,
+                      head_dim=128, seed=seed)
+    bs, D, Hkv, G = step.block_size, step.head_dim, step.num_kv_heads, 32 // 8
+    signs_h = np.array([1 if h % 2 == 0 else -1 for h in range(Hkv)], np.int8)
+    c_bits = round_to_bf16_bits(np.array([0.0, 0.5, 1.0, 1.5], np.float32))
+    if variant == "weighted":
+        step.q[...] = 0
+        step.q[:, :, 0] = round_to_bf16_bits(np.array([8.0], np.float32))[0]
+    for s, n in enumerate(step.context_lens):
+        n = int(n)
+        if n == 0:
+            continue
+        nt = (n + bs - 1) // bs
+        blocks = step.block_tables[s, :nt]
+        sg = tile_signs(nt, D)[:, None, :] * signs_h[None, :, None] * (1 if s % 2 == 0 else -1)
+        vbits = np.where(sg > 0, _BF16_ONE, _BF16_MINUS_ONE)          # [nt][Hkv][D]
+        step.v_cache[blocks] = vbits[:, :, None, :]
+        step.k_cache[blocks] = 0
+        last = n - 1
+        step.v_new[s] = vbits[last // bs]
+        step.k_new[s] = 0
+        if variant == "weighted":
+            chunk = (np.arange(nt * bs) // partition_rows).reshape(nt, bs)
+            cbits = c_bits[(5 * chunk + s) % 4]                         # [nt][bs]
+            step.k_cache[blocks, :, :, 0] = cbits[:, None, :]
+            step.k_new[s, :, 0] = c_bits[(5 * (last // partition_rows) + s) % 4]
+    step.meta = dict(step.meta, structured=variant, partition_rows=partition_rows)
+    return step
+
 WORKLOADS = {
     "tiny": tiny,
     "7b_mha": mha_7b,

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, DeviceStep, from_torch, max_abs, oracle_reference
+from gpu_helpers import DeviceStep, assert_parity, from_torch, oracle_reference
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -63,7 +63,7 @@ def test_fused_step_equals_append_then_decode(dtype, hq, hkv, d, bs):
     np.testing.assert_array_equal(from_torch(fused.k_cache), k_ref)
     np.testing.assert_array_equal(from_torch(fused.v_cache), v_ref)
     np.testing.assert_array_equal(from_torch(fused.out), from_torch(two.out))
-    assert max_abs(fused.result(), out_ref) <= TOL[dtype]
+    assert_parity(fused.result(), out_ref, dtype)
 
 
 def test_negative_slots_append_nothing():
@@ -76,7 +76,7 @@ def test_negative_slots_append_nothing():
     assert fused.error_word() == 0
     np.testing.assert_array_equal(from_torch(fused.k_cache), k_ref)
     np.testing.assert_array_equal(from_torch(fused.v_cache), v_ref)
-    assert max_abs(fused.result(), out_ref) <= TOL["bf16"]
+    assert_parity(fused.result(), out_ref, "bf16")
 
 
 def test_slot_of_another_row_is_flagged_and_not_written():
@@ -99,7 +99,7 @@ def test_slot_of_another_row_is_flagged_and_not_written():
                                                          -1, step.slot_mapping))
     _, _, out_ref = oracle_reference(ok)
     keep = [0, 2, 4]
-    assert max_abs(fused.result()[keep], out_ref[keep]) <= TOL["bf16"]
+    assert_parity(fused.result()[keep], out_ref[keep], "bf16")
 
 
 def _u8(a):
@@ -197,7 +197,7 @@ def _check_quantised_fused(fmt, step):
         np.testing.assert_array_equal(got.view(np.uint8), np.ascontiguousarray(ref).view(np.uint8))
     np.testing.assert_array_equal(from_torch(fused["out"]), from_torch(two["out"]))
     got = wl.as_f32(from_torch(fused["out"]), "bf16").astype(np.float64)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 @pytest.mark.parametrize("name", ["8b_gqa", "7b_mha", "long_skew", "prefix_shared"])
@@ -212,7 +212,7 @@ def test_fused_step_on_full_workloads(name):
     np.testing.assert_array_equal(from_torch(fused.k_cache), k_ref)
     np.testing.assert_array_equal(from_torch(fused.v_cache), v_ref)
     np.testing.assert_array_equal(from_torch(fused.out), from_torch(two.out))
-    assert max_abs(fused.result(), out_ref) <= TOL[step.cache_dtype]
+    assert_parity(fused.result(), out_ref, step.cache_dtype)
 
 
 def test_fused_steps_in_a_row_follow_the_oracle():
@@ -254,7 +254,7 @@ def test_fused_steps_in_a_row_follow_the_oracle():
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-        assert max_abs(got, ref) <= TOL["bf16"]
+        assert_parity(got, ref, "bf16")
         assert np.array_equal(from_torch(kd), k) and np.array_equal(from_torch(vd), v)
 
 

@@ -9,7 +9,7 @@ import subprocess
 import numpy as np
 import pytest
 
-from gpu_helpers import TOL, max_abs, oracle_reference
+from gpu_helpers import assert_parity, oracle_reference
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -52,4 +52,4 @@ def test_c_program_decodes_the_tiny_workload(tmp_path):
     assert run.returncode == 0, (run.returncode, run.stderr)
     got = np.fromfile(out, dtype=np.float32).reshape(B, Hq, D).astype(np.float64)
     _, _, ref = oracle_reference(step)
-    assert max_abs(got, ref) <= TOL["f32"]
+    assert_parity(got, ref, "f32")

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, max_abs, to_torch
 import oracle
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
@@ -130,7 +130,7 @@ def test_fork_copy_append_decode_follows_the_oracle():
     np.testing.assert_array_equal(from_torch(kd), wk)
     np.testing.assert_array_equal(from_torch(vd), wv)
     got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
     # the four sequences now differ only in their last row
     assert max_abs(want[0], want[1]) > 0
 

@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import TOL, assert_parity, from_torch, max_abs, to_torch
+from parity import assert_scaled
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -55,8 +56,7 @@ def test_fp8_workload_append_and_decode():
     assert int(d["err"].item()) == 0
     np.testing.assert_array_equal(d["k"].cpu().numpy(), k)
     np.testing.assert_array_equal(d["v"].cpu().numpy(), v)
-    err = max_abs(got, want)
-    assert err <= TOL["bf16"], err
+    assert_parity(got, want, "bf16", "8b_gqa_fp8")
 
 
 @pytest.mark.parametrize("new_dtype", ["bf16", "f32"])
@@ -90,8 +90,13 @@ def test_fp8_ragged_groups_and_scales(hq, hkv, k_scale, v_scale):
     step = wl.build_step("fp8r", lens, hq, hkv, 128, cache_dtype="fp8", seed=hq + hkv)
     _, got = _gpu_step(step, k_scale, v_scale)
     _, _, want = _oracle_step(step, k_scale, v_scale)
+    # The output is v_scale times an attention over e4m3 values: the absolute
+    # bar, stated for outputs of unit-size values, grows with v_scale above 1
+    # (bf16 rounding of a 3x larger output is 3x larger); the output-scaled
+    # bound needs no such change.
     err = max_abs(got, want)
     assert err <= TOL["bf16"] * max(1.0, v_scale), err
+    assert_scaled(got, want, "bf16", f"fp8 {hq}/{hkv} scales {k_scale}, {v_scale}")
 
 
 def test_fp8_nan_codes_past_the_end_do_not_leak():
@@ -106,7 +111,7 @@ def test_fp8_nan_codes_past_the_end_do_not_leak():
     _, got = _gpu_step(step, append=False)
     _, _, want = _oracle_step(step, append=False)
     assert np.isfinite(got).all()
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 def test_fp8_batch_invariance():

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -52,7 +52,7 @@ def test_int8_workload_append_and_decode():
     assert err == 0
     for d, w in zip(dev, pools):
         np.testing.assert_array_equal(d.cpu().numpy(), w)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 @pytest.mark.parametrize("new_dtype", ["bf16", "f32"])
@@ -89,7 +89,7 @@ def test_int8_ragged_groups(hq, hkv):
     _, got, err = _gpu_step(step)
     _, want = _oracle_step(step)
     assert err == 0
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 def test_int8_garbage_scales_past_the_end_do_not_leak():
@@ -104,7 +104,7 @@ def test_int8_garbage_scales_past_the_end_do_not_leak():
     _, got, _ = _gpu_step(step, append=False)
     _, want = _oracle_step(step, append=False)
     assert np.isfinite(got).all()
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 def test_int8_batch_invariance():

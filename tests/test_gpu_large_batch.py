@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, DeviceStep, from_torch, max_abs, oracle_reference, to_torch
+from gpu_helpers import DeviceStep, assert_parity, from_torch, oracle_reference, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -44,7 +44,7 @@ def test_large_batch_two_calls_and_fused():
     for dev in (two, fused):
         np.testing.assert_array_equal(from_torch(dev.k_cache), k_ref)
         np.testing.assert_array_equal(from_torch(dev.v_cache), v_ref)
-        assert max_abs(dev.result(), out_ref) <= TOL["bf16"]
+        assert_parity(dev.result(), out_ref, "bf16")
     np.testing.assert_array_equal(from_torch(fused.out), from_torch(two.out))
 
 
@@ -80,4 +80,4 @@ def test_large_batch_quantised_fused(fmt):
         np.testing.assert_array_equal(dev.cpu().numpy().view(np.uint8),
                                       np.ascontiguousarray(ref).view(np.uint8))
     got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -43,7 +43,7 @@ def test_multi_query_workload():
     step = wl.make("8b_gqa_mq2")
     got, err = _gpu(step)
     assert err == 0
-    assert max_abs(got, _oracle(step)) <= TOL["bf16"]
+    assert_parity(got, _oracle(step), "bf16")
 
 
 @pytest.mark.parametrize("hq,hkv,Q,d", [(8, 8, 2, 128), (8, 8, 3, 64), (16, 8, 3, 128),
@@ -54,7 +54,7 @@ def test_multi_query_ragged(hq, hkv, Q, d):
     step = wl.build_step("mq", lens, hq, hkv, d, seed=hq * 10 + Q, num_queries=Q)
     got, err = _gpu(step)
     assert err == 0
-    assert max_abs(got, _oracle(step)) <= TOL["bf16"]
+    assert_parity(got, _oracle(step), "bf16")
 
 
 def test_single_query_matches_pa_decode_bitwise():
@@ -94,7 +94,7 @@ def test_multi_query_empty_and_short_sequences():
     assert err == 0
     assert not got[0].any() and not got[2].any()
     want = _oracle(step)
-    assert max_abs(got[[1, 3]], want[[1, 3]]) <= TOL["bf16"]
+    assert_parity(got[[1, 3]], want[[1, 3]], "bf16")
     # a sequence shorter than its query tokens is flagged
     step.context_lens[1] = 1
     _, err = _gpu(step, append=False)

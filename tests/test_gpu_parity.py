@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import TOL, DeviceStep, from_torch, max_abs, oracle_reference
+from gpu_helpers import DeviceStep, assert_parity, from_torch, oracle_reference
+from parity import assert_elements
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -37,9 +38,8 @@ def test_named_workload_append_and_decode(name):
         if kernel == "auto":   # the append is bit-exact: compare whole pools
             assert np.array_equal(from_torch(dev.k_cache), k_ref)
             assert np.array_equal(from_torch(dev.v_cache), v_ref)
-        err = max_abs(out, out_ref)
-        assert err <= TOL[step.cache_dtype], f"{name}/{kernel}: max-abs {err}"
         assert np.isfinite(out).all()
+        assert_parity(out, out_ref, step.cache_dtype, f"{name}/{kernel}")
 
 
 def ragged_step(dtype, hq, hkv, d, bs=16, lens=None, seed=0):
@@ -57,7 +57,7 @@ def test_ragged_shapes_all_kernels(dtype, hq, hkv, d):
         dev = DeviceStep(step)
         out = dev.run(kernel)
         assert dev.error_word() == 0
-        assert max_abs(out, ref) <= TOL[dtype], kernel
+        assert_parity(out, ref, dtype, kernel)
 
 
 @pytest.mark.parametrize("partition", [16, 48, 64, 512, 1024, 4096])
@@ -67,7 +67,7 @@ def test_partition_sizes(partition):
     for kernel in ["mma", "simt", "generic"]:
         dev = DeviceStep(step, partition_size=partition)
         out = dev.run(kernel)
-        assert max_abs(out, ref) <= TOL["bf16"], (kernel, partition)
+        assert_parity(out, ref, "bf16", (kernel, partition))
 
 
 @pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64])
@@ -77,10 +77,10 @@ def test_block_sizes(bs):
     dev = DeviceStep(step)
     out = dev.run("auto")
     assert np.array_equal(from_torch(dev.k_cache), k_ref)
-    assert max_abs(out, ref) <= TOL["bf16"]
+    assert_parity(out, ref, "bf16")
     if bs % 16 == 0:
         dev2 = DeviceStep(step)
-        assert max_abs(dev2.run("simt"), ref) <= TOL["bf16"]
+        assert_parity(dev2.run("simt"), ref, "bf16")
 
 
 def test_garbage_rows_do_not_leak():
@@ -101,7 +101,7 @@ def test_garbage_rows_do_not_leak():
         for kernel in KERNELS_FOR[dtype][1:]:
             out = DeviceStep(step).run(kernel)
             assert np.isfinite(out).all(), kernel
-            assert max_abs(out, ref) <= TOL[dtype], kernel
+            assert_parity(out, ref, dtype, kernel)
 
 
 def _run_subset(step, dev, idx, kernel):
@@ -166,7 +166,7 @@ def test_empty_sequences_give_zeros():
         dev.out.fill_(7.0)
         out = dev.run(kernel)
         assert np.all(out[[0, 2, 4]] == 0.0)
-        assert max_abs(out, ref) <= TOL["bf16"]
+        assert_parity(out, ref, "bf16")
 
 
 def test_device_errors_are_flagged_not_faulted():
@@ -182,7 +182,7 @@ def test_device_errors_are_flagged_not_faulted():
         torch.cuda.synchronize()
         assert dev.error_word() & pa.PA_DEVERR_BLOCK_ID, kernel
         out = dev.result()
-        assert max_abs(out[[0, 2]], ref[[0, 2]]) <= TOL["bf16"]
+        assert_parity(out[[0, 2]], ref[[0, 2]], "bf16")
     dev = DeviceStep(step)
     dev.append()
     dev.lens[2] = 10_000                           # past max_context_len
@@ -252,5 +252,44 @@ def test_incremental_steps_follow_the_oracle():
                      1 / np.sqrt(d), out, int(lens.max()))
         torch.cuda.synchronize()
         got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-        assert max_abs(got, ref) <= TOL["bf16"]
+        assert_parity(got, ref, "bf16")
         assert np.array_equal(from_torch(kd), k) and np.array_equal(from_torch(vd), v)
+
+
+# Element bound for the structured inputs (checked for sensitivity on the CPU
+# in tests/test_parity_bounds.py): one bf16 ulp of the element plus 2^-16 of
+# the row's largest element for the fp32 weight arithmetic.
+STRUCT_ULPS, STRUCT_REL = 1.0, 2.0 ** -16
+
+
+@pytest.mark.parametrize("variant", ["uniform", "weighted"])
+def test_structured_long_context(variant):
+    """long_skew's shape (one 100,000-row sequence, seven of 1,500) with V
+    rows that carry a Walsh pattern of their tile index and K rows that give
+    every row the same weight ("uniform") or a different weight per 512-row
+    chunk ("weighted"). Many output elements are then exactly zero, and a
+    dropped, repeated or re-weighted tile or partition moves them far past
+    the element bound (tests/test_parity_bounds.py shows this on the CPU).
+    The 100,000-row sequence spans well over 32 partitions, so its heads go
+    through the merge kernel's multi-warp branch."""
+    step = wl.structured_long(variant)
+    assert -(-100_000 // pa.pa_default_partition_size("bf16")) > 32
+    k_ref, v_ref, ref = oracle_reference(step)
+    runs = {}
+    for kernel in ("auto", "simt"):
+        dev = DeviceStep(step)
+        runs[kernel] = dev.run(kernel)
+        assert dev.error_word() == 0
+        if kernel == "auto":
+            assert np.array_equal(from_torch(dev.k_cache), k_ref)
+            assert np.array_equal(from_torch(dev.v_cache), v_ref)
+    fused = DeviceStep(step)
+    pa.pa_append_decode(fused.k_new, fused.v_new, fused.slots, fused.k_cache, fused.v_cache,
+                        fused.q, fused.tables, fused.lens, step.scale, fused.out,
+                        step.max_context_len, workspace=fused.workspace, error_word=fused.err)
+    torch.cuda.synchronize()
+    assert fused.error_word() == 0
+    runs["fused"] = fused.result()
+    for what, out in runs.items():
+        assert_elements(out, ref, "bf16", STRUCT_ULPS, STRUCT_REL, f"{variant}/{what}")
+        assert_parity(out, ref, "bf16", f"{variant}/{what}")

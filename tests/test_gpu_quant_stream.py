@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -74,7 +74,7 @@ def test_work_list_shapes(fmt, case):
     assert err == 0
     empty = [s for s, n in enumerate(lens) if n == 0]
     assert np.all(got[empty] == 0.0)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -88,11 +88,11 @@ def test_bad_block_id_mid_stream_is_flagged(fmt):
     got, err = _run(fmt, step, tables=bad)
     assert err & pa.PA_DEVERR_BLOCK_ID
     ok = [0, 2, 3, 5]
-    assert max_abs(got[ok], want[ok]) <= TOL["bf16"]
+    assert_parity(got[ok], want[ok], "bf16")
     # The next call on a clean table is exact again (no state carried over).
     got, err = _run(fmt, step)
     assert err == 0
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 @pytest.mark.parametrize("mcl", [0, 16])
@@ -138,4 +138,4 @@ def test_larger_blocks(fmt, bs):
                          seed=35 + bs)
     got, err = _run(fmt, step)
     assert err == 0
-    assert max_abs(got, _reference(fmt, step)) <= TOL["bf16"]
+    assert_parity(got, _reference(fmt, step), "bf16")

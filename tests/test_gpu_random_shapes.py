@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, DeviceStep, from_torch, max_abs, oracle_reference, to_torch
+from gpu_helpers import DeviceStep, assert_parity, from_torch, oracle_reference, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -41,7 +41,7 @@ def test_random_shape(i):
     out = dev.run("auto")
     assert dev.error_word() == 0, (i, dtype, hq, hkv, d, bs, part, lens)
     np.testing.assert_array_equal(from_torch(dev.k_cache), k_ref)
-    assert max_abs(out, ref) <= TOL[dtype], (i, dtype, hq, hkv, d, bs, part, lens)
+    assert_parity(out, ref, dtype, (i, dtype, hq, hkv, d, bs, part, lens))
     if part == 0:
         fused = DeviceStep(step)
         pa.pa_append_decode(fused.k_new, fused.v_new, fused.slots, fused.k_cache, fused.v_cache,
@@ -51,7 +51,7 @@ def test_random_shape(i):
         torch.cuda.synchronize()
         assert fused.error_word() == 0
         np.testing.assert_array_equal(from_torch(fused.k_cache), k_ref)
-        assert max_abs(fused.result(), ref) <= TOL[dtype]
+        assert_parity(fused.result(), ref, dtype)
 
 
 @pytest.mark.parametrize("i", range(12))
@@ -97,7 +97,7 @@ def test_random_shape_8bit(i):
         np.testing.assert_array_equal(got.cpu().numpy().view(np.uint8),
                                       np.ascontiguousarray(ref).view(np.uint8))
     got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-    assert max_abs(got, want) <= TOL["bf16"], (i, fmt, g, hkv, bs, lens)
+    assert_parity(got, want, "bf16", (i, fmt, g, hkv, bs, lens))
 
 
 @pytest.mark.parametrize("i", range(10))
@@ -116,7 +116,7 @@ def test_random_window(i):
                          block_size=bs, seed=int(rng.integers(1 << 30)))
     got, err = tw._gpu(step, window)
     assert err == 0, (i, dtype, hq, hkv, d, bs, window, list(lens))
-    assert max_abs(got, tw._oracle(step, window)) <= TOL[dtype], (i, window)
+    assert_parity(got, tw._oracle(step, window), dtype, (i, window))
 
 
 @pytest.mark.parametrize("i", range(10))
@@ -134,4 +134,4 @@ def test_random_multi_query(i):
                          seed=int(rng.integers(1 << 30)), num_queries=Q)
     got, err = tm._gpu(step)
     assert err == 0, (i, Q, g, hkv, d, bs, list(lens))
-    assert max_abs(got, tm._oracle(step)) <= TOL["bf16"], (i, Q, g)
+    assert_parity(got, tm._oracle(step), "bf16", (i, Q, g))

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -62,7 +62,7 @@ def test_withheld_tile_times_out_and_context_stays_usable(fmt):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     got = wl.as_f32(from_torch(out), "bf16").astype(np.float64)
-    assert max_abs(got, want) <= TOL["bf16"]
+    assert_parity(got, want, "bf16")
 
 
 def test_withhold_past_the_stream_changes_nothing():
@@ -77,4 +77,4 @@ def test_withhold_past_the_stream_changes_nothing():
     assert int(err.item()) == 0
     want = oracle.decode(step.q, step.k_cache, step.v_cache, step.block_tables,
                          step.context_lens, step.scale)
-    assert max_abs(wl.as_f32(from_torch(out), "bf16").astype(np.float64), want) <= TOL["bf16"]
+    assert_parity(wl.as_f32(from_torch(out), "bf16").astype(np.float64), want, "bf16")

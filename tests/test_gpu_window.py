@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, from_torch, max_abs, to_torch
+from gpu_helpers import assert_parity, from_torch, to_torch
 from paged_kv_cache_29_gb300 import _binding as pa
 from paged_kv_cache_29_gb300 import workloads as wl
 
@@ -42,7 +42,7 @@ def test_window_workload():
     step = wl.make("8b_gqa_win1024")
     got, err = _gpu(step, step.window)
     assert err == 0
-    assert max_abs(got, _oracle(step, step.window)) <= TOL["bf16"]
+    assert_parity(got, _oracle(step, step.window), "bf16")
 
 
 LENS = [1, 15, 16, 17, 100, 511, 512, 513, 1000, 1025, 2049, 5000]
@@ -55,7 +55,7 @@ def test_window_ragged(dtype, hq, hkv, d, window):
     step = wl.build_step("win", LENS, hq, hkv, d, cache_dtype=dtype, seed=window + hq)
     got, err = _gpu(step, window)
     assert err == 0
-    assert max_abs(got, _oracle(step, window)) <= TOL[dtype]
+    assert_parity(got, _oracle(step, window), dtype)
 
 
 def test_window_past_every_sequence_equals_pa_decode_bitwise():
