@@ -397,6 +397,17 @@ typedef struct pa_decode_options {
     int kernel;          /* a pa_kernel value */
     int partition_size;  /* rows per split-K partition: a multiple of 16, 16..4096;
                             0 = pa_default_partition_size(dtype) */
+    /* Optional larger partitions for long sequences: a sequence whose
+     * partitions cover more than long_partition_from rows (its context length,
+     * or for a sliding window the rows from the tile holding the window's
+     * first row) is split into partitions of long_partition_size rows (a
+     * multiple of 16, partition_size..4096). The choice depends on the
+     * sequence's own length only, so its result stays independent of the rest
+     * of the batch. 0 (the default) = one partition size for all. Measured on
+     * the bench workloads it is no faster: fewer, larger items balance worse
+     * across the persistent CTAs than they save in per-item work. */
+    int long_partition_size;
+    int long_partition_from;
 } pa_decode_options;
 
 /* pa_decode with explicit options (NULL = defaults). The workspace must be

@@ -43,7 +43,8 @@ class PagedAttentionError(RuntimeError):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("partition_size", ctypes.c_int)]
+    _fields_ = [("kernel", ctypes.c_int), ("partition_size", ctypes.c_int),
+                ("long_partition_size", ctypes.c_int), ("long_partition_from", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -512,13 +513,16 @@ def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
 
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
               workspace=None, error_word=None, stream=None, kernel: str = "auto",
-              partition_size: int = 0) -> None:
+              partition_size: int = 0, long_partition_size: int = 0,
+              long_partition_from: int = 0) -> None:
     """Decode attention for every sequence, written into ``out`` ([B][Hq][D]).
 
     max_context_len bounds context_lens (host value; sizes the work list and
     the workspace). workspace: a CUDA tensor of at least
     pa_decode_workspace_size(...) bytes; when None, one is allocated from
-    torch's caching allocator for this call."""
+    torch's caching allocator for this call. long_partition_size /
+    long_partition_from: partitions of that many rows for sequences longer
+    than long_partition_from rows (0 = one size for all)."""
     import torch
     _check_cuda("k_cache", k_cache, ndim=4)
     _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
@@ -542,7 +546,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_c
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check_cuda("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
-    opts = _Options(KERNELS[kernel], int(partition_size))
+    opts = _Options(KERNELS[kernel], int(partition_size), int(long_partition_size),
+                    int(long_partition_from))
     rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             _ptr(context_lens), float(scale), _ptr(out), B, hq, hkv, d, bs, nb,
                             int(block_tables.shape[1]), int(max_context_len),

@@ -134,6 +134,10 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         return PA_ERR_INVALID_ARG;
     if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
     if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
+    if (options && options->long_partition_from != 0 &&
+        (options->long_partition_from < 0 || options->long_partition_size < partition ||
+         options->long_partition_size > 4096 || options->long_partition_size % 16 != 0))
+        return PA_ERR_INVALID_ARG;
     if (!(scale == scale)) return PA_ERR_INVALID_ARG;   // NaN scale
     if (head_dim > pa::kMaxHeadDim) return PA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_context_len) >
@@ -194,9 +198,11 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
                (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group, 1))) {
         return PA_ERR_UNSUPPORTED;
     }
+    const int largest_partition =
+        (options && options->long_partition_from > 0) ? options->long_partition_size : partition;
     if (kernel == PA_KERNEL_GENERIC &&
         (window > 0 ||   // the direct-load kernel has no sliding window
-         pa::generic_smem_bytes(group, head_dim, partition, block_size) > kMaxDynamicSmem))
+         pa::generic_smem_bytes(group, head_dim, largest_partition, block_size) > kMaxDynamicSmem))
         return PA_ERR_UNSUPPORTED;
 
     // Fused append: the in-order tile-ring kernels write each sequence's new
@@ -236,6 +242,12 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
     base.max_blocks_per_seq = max_blocks_per_seq;
     base.context_cap = max_context_len;
     base.partition_size = partition;
+    // Larger partitions for long sequences by default (tile-ring kernels); an
+    // explicit partition size, and the direct-load kernel, keep one size.
+    // Optional larger partitions for long sequences (checked above).
+    const bool tiered = options && options->long_partition_from > 0;
+    base.partition_long = tiered ? options->long_partition_size : partition;
+    base.partition_long_from = tiered ? options->long_partition_from : pa::kNoLongPartitions;
     base.max_parts = static_cast<int>(max_parts);
 
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -320,6 +332,8 @@ int pa_default_partition_size(pa_dtype cache_dtype) {
     if (!valid_decode_cache_dtype(cache_dtype)) return 0;
     return cache_dtype == PA_DTYPE_FP8_E4M3 ? pa::kDefaultPartition8 : pa::kDefaultPartition;
 }
+
+
 
 size_t pa_decode_workspace_size_ex(int num_seqs, int num_heads, int head_dim,
                                    int max_context_len, int partition_size) {

@@ -45,10 +45,10 @@ decode_generic_kernel(const DecodeParams p, int group) {
     using E = ElemTraits<T>;
     extern __shared__ float sm[];
     const int D = p.head_dim;
-    const int P = p.partition_size;
+    const int PS = max(p.partition_size, p.partition_long);   // score row stride
     float* qf = sm;                           // [group][D]
-    float* sc = qf + group * D;               // [group][P]
-    float* red = sc + group * P;              // [group][2]: max, sum
+    float* sc = qf + group * D;               // [group][PS]
+    float* red = sc + group * PS;             // [group][2]: max, sum
     int32_t* ids = reinterpret_cast<int32_t*>(red + 2 * group);   // partition's block ids
     __shared__ int bad;
 
@@ -62,6 +62,7 @@ decode_generic_kernel(const DecodeParams p, int group) {
         if (threadIdx.x == 0 && part == 0 && h == 0) raise_error(p.error_word, PA_DEVERR_CONTEXT);
         return;
     }
+    const int P = seq_partition(p, n);        // rows per partition of this sequence
     const int lo = part * P;
     const size_t row0 = static_cast<size_t>(s) * p.num_heads + static_cast<size_t>(h) * group;
     if (n == 0) {
@@ -109,19 +110,19 @@ decode_generic_kernel(const DecodeParams p, int group) {
             float acc = 0.f;
             for (int d = lane; d < D; d += 32) acc = fmaf(qf[g * D + d], E::load(krow + d), acc);
             acc = warp_sum(acc);
-            if (lane == 0) sc[g * P + i] = acc;
+            if (lane == 0) sc[g * PS + i] = acc;
         }
     }
     __syncthreads();
     // softmax per query head: one warp per head
     for (int g = warp; g < group; g += nwarps) {
         float mx = -INFINITY;
-        for (int i = lane; i < len; i += 32) mx = fmaxf(mx, sc[g * P + i]);
+        for (int i = lane; i < len; i += 32) mx = fmaxf(mx, sc[g * PS + i]);
         mx = warp_max(mx);
         float sum = 0.f;
         for (int i = lane; i < len; i += 32) {
-            const float e = fast_exp2(sc[g * P + i] - mx);
-            sc[g * P + i] = e;
+            const float e = fast_exp2(sc[g * PS + i] - mx);
+            sc[g * PS + i] = e;
             sum += e;
         }
         sum = warp_sum(sum);
@@ -135,7 +136,7 @@ decode_generic_kernel(const DecodeParams p, int group) {
     for (int idx = threadIdx.x; idx < group * D; idx += blockDim.x) {
         const int g = idx / D, d = idx - g * D;
         float acc = 0.f;
-        for (int i = 0; i < len; ++i) acc = fmaf(sc[g * P + i], E::load(vc + row_of(i) + d), acc);
+        for (int i = 0; i < len; ++i) acc = fmaf(sc[g * PS + i], E::load(vc + row_of(i) + d), acc);
         const size_t row = row0 + g;
         if (nparts == 1) {
             E::store(static_cast<T*>(p.out) + row * D + d, acc / red[2 * g + 1]);
@@ -190,8 +191,8 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(const De
     // (0, 0) always waits, so that this grid never completes before the
     // decode kernel does.
     const int n = __ldg(p.context_lens + s);
-    const int P = p.partition_size;
     const int span = n - seq_row_base(n, p.window);       // rows of the partitions
+    const int P = seq_partition(p, span);
     const bool merge = n <= p.context_cap && n >= p.num_queries && span > P;   // else flagged or one partition
     if (!merge && (blockIdx.x | blockIdx.y) != 0) return;
     asm volatile("griddepcontrol.wait;" ::: "memory");    // the partials are the decode kernel's output
@@ -296,7 +297,8 @@ size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block
 
 cudaError_t launch_decode_generic(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream) {
     const int group = p.num_heads / p.num_kv_heads;
-    const size_t smem = generic_smem_bytes(group, p.head_dim, p.partition_size, p.block_size);
+    const size_t smem = generic_smem_bytes(group, p.head_dim,
+                                           max(p.partition_size, p.partition_long), p.block_size);
     const long long grid = static_cast<long long>(p.max_parts) * p.num_seqs * p.num_kv_heads;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -163,8 +163,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (k >= total) return make_int4(-1, 0, 0, 0);
         return j < 2 ? first_items[j] : p.items[k];
     };
-    const int P = p.partition_size;
     const int bs = p.block_size;
+    // Rows per partition of the sequence an item belongs to (n rows).
+    auto part_rows = [&](int n) { return seq_partition(p, n - seq_row_base(n, p.window)); };
     const uint32_t ring_addr = smem_addr(ring);
 
     if (warp == W) {
@@ -200,6 +201,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // first block, tiles, tiles per consumer warp, first stream index, bad.
             auto request = [&]() {
                 const int4 it = d_req;
+                const int P = part_rows(it.w);
                 const int lo = seq_row_base(it.w, p.window) + it.z * P;
                 const int hi = min(it.w, lo + P);
                 const int b0 = lo / bs;
@@ -248,7 +250,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if constexpr (Math::kQuantAppend) {
                     const int4 it = d_val;
                     const int lo = m[2];
-                    if (p.k_new != nullptr && !bad && min(it.w, lo + P) == it.w) {
+                    if (p.k_new != nullptr && !bad && min(it.w, lo + part_rows(it.w)) == it.w) {
                         const long long slot = __ldg(p.slot_mapping + it.x);
                         if (slot >= 0) {
                             const int r = it.w - 1;
@@ -412,6 +414,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // with cp.async one item ahead of their use.
             auto prefetch_ids = [&](const int4& it, int32_t* buf) {
                 if (it.x >= 0) {
+                    const int P = part_rows(it.w);
                     const int lo = seq_row_base(it.w, p.window) + it.z * P;
                     const int hi = min(it.w, lo + P);
                     const int b0 = lo / bs;
@@ -433,6 +436,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
                 cp_async_wait_group_1();                // this item's ids have landed
                 __syncwarp();
+                const int P = part_rows(cur.w);
                 const int lo = seq_row_base(cur.w, p.window) + cur.z * P;
                 const int hi = min(cur.w, lo + P);
                 const int b0 = lo / bs;
@@ -596,6 +600,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int j = 0; it.x >= 0; ++j) {
         const int s = it.x, h = it.y, part = it.z, n = it.w;
         const int base = seq_row_base(n, p.window);
+        const int P = seq_partition(p, n - base);
         const int lo = base + part * P;
         const int hi = min(n, lo + P);
         const int ntiles = (hi - lo + kTileRows - 1) / kTileRows;

@@ -44,8 +44,10 @@ struct DecodeParams {
     int num_blocks;
     int max_blocks_per_seq;
     int context_cap;               // min(max_context_len, max_blocks_per_seq * block_size)
-    int partition_size;
-    int max_parts;                 // ceil(max_context_len / partition_size), >= 1
+    int partition_size;            // rows per partition (seq_partition: of shorter sequences)
+    int partition_long;            // rows per partition of sequences past partition_long_from
+    int partition_long_from;       // span (rows from seq_row_base) above which partition_long applies
+    int max_parts;                 // ceil(max_context_len / partition_size), >= 1: the partials' row stride
     // Failure test only (-1 otherwise): the tile-ring kernels' CTA 0 announces
     // its stream tile withhold_tile without copying it or completing its
     // barrier, so the consumer's bounded wait expires.
@@ -107,6 +109,15 @@ size_t generic_smem_bytes(int group, int head_dim, int partition_size, int block
 // Merge of partition partials for sequences longer than one partition.
 cudaError_t launch_combine(const DecodeParams& p, pa_dtype dtype, cudaStream_t stream);
 
+// Rows per partition of a sequence whose partitions cover `span` rows (its
+// rows from seq_row_base on): partition_size, or partition_long for spans
+// above partition_long_from. A function of the sequence's own length, so a
+// sequence's partition boundaries and merge order never depend on the rest of
+// the batch.
+__host__ __device__ inline int seq_partition(const DecodeParams& p, int span) {
+    return span > p.partition_long_from ? p.partition_long : p.partition_size;
+}
+
 // First row of a sequence's partitions: 0, or with a sliding window of W rows
 // the window's first row rounded down to a 16-row tile (partition p covers
 // rows base + p * partition_size ..). Depends only on n and W.
@@ -123,5 +134,6 @@ constexpr int kDefaultPartition = 512;
 // than CTAs a small batch waits for its largest item, and there 1024 rows
 // measured slower.
 constexpr int kDefaultPartition8 = 1024;
+constexpr int kNoLongPartitions = 0x7fffffff;   // partition_long_from: one size for all
 
 }  // namespace pa

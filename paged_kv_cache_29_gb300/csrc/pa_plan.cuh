@@ -1,15 +1,16 @@
 // pa_plan.cuh -- the work list of one persistent decode launch, computed by
 // every CTA of that launch for itself.
 //
-// A work item is one (sequence, KV head, partition) of at most partition_size
-// rows (partitions start at seq_row_base: row 0, or the tile holding the first
-// row of a sliding window). The items of the batch are numbered in one global
-// order:
-//   1. every full partition (partition_size rows), by sequence, partition,
-//      KV head;
-//   2. then the partial last partitions, in kBuckets buckets of decreasing
-//      size (by sequence within a bucket), so that the last items a persistent
-//      CTA picks up are the smallest.
+// A work item is one (sequence, KV head, partition) of at most
+// seq_partition(span) rows (partitions start at seq_row_base: row 0, or the
+// tile holding the first row of a sliding window). The items of the batch
+// are numbered in one global order, largest first:
+//   1. every full partition of the sequences that take partition_long rows,
+//      by sequence, partition, KV head;
+//   2. every full partition of the others (partition_size rows), likewise;
+//   3. then the partial last partitions, in kPlanBuckets buckets of
+//      decreasing size (by sequence within a bucket), so that the last items
+//      a persistent CTA picks up are the smallest.
 // CTA c of C processes items c, 2C-1-c, 2C+c, ... (a snake, so that the
 // per-CTA totals even out). Each CTA walks the context lengths twice (the
 // prefix of full partitions, then the bucket ranks) and writes only its own
@@ -46,7 +47,7 @@ __device__ __forceinline__ int own_item_count(int c, int C, int total) {
 
 // Shared ints plan_cta needs for NT threads.
 __host__ __device__ constexpr int plan_scratch_ints(int nt) {
-    return (nt / 32) * (1 + kPlanBuckets) + 3 * kPlanBuckets + 4;
+    return (nt / 32) * (1 + kPlanBuckets) + 3 * kPlanBuckets + 4;   // carry: 4
 }
 
 // Calls f(k) for every k in [a, e) that is one of CTA c's items.
@@ -70,8 +71,37 @@ __device__ __forceinline__ int plan_len(const DecodeParams& p, int s, bool flag)
     return n;
 }
 
+// Size bucket of a partial partition of r rows: 0 for the largest (r close to
+// P, the partition size of short sequences, or above it: the partial last
+// partitions of long sequences all fall in bucket 0), kPlanBuckets - 1 for the
+// smallest.
 __device__ __forceinline__ int plan_bucket(int r, int P) {
-    return r > 0 ? min(kPlanBuckets - 1, ((P - r) * kPlanBuckets) / P) : -1;
+    return r > 0 ? min(kPlanBuckets - 1, max(0, ((P - r) * kPlanBuckets) / P)) : -1;
+}
+
+// Exclusive prefix of v over the threads of the block, starting at *carry,
+// which then grows by the block's sum. All NT threads call it; wsum holds NW
+// ints.
+template <int NW>
+__device__ __forceinline__ int block_scan(int v, int* wsum, int* carry) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int base = *carry, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) base += wsum[w];
+        total += wsum[w];
+    }
+    __syncthreads();
+    if (tid == 0) *carry += total;
+    return base + incl - v;
 }
 
 // Writes CTA c's items and returns the number of items of the launch; the
@@ -87,47 +117,43 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
     int* bcount = wcnt + NW * kPlanBuckets;  // [kPlanBuckets]
     int* bcursor = bcount + kPlanBuckets;    // [kPlanBuckets]
     int* brun = bcursor + kPlanBuckets;      // [kPlanBuckets]
-    int* carry = brun + kPlanBuckets;        // [1] full partitions so far; [1] total
+    // [0] long full partitions so far, [1] short full partitions, [2] short
+    // full partitions so far (pass 2, after the long ones), [3] total items
+    int* carry = brun + kPlanBuckets;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = p.num_seqs, P = p.partition_size, Hkv = p.num_kv_heads;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
+    const int Pb = p.partition_size;
     if (tid < kPlanBuckets) {
         bcount[tid] = 0;
         brun[tid] = 0;
     }
-    if (tid == 0) carry[0] = 0;
+    if (tid < 4) carry[tid] = 0;
     __syncthreads();
 
-    // Pass 1: exclusive prefix of full partitions, chunk by chunk; emit the
-    // full items; count partial partitions per bucket.
+    // The order: full partitions of long sequences (partition_long rows),
+    // then full partitions of the others (partition_size rows), each by
+    // sequence, partition, KV head; then the partial last partitions by size
+    // bucket, largest first, by sequence within a bucket.
+    // Pass 1: exclusive prefix of the long full partitions, chunk by chunk;
+    // emit those items; total the short full partitions; count partial
+    // partitions per bucket.
     for (int s0 = 0; s0 < B; s0 += NT) {
         const int s = s0 + tid;
         const int n = s < B ? plan_len(p, s, s % C == c) : -1;
         const int span = n > 0 ? n - seq_row_base(n, p.window) : 0;   // rows of its partitions
+        const int P = seq_partition(p, span);
+        const bool lng = P != Pb;
         const int nf = span / P;
-        int incl = nf;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        int base = carry[0], chunk = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w < warp) base += wsum[w];
-            chunk += wsum[w];
-        }
-        __syncthreads();
-        if (tid == 0) carry[0] += chunk;
-        const int pf = base + incl - nf;     // full partitions before sequence s
-        for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
-            const int unit = k / Hkv;
-            const int4 v = make_int4(s, k - unit * Hkv, unit - pf, n);
-            p.items[k] = v;
-            if (k < 2 * C) first[k / C] = v;
-        });
-        const int b = n > 0 ? plan_bucket(span % P, P) : -1;
+        const int pf = block_scan<NW>(lng ? nf : 0, wsum, &carry[0]);   // long full partitions before s
+        if (!lng && nf > 0) atomicAdd(&carry[1], nf);
+        if (lng)
+            for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
+                const int unit = k / Hkv;
+                const int4 v = make_int4(s, k - unit * Hkv, unit - pf, n);
+                p.items[k] = v;
+                if (k < 2 * C) first[k / C] = v;
+            });
+        const int b = n > 0 ? plan_bucket(span % P, Pb) : -1;
         if (b >= 0) atomicAdd(&bcount[b], 1);
         if (n == 0 && s % C == c) {
             // A fused append for an empty sequence has no row to go to.
@@ -149,21 +175,33 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
             bcursor[b] = acc;
             acc += bcount[b];
         }
-        carry[1] = (carry[0] + acc) * Hkv;
+        carry[3] = (carry[0] + carry[1] + acc) * Hkv;
+        carry[2] = carry[0];            // the short full partitions start here
     }
     __syncthreads();
-    const int full_items = carry[0] * Hkv;
-    const int total = carry[1];
+    const int full_items = (carry[0] + carry[1]) * Hkv;
+    const int total = carry[3];
 
-    // Pass 2: each partial partition's rank: bucket start, then earlier
-    // sequences of the same bucket (earlier chunks, earlier warps, earlier
-    // lanes).
+    // Pass 2: the short full partitions (prefix again, after the long ones),
+    // and each partial partition's rank: bucket start, then earlier sequences
+    // of the same bucket (earlier chunks, earlier warps, earlier lanes).
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int s0 = 0; s0 < B; s0 += NT) {
         const int s = s0 + tid;
         const int n = s < B ? plan_len(p, s, false) : -1;
         const int span = n > 0 ? n - seq_row_base(n, p.window) : 0;
-        const int b = n > 0 ? plan_bucket(span % P, P) : -1;
+        const int P = seq_partition(p, span);
+        const bool lng = P != Pb;
+        const int nf = span / P;
+        const int pf = block_scan<NW>(lng ? 0 : nf, wsum, &carry[2]);
+        if (!lng)
+            for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
+                const int unit = k / Hkv;
+                const int4 v = make_int4(s, k - unit * Hkv, unit - pf, n);
+                p.items[k] = v;
+                if (k < 2 * C) first[k / C] = v;
+            });
+        const int b = n > 0 ? plan_bucket(span % P, Pb) : -1;
         const unsigned same = __match_any_sync(0xffffffffu, b);
         if (lane < kPlanBuckets) wcnt[warp * kPlanBuckets + lane] = 0;
         __syncwarp();
@@ -173,7 +211,6 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
             int j = bcursor[b] + brun[b] + __popc(same & lt_mask);
             for (int w = 0; w < warp; ++w) j += wcnt[w * kPlanBuckets + b];
             const int a = full_items + j * Hkv;
-            const int nf = span / P;
             for_own_items(a, a + Hkv, c, C, [&](int k) {
                 const int4 v = make_int4(s, k - a, nf, n);
                 p.items[k] = v;

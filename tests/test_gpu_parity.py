@@ -70,6 +70,40 @@ def test_partition_sizes(partition):
         assert_parity(out, ref, "bf16", (kernel, partition))
 
 
+@pytest.mark.parametrize("long_p,long_from", [(1024, 1000), (2048, 600), (4096, 512)])
+def test_long_partitions(long_p, long_from):
+    """Larger partitions for sequences past a length (pa_decode_ex option):
+    parity on every kernel, lengths on both sides of the threshold, and a
+    sequence's result bitwise the same alone and inside the batch."""
+    lens = [1, 17, 511, 512, 599, 600, 601, 999, 1000, 1001, 2047, 4096, 4097, 9000, 20000]
+    step = ragged_step("bf16", 32, 8, 128, lens=lens, seed=long_p)
+    _, _, ref = oracle_reference(step)
+    opts = dict(long_partition_size=long_p, long_partition_from=long_from)
+    for kernel in ["mma", "simt", "generic"]:
+        dev = DeviceStep(step)
+        dev.append()
+        pa.pa_decode(dev.q, dev.k_cache, dev.v_cache, dev.tables, dev.lens, step.scale, dev.out,
+                     step.max_context_len, workspace=dev.workspace, error_word=dev.err,
+                     kernel=kernel, **opts)
+        torch.cuda.synchronize()
+        assert dev.error_word() == 0
+        out = dev.result()
+        assert_parity(out, ref, "bf16", (kernel, long_p, long_from))
+        if kernel == "mma":
+            # the 20,000-row sequence alone gives the same bits
+            one = wl.DecodeStep(**{**step.__dict__, "q": step.q[-1:],
+                                   "block_tables": step.block_tables[-1:],
+                                   "context_lens": step.context_lens[-1:]})
+            sub = DeviceStep(one)
+            sub.k_cache.copy_(dev.k_cache)
+            sub.v_cache.copy_(dev.v_cache)
+            pa.pa_decode(sub.q, sub.k_cache, sub.v_cache, sub.tables, sub.lens, step.scale,
+                         sub.out, 20000, workspace=sub.workspace, error_word=sub.err,
+                         kernel="mma", **opts)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(from_torch(sub.out)[0], from_torch(dev.out)[-1])
+
+
 @pytest.mark.parametrize("bs", [1, 2, 4, 8, 16, 32, 64])
 def test_block_sizes(bs):
     step = ragged_step("bf16", 8, 2, 128, bs=bs, lens=[1, 7, 16, 33, 300, 777], seed=bs)

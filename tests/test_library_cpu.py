@@ -266,3 +266,19 @@ def test_binding_refuses_tensors_on_another_device_before_any_call(monkeypatch):
     with pytest.raises(AssertionError, match="library was reached"):
         pa.pa_decode(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
                      0.1, t["out"], 64, workspace=t["workspace"])
+
+
+@pytest.mark.parametrize("long_size,long_from,status", [
+    (1024, 2048, None),                  # accepted: fails later only on the fake pointers' workspace
+    (500, 2048, pa.PA_ERR_INVALID_ARG),  # not a multiple of 16
+    (256, 2048, pa.PA_ERR_INVALID_ARG),  # smaller than the base partition (512)
+    (8192, 2048, pa.PA_ERR_INVALID_ARG), # past 4096 rows
+    (1024, -5, pa.PA_ERR_INVALID_ARG),   # negative threshold
+])
+def test_long_partition_options_checked_on_the_host(lib, long_size, long_from, status):
+    import ctypes as C
+    opts = pa._Options(0, 512, long_size, long_from)
+    args = [FAKE] * 5 + [0.1, FAKE, 4, 8, 2, 128, 16, 10, 4, 64, 1, None, 0, None]
+    rc = lib.pa_decode_ex(*args, C.byref(opts), None)
+    # with a valid option the call gets as far as the (missing) workspace
+    assert rc == (pa.PA_ERR_WORKSPACE if status is None else status)
