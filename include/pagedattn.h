@@ -291,6 +291,21 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                         size_t workspace_bytes, int32_t* error_word,
                         struct CUstream_st* stream);
 
+/* pa_decode_fp8 with explicit options (NULL = defaults; declared below):
+ * kernel PA_KERNEL_AUTO, PA_KERNEL_MMA (the tile ring with per-tile mma.sync
+ * on codes widened to f16) or PA_KERNEL_TC (tcgen05: 128-row chunks, e4m3
+ * products straight from the TMA-staged codes, q and the probabilities as
+ * three e4m3 terms each, accumulators in tensor memory); partition options as
+ * pa_decode_ex. */
+struct pa_decode_options;
+pa_status pa_decode_fp8_ex(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, float scale,
+                           float k_scale, float v_scale, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, void* workspace,
+                           size_t workspace_bytes, int32_t* error_word,
+                           const struct pa_decode_options* options, struct CUstream_st* stream);
+
 /*
  * Multi-query decode: num_queries (Q) new tokens per sequence verified
  * together, as speculative decoding does ("MLSys Engineer -- Inference Systems
@@ -389,8 +404,10 @@ pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
 typedef enum pa_kernel {
     PA_KERNEL_AUTO = 0,
     PA_KERNEL_SIMT = 1,    /* TMA tile ring, CUDA-core dot products */
-    PA_KERNEL_MMA = 2,     /* TMA tile ring, per-tile bf16 tensor-core MMA */
-    PA_KERNEL_GENERIC = 3  /* direct loads through the block table */
+    PA_KERNEL_MMA = 2,     /* TMA tile ring, per-tile tensor-core MMA (mma.sync) */
+    PA_KERNEL_GENERIC = 3, /* direct loads through the block table */
+    PA_KERNEL_TC = 4       /* FP8 caches only: 128-row chunks on the tcgen05 tensor cores
+                              (e4m3 x e4m3, accumulators in tensor memory) */
 } pa_kernel;
 
 typedef struct pa_decode_options {

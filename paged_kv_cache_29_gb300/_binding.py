@@ -29,7 +29,7 @@ PA_DEVERR_SLOT = 0x2
 PA_DEVERR_CONTEXT = 0x4
 PA_DEVERR_TIMEOUT = 0x8
 
-KERNELS = {"auto": 0, "simt": 1, "mma": 2, "generic": 3}
+KERNELS = {"auto": 0, "simt": 1, "mma": 2, "generic": 3, "tc": 4}
 DEFAULT_PARTITION = 512
 
 _lock = threading.Lock()
@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.pa_reshape_and_cache_fp8.restype = I
         L.pa_decode_fp8.argtypes = [P, P, P, P, P, F, F, F, P, I, I, I, I, I, I, I, I, P, S, P, P]
         L.pa_decode_fp8.restype = I
+        L.pa_decode_fp8_ex.argtypes = [P, P, P, P, P, F, F, F, P, I, I, I, I, I, I, I, I, P, S, P,
+                                       ctypes.POINTER(_Options), P]
+        L.pa_decode_fp8_ex.restype = I
         L.pa_test_withhold_tile.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, I, P, S, P,
                                             I, P]
         L.pa_test_withhold_tile.restype = I
@@ -270,8 +273,9 @@ def pa_reshape_and_cache_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_sca
 
 def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
                   k_scale=1.0, v_scale=1.0, workspace=None, error_word=None,
-                  stream=None) -> None:
-    """Decode attention over FP8 pools (uint8 e4m3 codes) with bf16 q/out."""
+                  stream=None, kernel: str = "auto") -> None:
+    """Decode attention over FP8 pools (uint8 e4m3 codes) with bf16 q/out.
+    kernel: "auto", "mma" (tile ring, mma.sync) or "tc" (tcgen05)."""
     import torch
     _check_cuda("k_cache", k_cache, ndim=4)
     _check_cuda("v_cache", v_cache, k_cache.dtype, 4)
@@ -294,12 +298,13 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, out, m
         need = pa_decode_workspace_size(B, hq, d, int(max_context_len))
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check_cuda("workspace", workspace)
-    rc = lib().pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                             _ptr(context_lens), float(scale), float(k_scale), float(v_scale),
-                             _ptr(out), B, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
-                             int(max_context_len), _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _ptr(error_word),
-                             _stream(stream))
+    opts = _Options(KERNELS[kernel], 0, 0, 0)
+    rc = lib().pa_decode_fp8_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), float(scale), float(k_scale), float(v_scale),
+                                _ptr(out), B, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+                                int(max_context_len), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(error_word),
+                                ctypes.byref(opts), _stream(stream))
     if rc != PA_OK:
         raise PagedAttentionError(rc, "pa_decode_fp8")
 

@@ -132,7 +132,7 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         num_heads % num_kv_heads != 0 || num_queries < 1 || window < 0 ||
         (window > 0 && num_queries > 1))
         return PA_ERR_INVALID_ARG;
-    if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_GENERIC) return PA_ERR_INVALID_ARG;
+    if (kernel_req < PA_KERNEL_AUTO || kernel_req > PA_KERNEL_TC) return PA_ERR_INVALID_ARG;
     if (partition < 16 || partition > 4096 || partition % 16 != 0) return PA_ERR_INVALID_ARG;
     if (options && options->long_partition_from != 0 &&
         (options->long_partition_from < 0 || options->long_partition_size < partition ||
@@ -182,11 +182,11 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
             return PA_ERR_UNSUPPORTED;
         kernel = PA_KERNEL_MMA;
     } else if (fp8) {
-        // One kernel family: the FP8 tensor-core tile ring.
+        // The FP8 tile ring (mma.sync on widened codes) or the tcgen05 kernel.
         if (!tma_shape || !pa::has_fp8_instance(head_dim, group) ||
-            (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA))
+            (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA && kernel != PA_KERNEL_TC))
             return PA_ERR_UNSUPPORTED;
-        kernel = PA_KERNEL_MMA;
+        if (kernel == PA_KERNEL_AUTO) kernel = pa::kFp8DefaultKernel;
     } else if (kernel == PA_KERNEL_AUTO) {
         if (tma_shape && pa::has_tma_instance(PA_KERNEL_MMA, dtype, head_dim, group, 1))
             kernel = PA_KERNEL_MMA;
@@ -194,8 +194,9 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
             kernel = PA_KERNEL_SIMT;
         else
             kernel = PA_KERNEL_GENERIC;
-    } else if (kernel != PA_KERNEL_GENERIC &&
-               (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group, 1))) {
+    } else if (kernel == PA_KERNEL_TC ||
+               (kernel != PA_KERNEL_GENERIC &&
+                (!tma_shape || !pa::has_tma_instance(kernel, dtype, head_dim, group, 1)))) {
         return PA_ERR_UNSUPPORTED;
     }
     const int largest_partition =
@@ -291,7 +292,8 @@ pa_status decode_call(const void* q, const void* k_cache, const void* v_cache,
         if (kernel == PA_KERNEL_GENERIC) {
             err = pa::launch_decode_generic(p, dtype, st);
         } else {
-            err = fp8                      ? pa::launch_decode_fp8(tk, tv, p, sm_count, st)
+            err = (fp8 && kernel == PA_KERNEL_TC) ? pa::launch_decode_fp8_tc(tk, tv, p, sm_count, st)
+                  : fp8                      ? pa::launch_decode_fp8(tk, tv, p, sm_count, st)
                   : int8                    ? pa::launch_decode_int8(tk, tv, p, sm_count, st)
                   : kernel == PA_KERNEL_MMA ? pa::launch_decode_mma(tk, tv, p, sm_count, st)
                                             : pa::launch_decode_simt(tk, tv, p, dtype, sm_count, st);
@@ -433,6 +435,21 @@ pa_status pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                        out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, PA_DTYPE_FP8_E4M3, PA_DTYPE_BF16,
                        workspace, workspace_bytes, error_word, nullptr, stream);
+}
+
+pa_status pa_decode_fp8_ex(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, float scale,
+                           float k_scale, float v_scale, void* out, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int max_context_len, void* workspace,
+                           size_t workspace_bytes, int32_t* error_word,
+                           const pa_decode_options* options, struct CUstream_st* stream) {
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || k_scale == INFINITY || v_scale == INFINITY)
+        return PA_ERR_INVALID_ARG;
+    return decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                       out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_DTYPE_FP8_E4M3, PA_DTYPE_BF16,
+                       workspace, workspace_bytes, error_word, options, stream);
 }
 
 pa_status pa_append_decode_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping,

@@ -81,6 +81,12 @@ cudaError_t launch_decode_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, int sm_count, cudaStream_t stream);
 bool has_fp8_instance(int head_dim, int group);
 
+// FP8 (e4m3) cache on the tcgen05 tensor cores: 128-row chunks, e4m3 MMAs
+// from the TMA-staged codes, accumulators in tensor memory (head dim 128; 1,
+// 2, 4 or 8 query heads per KV head; one query token, no window).
+cudaError_t launch_decode_fp8_tc(const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const DecodeParams& p, int sm_count, cudaStream_t stream);
+
 // INT8 cache with per-row scales, bf16 q/out (head dim 128; 1, 2, 4 or 8
 // query heads per KV head).
 cudaError_t launch_decode_int8(const CUtensorMap& tk, const CUtensorMap& tv,
@@ -135,5 +141,7 @@ constexpr int kDefaultPartition = 512;
 // measured slower.
 constexpr int kDefaultPartition8 = 1024;
 constexpr int kNoLongPartitions = 0x7fffffff;   // partition_long_from: one size for all
+// Kernel of pa_decode_fp8 and pa_append_decode_fp8 when none is requested.
+constexpr pa_kernel kFp8DefaultKernel = PA_KERNEL_MMA;
 
 }  // namespace pa

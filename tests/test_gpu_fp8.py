@@ -27,7 +27,7 @@ def _dev(step):
                 err=torch.zeros(1, dtype=torch.int32, device="cuda"))
 
 
-def _gpu_step(step, k_scale=1.0, v_scale=1.0, append=True, mcl=None):
+def _gpu_step(step, k_scale=1.0, v_scale=1.0, append=True, mcl=None, kernel="auto"):
     d = _dev(step)
     if append:
         pa.pa_reshape_and_cache_fp8(d["k_new"], d["v_new"], d["slots"], d["k"], d["v"],
@@ -35,7 +35,7 @@ def _gpu_step(step, k_scale=1.0, v_scale=1.0, append=True, mcl=None):
     out = torch.full_like(d["q"], float("nan"))
     pa.pa_decode_fp8(d["q"], d["k"], d["v"], d["tables"], d["lens"], step.scale, out,
                      step.max_context_len if mcl is None else mcl, k_scale, v_scale,
-                     error_word=d["err"])
+                     error_word=d["err"], kernel=kernel)
     torch.cuda.synchronize()
     return d, wl.as_f32(from_torch(out), "bf16").astype(np.float64)
 
@@ -49,9 +49,28 @@ def _oracle_step(step, k_scale=1.0, v_scale=1.0, append=True):
     return k, v, out
 
 
-def test_fp8_workload_append_and_decode():
+# Both FP8 kernels: the tile ring with mma.sync on widened codes, and the
+# tcgen05 kernel (e4m3 products on 128-row chunks, tensor-memory accumulators).
+FP8_KERNELS = ["mma", "tc"]
+
+
+@pytest.mark.parametrize("kernel", FP8_KERNELS)
+@pytest.mark.parametrize("lens,g", [([1, 2, 15, 16, 17, 100, 127, 128, 129, 300], 8),
+                                    ([5, 128, 1023, 1024, 1025, 3000], 4),
+                                    ([40, 257, 700], 2), ([33, 1200], 1)])
+def test_fp8_small_shapes(kernel, lens, g):
+    step = wl.build_step("fp8s", lens, 8 * g, 8, 128, cache_dtype="fp8", seed=len(lens) + g)
+    d, got = _gpu_step(step, kernel=kernel)
+    _, _, want = _oracle_step(step)
+    assert int(d["err"].item()) == 0
+    assert np.isfinite(got).all()
+    assert_parity(got, want, "bf16", (kernel, lens, g))
+
+
+@pytest.mark.parametrize("kernel", FP8_KERNELS)
+def test_fp8_workload_append_and_decode(kernel):
     step = wl.make("8b_gqa_fp8")
-    d, got = _gpu_step(step)
+    d, got = _gpu_step(step, kernel=kernel)
     k, v, want = _oracle_step(step)
     assert int(d["err"].item()) == 0
     np.testing.assert_array_equal(d["k"].cpu().numpy(), k)
@@ -83,12 +102,13 @@ def test_fp8_append_codes_bit_exact(new_dtype, k_scale, v_scale):
     np.testing.assert_array_equal(vd.cpu().numpy(), vc)
 
 
+@pytest.mark.parametrize("kernel", FP8_KERNELS)
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8)])
-@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 3.0)])
-def test_fp8_ragged_groups_and_scales(hq, hkv, k_scale, v_scale):
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 3.0), (0.01, 0.02)])
+def test_fp8_ragged_groups_and_scales(kernel, hq, hkv, k_scale, v_scale):
     lens = [1, 15, 16, 17, 100, 511, 512, 513, 1500, 3000]
     step = wl.build_step("fp8r", lens, hq, hkv, 128, cache_dtype="fp8", seed=hq + hkv)
-    _, got = _gpu_step(step, k_scale, v_scale)
+    _, got = _gpu_step(step, k_scale, v_scale, kernel=kernel)
     _, _, want = _oracle_step(step, k_scale, v_scale)
     # The output is v_scale times an attention over e4m3 values: the absolute
     # bar, stated for outputs of unit-size values, grows with v_scale above 1
@@ -99,7 +119,8 @@ def test_fp8_ragged_groups_and_scales(hq, hkv, k_scale, v_scale):
     assert_scaled(got, want, "bf16", f"fp8 {hq}/{hkv} scales {k_scale}, {v_scale}")
 
 
-def test_fp8_nan_codes_past_the_end_do_not_leak():
+@pytest.mark.parametrize("kernel", FP8_KERNELS)
+def test_fp8_nan_codes_past_the_end_do_not_leak(kernel):
     lens = [3, 17, 40, 600]
     step = wl.build_step("fp8nan", lens, 32, 8, 128, cache_dtype="fp8", seed=9)
     bs = step.block_size
@@ -108,16 +129,17 @@ def test_fp8_nan_codes_past_the_end_do_not_leak():
         for i in range(n, -(-n // bs) * bs):
             step.k_cache[t[i // bs], :, i % bs, :] = 0x7F
             step.v_cache[t[i // bs], :, i % bs, :] = 0xFF
-    _, got = _gpu_step(step, append=False)
+    _, got = _gpu_step(step, append=False, kernel=kernel)
     _, _, want = _oracle_step(step, append=False)
     assert np.isfinite(got).all()
     assert_parity(got, want, "bf16")
 
 
-def test_fp8_batch_invariance():
+@pytest.mark.parametrize("kernel", FP8_KERNELS)
+def test_fp8_batch_invariance(kernel):
     lens = [700, 33, 4000, 1, 515]
     big = wl.build_step("fp8b", lens, 32, 8, 128, cache_dtype="fp8", seed=3)
-    _, got_big = _gpu_step(big, append=False)
+    _, got_big = _gpu_step(big, append=False, kernel=kernel)
     for s in (0, 2, 4):
         one = wl.DecodeStep(name="one", cache_dtype="fp8", num_heads=32, num_kv_heads=8,
                             head_dim=128, block_size=16, q=big.q[s:s + 1],
@@ -126,7 +148,7 @@ def test_fp8_batch_invariance():
                             v_cache=big.v_cache, block_tables=big.block_tables[s:s + 1],
                             context_lens=big.context_lens[s:s + 1], scale=big.scale,
                             seed=0, act_dtype="bf16")
-        _, got_one = _gpu_step(one, append=False, mcl=big.max_context_len)
+        _, got_one = _gpu_step(one, append=False, mcl=big.max_context_len, kernel=kernel)
         np.testing.assert_array_equal(got_one[0], got_big[s])
 
 
