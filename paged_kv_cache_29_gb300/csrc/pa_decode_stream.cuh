@@ -73,13 +73,48 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// CTA c's first item as one warp can find it without the plan, or x = -1.
+// With one partition size for every sequence, item c of the launch (the
+// snake's first round) is, while c is below the full partitions' count times
+// Hkv, full partition c / Hkv in sequence order with KV head c % Hkv: the
+// order the plan gives its full partitions. A warp-wide scan of the
+// full-partition counts over the context lengths finds its sequence; a
+// flagged length counts no partition, as in the plan.
+__device__ __forceinline__ int4 first_item_by_warp(const DecodeParams& p, int c, int lane) {
+    if (p.partition_long != p.partition_size) return make_int4(-1, 0, 0, 0);
+    const int Hkv = p.num_kv_heads;
+    const int unit = c / Hkv;
+    int carry = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        const int n = s < p.num_seqs ? plan_len(p, s, false) : -1;
+        const int nf = n > 0 ? (n - seq_row_base(n, p.window)) / p.partition_size : 0;
+        int incl = nf;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        const int first = carry + incl - nf;   // full partitions before sequence s
+        const unsigned hit = __ballot_sync(0xffffffffu, unit >= first && unit < first + nf);
+        if (hit != 0u) {
+            const int src = __ffs(hit) - 1;
+            return make_int4(s0 + src, c - unit * Hkv, unit - __shfl_sync(0xffffffffu, first, src),
+                             __shfl_sync(0xffffffffu, n, src));
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return make_int4(-1, 0, 0, 0);
+}
+
 template <int W, int STAGES, typename Geom, int G, int D, int Math_kQBufBytes, int XBYTES,
           bool PER_WARP_ISSUE>
 struct StreamSmem {
     static constexpr int kRing = STAGES * Geom::kStageBytes;
     static constexpr int kState = 2 * G + G * D;        // m[G], l[G], o[G][D]
     static constexpr int kMerge = W * kState * 4;       // the warps' states at an item's end
-    static constexpr int kBarriers = 2 * STAGES * 8;
+    // full[STAGES], empty[STAGES], the plan's completion (+ 8 bytes of padding)
+    static constexpr int kBarriers = (2 * STAGES + 2) * 8;
     // stage_bad[STAGES], warp_bad[2 W], abort flag (+7), with per-warp issue
     // last_t[STAGES] and imeta[16]; then (16-byte aligned) the CTA's first two
     // items
@@ -109,7 +144,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     using Smem = StreamSmem<W, STAGES, Geom, G, D, Math::kQBufBytes, Math::kExtraStageBytes,
                             PER_WARP_ISSUE>;
     static_assert(Math::kExtraStageBytes % 16 == 0, "side data moves in 16-byte units");
-    static_assert(Smem::kMerge >= 4 * plan_scratch_ints((W + 1) * 32),
+    static_assert(Smem::kMerge >= 4 * plan_scratch_ints(W * 32),
                   "the plan's scratch lives in the merge area");
 
     extern __shared__ uint8_t smem_raw[];
@@ -118,16 +153,21 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float* merge = reinterpret_cast<float*>(ring + Smem::kRing);
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + Smem::kRing + Smem::kMerge);
     uint64_t* empty = full + STAGES;
-    volatile int32_t* stage_bad = reinterpret_cast<volatile int32_t*>(empty + STAGES);
+    uint64_t* plan_bar = empty + STAGES;                      // the consumers' plan is complete
+    uint64_t* q0_bar = empty + STAGES + 1;                    // the producer's copy of item 0's q
+    uint64_t* flags_base = empty + STAGES + 2;
+    volatile int32_t* stage_bad = reinterpret_cast<volatile int32_t*>(flags_base);
     volatile int32_t* warp_bad = stage_bad + STAGES;          // [2][W]: per item parity
     volatile int32_t* abort_flag = warp_bad + 2 * W;
+    volatile int32_t* total_sm = abort_flag + 1;              // the launch's item count (the plan's)
+    volatile int32_t* q0_sm = abort_flag + 2;                 // (sequence, KV head) of that copy, or -1
     // per-warp issue only: the producer's last tile per stage, item meta [2][8]
     volatile int32_t* last_t = abort_flag + 8;
     volatile int32_t* imeta = last_t + STAGES;
     int4* first_items = reinterpret_cast<int4*>(
-        reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFirstItemsOffset);   // [2]
+        reinterpret_cast<uint8_t*>(flags_base) + Smem::kFirstItemsOffset);   // [2]
     int32_t* ids_buf = reinterpret_cast<int32_t*>(
-        reinterpret_cast<uint8_t*>(empty + STAGES) + Smem::kFlags);   // [2][kMaxItemBlocks]
+        reinterpret_cast<uint8_t*>(flags_base) + Smem::kFlags);   // [2][kMaxItemBlocks]
     uint8_t* qbuf = reinterpret_cast<uint8_t*>(ids_buf + 2 * kMaxItemBlocks);   // [2][kQBufBytes]
     // [STAGES][kExtraStageBytes]: per-row scales of a stage's K and V tiles
     const uint32_t xring = smem_addr(qbuf + Smem::kQBuf);
@@ -140,6 +180,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_init(smem_addr(&full[i]), 1);
             mbar_init(smem_addr(&empty[i]), 1);
         }
+        mbar_init(smem_addr(plan_bar), 1);
+        // the producer lanes' copies (one completion each) and lane 0's note
+        mbar_init(smem_addr(q0_bar), 33);
         abort_flag[0] = 0;
         mbar_init_fence();
     }
@@ -153,10 +196,21 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     const int C = gridDim.x;
     const int c = blockIdx.x;
-    // The CTA's work list; its scratch is the merge area, free until the first
-    // item ends. The items are read back with plain (coherent) loads.
-    const int total = plan_cta<T, (W + 1) * 32>(p, c, C, reinterpret_cast<int*>(merge), first_items);
-    __syncthreads();
+    // The CTA's work list, computed by the consumer warps (named barrier 1)
+    // while the producer warp starts on the first item where it can find that
+    // item alone (below); its scratch is the merge area, free until the first
+    // item ends. The items are read back with plain (coherent) loads. The
+    // producer reads the item count and any item after its first one only
+    // after the plan barrier completes.
+    int total = 0;
+    if (warp < W) {
+        total = plan_cta<T, W * 32, 1>(p, c, C, reinterpret_cast<int*>(merge), first_items);
+        named_barrier(1, W * 32);       // every consumer's item writes precede the arrival
+        if (threadIdx.x == 0) {
+            total_sm[0] = total;
+            mbar_arrive(smem_addr(plan_bar));
+        }
+    }
     // The CTA's j-th item (x = -1: none): the first two from shared memory.
     auto own_item = [&](int j) -> int4 {
         const int k = snake_item(c, j, C);
@@ -184,7 +238,16 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // runs more than one item ahead of the slowest one. The block ids of
             // item j (one coalesced cp.async, checked against the pool) live in
             // buffer j & 1; those of item j + 1 are fetched once every lane has
-            // entered item j. Item descriptors are read two items ahead.
+            // entered item j. Item descriptors are read two items ahead, after
+            // the consumers' plan is complete.
+            bool plan_ok = true;
+            if (lane == 0) plan_ok = mbar_wait(smem_addr(plan_bar), 0);
+            plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
+            if (!plan_ok && lane == 0) {
+                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                abort_flag[0] = 1;
+            }
+            total = plan_ok ? total_sm[0] : 0;
             const int n_items = own_item_count(c, C, total);
             auto load_item = own_item;
             if (lane < STAGES) last_t[lane] = -1;
@@ -424,17 +487,61 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 cp_async_commit();
             };
-            int4 cur = load_item(0);
-            int4 nxt = load_item(1);
-            prefetch_ids(cur, ids_buf);
+            // The plan's completion: the item count, then items 0, 1, ... .
+            bool planned = false;
+            auto wait_plan = [&]() -> bool {
+                bool done = true;
+                if (lane == 0) done = mbar_wait(smem_addr(plan_bar), 0);
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (done) {
+                    total = total_sm[0];
+                    planned = true;
+                }
+                return done;
+            };
+            // The first item without the plan where the warp can find it
+            // alone (first_item_by_warp); otherwise the warp waits for the plan.
+            int4 cur = first_item_by_warp(p, c, lane);
+            if constexpr (Math::kQInSmem) {
+                // That item's q goes to the consumers' first q buffer at once
+                // (they take it from there if the plan gives them the same
+                // item, after the completion of every lane's copies and the
+                // note of which item it is).
+                if (cur.x >= 0) {
+                    const int grp0 = Math::kCausal ? p.num_heads / p.num_kv_heads : G;
+                    Math().stage_q(p, cur.x, cur.y, Math::kCausal ? grp0 * p.num_queries : G, grp0,
+                                   smem_addr(qbuf), lane);
+                }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(q0_bar))
+                             : "memory");
+                if (lane == 0) {
+                    q0_sm[0] = cur.x;
+                    q0_sm[1] = cur.y;
+                    mbar_arrive(smem_addr(q0_bar));
+                }
+            }
+            int4 nxt = make_int4(-1, 0, 0, 0);
+            bool ok = true;
+            if (cur.x < 0) {
+                ok = wait_plan();
+                if (ok) {
+                    cur = load_item(0);
+                    nxt = load_item(1);
+                }
+            }
+            if (ok) prefetch_ids(cur, ids_buf);
             int t = 0;              // stream tile counter
             int issued = 0;
-            bool ok = true;
             for (int j = 0; cur.x >= 0 && ok; ++j) {
-                const int4 nxt2 = load_item(j + 2);     // used two items from now
+                int4 nxt2 = make_int4(-1, 0, 0, 0);   // used two items from now
                 int32_t* ids = ids_buf + (j & 1) * kMaxItemBlocks;
-                prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
-                cp_async_wait_group_1();                // this item's ids have landed
+                if (planned) {
+                    nxt2 = load_item(j + 2);
+                    prefetch_ids(nxt, ids_buf + ((j + 1) & 1) * kMaxItemBlocks);
+                    cp_async_wait_group_1();            // this item's ids have landed
+                } else {
+                    cp_async_wait_all();                // the first item's ids, the only group
+                }
                 __syncwarp();
                 const int P = part_rows(cur.w);
                 const int lo = seq_row_base(cur.w, p.window) + cur.z * P;
@@ -533,6 +640,15 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                               : static_cast<const void*>(&tmap_k),
                                     fb, 0, row, 0);
                     }
+                    if (!planned && tt == min(span, STAGES) - 1) {
+                        // The ring is full with the first item's tiles: now the
+                        // plan, then the next items as in every other round.
+                        ok = wait_plan();
+                        if (!ok) break;
+                        nxt = load_item(1);
+                        nxt2 = load_item(2);
+                        prefetch_ids(nxt, ids_buf + kMaxItemBlocks);
+                    }
                     if constexpr (Math::kExtraStageBytes > 0) {
                         // Lanes 2 and 3: the tile's 16 K and 16 V row scales (64 bytes
                         // each, 64-byte aligned: the tile's first row is a multiple of
@@ -585,18 +701,35 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int4 it = item_at(0);
     int4 it_next = item_at(1);
     typename Math::QRegs q_next;
+    bool aborted = false;
     if constexpr (Math::kQInSmem) {
-        // q of item 0 now, then always one item ahead, copied by warp 0.
+        // q of item 0 now (unless the producer already copied it), then always
+        // one item ahead, copied by warp 0.
         if (warp == 0 && it.x >= 0) {
-            math.stage_q(p, it.x, it.y, ncols, grp, smem_addr(qbuf), lane);
-            cp_async_wait_all();
+            bool have = false;
+            if constexpr (!PER_WARP_ISSUE) {
+                bool landed = true;
+                if (lane == 0) landed = mbar_wait(smem_addr(q0_bar), 0);
+                landed = __shfl_sync(0xffffffffu, landed, 0);
+                if (!landed) {
+                    aborted = true;
+                    if (lane == 0) {
+                        raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                        abort_flag[0] = 1;
+                    }
+                }
+                have = landed && q0_sm[0] == it.x && q0_sm[1] == it.y;
+            }
+            if (!have) {
+                math.stage_q(p, it.x, it.y, ncols, grp, smem_addr(qbuf), lane);
+                cp_async_wait_all();
+            }
         }
         named_barrier(1, W * 32);
     } else {
         if (it.x >= 0) math.load_q(p, it.x, it.y, q_next);
     }
     int t0 = 0;                 // stream index of the current item's first tile (a multiple of W)
-    bool aborted = false;
     for (int j = 0; it.x >= 0; ++j) {
         const int s = it.x, h = it.y, part = it.z, n = it.w;
         const int base = seq_row_base(n, p.window);

@@ -79,10 +79,21 @@ __device__ __forceinline__ int plan_bucket(int r, int P) {
     return r > 0 ? min(kPlanBuckets - 1, max(0, ((P - r) * kPlanBuckets) / P)) : -1;
 }
 
-// Exclusive prefix of v over the threads of the block, starting at *carry,
-// which then grows by the block's sum. All NT threads call it; wsum holds NW
-// ints.
-template <int NW>
+// Barrier among the plan's threads: the whole CTA (BAR = 0) or the first NT
+// threads on named barrier BAR.
+template <int NT, int BAR>
+__device__ __forceinline__ void plan_sync() {
+    if constexpr (BAR == 0) {
+        __syncthreads();
+    } else {
+        named_barrier(BAR, NT);
+    }
+}
+
+// Exclusive prefix of v over the plan's NT = 32 NW threads, starting at
+// *carry, which then grows by their sum. All NT threads call it; wsum holds
+// NW ints.
+template <int NW, int BAR>
 __device__ __forceinline__ int block_scan(int v, int* wsum, int* carry) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int incl = v;
@@ -92,24 +103,25 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* carry) {
         if (lane >= off) incl += u;
     }
     if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
+    plan_sync<NW * 32, BAR>();
     int base = *carry, total = 0;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
         if (w < warp) base += wsum[w];
         total += wsum[w];
     }
-    __syncthreads();
+    plan_sync<NW * 32, BAR>();
     if (tid == 0) *carry += total;
     return base + incl - v;
 }
 
 // Writes CTA c's items and returns the number of items of the launch; the
 // CTA's first two items also go to `first` (shared memory), so that its work
-// starts without a global-memory round trip. All NT threads of the CTA call
-// it; `sm` holds plan_scratch_ints(NT) ints. Row bytes
-// of the output (num_heads * head_dim * sizeof(T)) are a multiple of 16.
-template <typename T, int NT>
+// starts without a global-memory round trip. Threads 0 .. NT - 1 of the CTA
+// call it (all of them with BAR = 0, else they meet on named barrier BAR);
+// `sm` holds plan_scratch_ints(NT) ints. Row bytes of the output (num_heads *
+// head_dim * sizeof(T)) are a multiple of 16.
+template <typename T, int NT, int BAR = 0>
 __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* first) {
     constexpr int NW = NT / 32;
     int* wsum = sm;                          // [NW]
@@ -128,7 +140,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         brun[tid] = 0;
     }
     if (tid < 4) carry[tid] = 0;
-    __syncthreads();
+    plan_sync<NT, BAR>();
 
     // The order: full partitions of long sequences (partition_long rows),
     // then full partitions of the others (partition_size rows), each by
@@ -144,7 +156,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         const int P = seq_partition(p, span);
         const bool lng = P != Pb;
         const int nf = span / P;
-        const int pf = block_scan<NW>(lng ? nf : 0, wsum, &carry[0]);   // long full partitions before s
+        const int pf = block_scan<NW, BAR>(lng ? nf : 0, wsum, &carry[0]);   // long full partitions before s
         if (!lng && nf > 0) atomicAdd(&carry[1], nf);
         if (lng)
             for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
@@ -168,7 +180,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
             for (int i = 0; i < chunks; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    __syncthreads();
+    plan_sync<NT, BAR>();
     if (tid == 0) {
         int acc = 0;
         for (int b = 0; b < kPlanBuckets; ++b) {
@@ -178,7 +190,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         carry[3] = (carry[0] + carry[1] + acc) * Hkv;
         carry[2] = carry[0];            // the short full partitions start here
     }
-    __syncthreads();
+    plan_sync<NT, BAR>();
     const int full_items = (carry[0] + carry[1]) * Hkv;
     const int total = carry[3];
 
@@ -193,7 +205,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         const int P = seq_partition(p, span);
         const bool lng = P != Pb;
         const int nf = span / P;
-        const int pf = block_scan<NW>(lng ? 0 : nf, wsum, &carry[2]);
+        const int pf = block_scan<NW, BAR>(lng ? 0 : nf, wsum, &carry[2]);
         if (!lng)
             for_own_items(pf * Hkv, (pf + nf) * Hkv, c, C, [&](int k) {
                 const int unit = k / Hkv;
@@ -206,7 +218,7 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
         if (lane < kPlanBuckets) wcnt[warp * kPlanBuckets + lane] = 0;
         __syncwarp();
         if (b >= 0 && (same & lt_mask) == 0) wcnt[warp * kPlanBuckets + b] = __popc(same);
-        __syncthreads();
+        plan_sync<NT, BAR>();
         if (b >= 0) {
             int j = bcursor[b] + brun[b] + __popc(same & lt_mask);
             for (int w = 0; w < warp; ++w) j += wcnt[w * kPlanBuckets + b];
@@ -217,13 +229,13 @@ __device__ int plan_cta(const DecodeParams& p, int c, int C, int* sm, int4* firs
                 if (k < 2 * C) first[k / C] = v;
             });
         }
-        __syncthreads();
+        plan_sync<NT, BAR>();
         if (tid < kPlanBuckets) {
             int add = 0;
             for (int w = 0; w < NW; ++w) add += wcnt[w * kPlanBuckets + tid];
             brun[tid] += add;
         }
-        __syncthreads();
+        plan_sync<NT, BAR>();
     }
     return total;
 }
