@@ -595,32 +595,16 @@ def run_native(args) -> dict | None:
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
-
-    def timed_e2e(run):
-        ms = []
-        for i in range(K):
-            flush_l2(i)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            run()
-            b.record(stream)
-            b.synchronize()
-            ms.append(a.elapsed_time(b))
-        return sum(ms)
-
-    # Eagerly (each step's copies and calls issued from the host), and as one
-    # captured CUDA graph per step (the host-to-device copy, the step's calls
-    # and the device-to-host copy, replayed every step as a serving loop
-    # replays a captured decode step). Each timed step ends with the host
-    # waiting for its output.
-    e2e_eager_total = timed_e2e(e2e_step)
-    graph_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_e2e):
+    e2e_ms = []
+    for i in range(K):
+        flush_l2(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         e2e_step()
-    for _ in range(args.warmup):
-        graph_e2e.replay()
-    torch.cuda.synchronize()
-    e2e_total = timed_e2e(graph_e2e.replay)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
 
     # Copy-on-write block copies (pa_copy_blocks): COPY_PAIRS random distinct
     # (src, dst) pairs of this pool, after every other measurement (it
@@ -643,9 +627,8 @@ def run_native(args) -> dict | None:
     torch.cuda.synchronize()
     w.check_error_word("in the timed region")
 
-    (total_ms, e2e_total, e2e_eager_total, decode_avg), (all_bytes, all_seqs) = reduce_over_ranks(
-        [total_ms, e2e_total, e2e_eager_total, decode_avg],
-        [float(bytes_.total), float(step.num_seqs)], dev)
+    (total_ms, e2e_total, decode_avg), (all_bytes, all_seqs) = reduce_over_ranks(
+        [total_ms, e2e_total, decode_avg], [float(bytes_.total), float(step.num_seqs)], dev)
     if rank != 0:
         return None
 
@@ -714,11 +697,6 @@ def run_native(args) -> dict | None:
             "d2h_bytes_per_step": d2h,
             "transfers": "inputs: one copy of a packed pinned buffer (q, new K/V rows, slots, "
                          "block tables, lengths); output: one copy to pinned memory",
-            "how": "each step one replay of a captured CUDA graph (copy in, the step's calls, "
-                   "copy out), then the host waits for the output",
-            "eager": {"value": round(all_bytes / (e2e_eager_total / K * 1e-3) / 1e9, 2),
-                      "ms_per_step": round(e2e_eager_total / K, 5),
-                      "how": "the same copies and calls issued from the host every step"},
         },
         "gpu_launches": w.launches_per_step * K,
         "gpu_launches_note": "kernels of this library in the timed graph replays",
