@@ -224,6 +224,26 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == W) {
         // ------------------------------ producer ------------------------------
+        // The CTA's first item where this warp can find it alone
+        // (first_item_by_warp); its q goes to the consumers' first q buffer at
+        // once (they take it from there if the plan gives them the same item,
+        // after the completion of every lane's copies and lane 0's note of
+        // which item it is).
+        const int4 first = first_item_by_warp(p, c, lane);
+        if constexpr (Math::kQInSmem) {
+            if (first.x >= 0) {
+                const int grp0 = Math::kCausal ? p.num_heads / p.num_kv_heads : G;
+                Math().stage_q(p, first.x, first.y, Math::kCausal ? grp0 * p.num_queries : G, grp0,
+                               smem_addr(qbuf), lane);
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(q0_bar))
+                         : "memory");
+            if (lane == 0) {
+                q0_sm[0] = first.x;
+                q0_sm[1] = first.y;
+                mbar_arrive(smem_addr(q0_bar));
+            }
+        }
         if constexpr (PER_WARP_ISSUE) {
             // Consumer warp w takes tiles w, w + W, ... of every item, in ring
             // stages w, w + W, ... . Lane w < W of this warp issues warp w's tiles
@@ -238,21 +258,29 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // runs more than one item ahead of the slowest one. The block ids of
             // item j (one coalesced cp.async, checked against the pool) live in
             // buffer j & 1; those of item j + 1 are fetched once every lane has
-            // entered item j. Item descriptors are read two items ahead, after
-            // the consumers' plan is complete.
-            bool plan_ok = true;
-            if (lane == 0) plan_ok = mbar_wait(smem_addr(plan_bar), 0);
-            plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
-            if (!plan_ok && lane == 0) {
-                raise_error(p.error_word, PA_DEVERR_TIMEOUT);
-                abort_flag[0] = 1;
-            }
-            total = plan_ok ? total_sm[0] : 0;
-            const int n_items = own_item_count(c, C, total);
+            // entered item j. Item descriptors are read two items ahead, once
+            // the consumers' plan is complete; the first item, where this warp
+            // found it alone, starts before that (its item count unknown
+            // until then: no lane leaves the first item before the plan).
+            bool planned = false;
+            int n_items = INT_MAX;
             auto load_item = own_item;
+            if (first.x < 0) {
+                bool plan_ok = true;
+                if (lane == 0) plan_ok = mbar_wait(smem_addr(plan_bar), 0);
+                plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
+                if (!plan_ok && lane == 0) {
+                    raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                    abort_flag[0] = 1;
+                }
+                total = plan_ok ? total_sm[0] : 0;
+                n_items = own_item_count(c, C, total);
+                planned = true;
+            }
             if (lane < STAGES) last_t[lane] = -1;
-            int4 d_req = load_item(0);      // descriptor of item jl, the next whose ids to fetch
-            int4 d_req2 = load_item(1);
+            // descriptor of item jl, the next whose ids to fetch, and the one after
+            int4 d_req = planned ? load_item(0) : first;
+            int4 d_req2 = planned ? load_item(1) : make_int4(-1, 0, 0, 0);
             int4 d_val = make_int4(-1, 0, 0, 0);   // descriptor of the requested, unchecked item
             // Fused append: this lane's share of that item's new K and V rows,
             // loaded at the request (used once its block ids are checked).
@@ -291,8 +319,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         new_v = __ldg(static_cast<const uint2*>(p.v_new) + src + lane);
                     }
                 }
-                d_req = d_req2;
-                d_req2 = load_item(jl + 1);
+                if (planned) {
+                    d_req = d_req2;
+                    d_req2 = load_item(jl + 1);
+                } else {
+                    d_req = make_int4(-1, 0, 0, 0);   // read once the plan is complete
+                }
             };
             auto validate = [&](int j) {
                 cp_async_wait_all();
@@ -337,7 +369,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (n_items > 0) {
                 request();
                 validate(0);
-                if (jl < n_items) request();
+                if (planned && jl < n_items) request();
                 // lane w < W: warp w's item and next tile within it, and that item's meta
                 int cj = 0, ci = 0;
                 int h = 0, lo = 0, b0 = 0, ntiles = 0, share = 0, t0 = 0, bad = 0;
@@ -349,6 +381,19 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 uint32_t idle_rounds = 0;
                 uint64_t idle_since = 0;
                 while (true) {
+                    if (!planned) {
+                        // The plan (not waited for): the item count and the
+                        // descriptors of the items after the first.
+                        bool done = false;
+                        if (lane == 0) done = mbar_test_wait(smem_addr(plan_bar), 0);
+                        if (__shfl_sync(0xffffffffu, done, 0)) {
+                            planned = true;
+                            total = total_sm[0];
+                            n_items = own_item_count(c, C, total);
+                            d_req = load_item(jl);
+                            d_req2 = load_item(jl + 1);
+                        }
+                    }
                     // Issue first (a lane woken by its stage's release refills it
                     // at once), then the item bookkeeping.
                     bool moved = false;
@@ -410,7 +455,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     if (jmin == INT_MAX) break;                 // every tile issued
                     // The ids of the next item: buffer jl & 1 last held item jl - 2,
                     // which every lane has left.
-                    if (jl < n_items && jl == ready && jl <= jmin + 1) {
+                    if (planned && jl < n_items && jl == ready && jl <= jmin + 1) {
                         request();
                         moved = true;
                     }
@@ -501,25 +546,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
             };
             // The first item without the plan where the warp can find it
             // alone (first_item_by_warp); otherwise the warp waits for the plan.
-            int4 cur = first_item_by_warp(p, c, lane);
-            if constexpr (Math::kQInSmem) {
-                // That item's q goes to the consumers' first q buffer at once
-                // (they take it from there if the plan gives them the same
-                // item, after the completion of every lane's copies and the
-                // note of which item it is).
-                if (cur.x >= 0) {
-                    const int grp0 = Math::kCausal ? p.num_heads / p.num_kv_heads : G;
-                    Math().stage_q(p, cur.x, cur.y, Math::kCausal ? grp0 * p.num_queries : G, grp0,
-                                   smem_addr(qbuf), lane);
-                }
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(q0_bar))
-                             : "memory");
-                if (lane == 0) {
-                    q0_sm[0] = cur.x;
-                    q0_sm[1] = cur.y;
-                    mbar_arrive(smem_addr(q0_bar));
-                }
-            }
+            int4 cur = first;
             int4 nxt = make_int4(-1, 0, 0, 0);
             bool ok = true;
             if (cur.x < 0) {
@@ -706,20 +733,17 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // q of item 0 now (unless the producer already copied it), then always
         // one item ahead, copied by warp 0.
         if (warp == 0 && it.x >= 0) {
-            bool have = false;
-            if constexpr (!PER_WARP_ISSUE) {
-                bool landed = true;
-                if (lane == 0) landed = mbar_wait(smem_addr(q0_bar), 0);
-                landed = __shfl_sync(0xffffffffu, landed, 0);
-                if (!landed) {
-                    aborted = true;
-                    if (lane == 0) {
-                        raise_error(p.error_word, PA_DEVERR_TIMEOUT);
-                        abort_flag[0] = 1;
-                    }
+            bool landed = true;
+            if (lane == 0) landed = mbar_wait(smem_addr(q0_bar), 0);
+            landed = __shfl_sync(0xffffffffu, landed, 0);
+            if (!landed) {
+                aborted = true;
+                if (lane == 0) {
+                    raise_error(p.error_word, PA_DEVERR_TIMEOUT);
+                    abort_flag[0] = 1;
                 }
-                have = landed && q0_sm[0] == it.x && q0_sm[1] == it.y;
             }
+            const bool have = landed && q0_sm[0] == it.x && q0_sm[1] == it.y;
             if (!have) {
                 math.stage_q(p, it.x, it.y, ncols, grp, smem_addr(qbuf), lane);
                 cp_async_wait_all();
