@@ -1,7 +1,7 @@
 """Benchmark of one paged-attention decode step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b_gqa]
-                    [--kernel auto|mma|simt|generic] [--impl native|reference]
+                    [--kernel auto|mma|simt|generic|tc] [--impl native|reference]
 
 A step is the whole hot path over one batch: pa_reshape_and_cache (append the
 new K/V rows) then pa_decode (attention through the block tables, with the
@@ -365,7 +365,9 @@ class DeviceWorkload:
                                                step.head_dim, step.max_context_len)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self.pa = pa
-        self.fused = step.num_queries == 1 and step.window == 0
+        # (the fused calls take no kernel choice: a requested kernel runs the
+        # append call, then the decode call with that kernel)
+        self.fused = step.num_queries == 1 and step.window == 0 and kernel == "auto"
         # append (not in the fused step), decode, and the split-K merge when a
         # sequence can span more than one partition (at most 4096 sequences:
         # one launch each)
@@ -396,7 +398,7 @@ class DeviceWorkload:
                               self.tables, self.lens, s.scale, self.out, mcl, **common)
         elif self.fp8:
             pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.tables, self.lens, s.scale,
-                             self.out, mcl, s.k_scale, s.v_scale, **common)
+                             self.out, mcl, s.k_scale, s.v_scale, kernel=self.kernel, **common)
         elif s.num_queries > 1:
             pa.pa_decode_multi(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
                                s.scale, self.out, mcl, **common)
@@ -522,6 +524,19 @@ def workload_summary(pa, name: str, args, dev, flush, stream, peak: float,
     return res
 
 
+def kernel_supported(step: wl.DecodeStep, kernel: str) -> bool:
+    """Whether the workload's decode call takes this kernel choice: bf16/fp32
+    single-query decode any of mma, simt, generic; FP8 mma or tc; INT8,
+    multi-query and window calls only their default."""
+    if kernel == "auto":
+        return True
+    if step.cache_dtype == "fp8":
+        return kernel in ("mma", "tc")
+    if step.cache_dtype == "int8" or step.num_queries > 1 or step.window > 0:
+        return False
+    return kernel in ("mma", "simt", "generic")
+
+
 def run_native(args) -> dict | None:
     import torch
     import paged_kv_cache_29_gb300 as pa
@@ -535,6 +550,8 @@ def run_native(args) -> dict | None:
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     step = wl.make(args.workload, seed=wl.WORKLOAD_SEEDS[args.workload] + 1000 * rank)
+    if not kernel_supported(step, args.kernel):
+        raise SystemExit(f"--kernel {args.kernel} does not apply to workload {args.workload}")
     bytes_ = accounting.step_bytes_for(step)
     cd = step.cache_dtype
     mcl = step.max_context_len
@@ -790,7 +807,8 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="8b_gqa", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt", "generic"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "simt", "generic", "tc"],
+                    help="decode kernel (bf16/fp32 caches: mma, simt, generic; FP8: mma, tc)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle time of the CPU baseline sample")

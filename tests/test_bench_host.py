@@ -1,7 +1,7 @@
 """bench.py's host-side pieces on the CPU: the packed layout of a step's
 inputs (one host buffer, one copy per end-to-end step) holds every array
 unchanged, 256-byte aligned, and the same layout cut from another buffer
-gives the same views."""
+gives the same views; which --kernel choices apply to which workload."""
 import numpy as np
 import pytest
 import torch
@@ -32,3 +32,18 @@ def test_packed_inputs_round_trip(name):
     _, again = bench.packed_buffer(arrays, storage=buf.clone())
     for a, v in zip(arrays, again):
         np.testing.assert_array_equal(_host(v), a)
+
+
+def test_kernel_choices_per_workload():
+    """--kernel applies where the workload's decode call takes a kernel
+    choice; elsewhere the run stops before touching the GPU."""
+    tiny, fp8 = wl.make("tiny"), wl.make("8b_gqa_fp8")
+    for k in ("auto", "mma", "simt", "generic"):
+        assert bench.kernel_supported(tiny, k)
+    assert not bench.kernel_supported(tiny, "tc")
+    assert bench.kernel_supported(fp8, "tc") and bench.kernel_supported(fp8, "mma")
+    assert not bench.kernel_supported(fp8, "simt")
+    for name in ("8b_gqa_int8", "8b_gqa_mq2", "8b_gqa_win1024"):
+        step = wl.make(name)
+        assert bench.kernel_supported(step, "auto")
+        assert not any(bench.kernel_supported(step, k) for k in ("mma", "simt", "generic", "tc"))
