@@ -2,10 +2,18 @@
 //
 // Work item: one (sequence s, KV head h, partition p) of at most
 // partition_size rows. A fixed set of CTAs (a few per SM) shares the items of
-// the launch; each CTA first computes and stores its own items (pa_plan.cuh:
-// full partitions first, then the partial last partitions, largest first,
-// dealt out in a snake) and then streams all of their tiles through one ring
-// without stopping between items.
+// the launch; each CTA computes and stores its own items (pa_plan.cuh: full
+// partitions first, then the partial last partitions, largest first, dealt
+// out in a snake) and streams all of their tiles through one ring without
+// stopping between items.
+//
+// Start-up: the consumer warps compute the CTA's work list while the producer
+// warp finds the CTA's first item alone where it can (first_item_by_warp: a
+// warp scan of the context lengths), fetches its block ids, issues its first
+// tiles and copies its q into the consumers' first q buffer (an mbarrier
+// completed by the copies and by a note of which item it is). The producer
+// reads the item count and the items after the first once the plan's
+// mbarrier completes.
 //
 // Producer warp: for each item, loads its block ids (one coalesced load,
 // validated against the pool, prefetched one item ahead), then for every
@@ -29,15 +37,18 @@
 // the area for the next item (one buffer: with 8 query columns a second one
 // would cost a CTA per SM).
 //
-// Sizing: a random 4 KB tile gather streams at about 6.6 TB/s on GB300 only
-// with four or more independent rings per SM (a ring's single producer waits
-// on its oldest stage); deeper rings in fewer CTAs stream slower. So the
-// kernel runs several small CTAs per SM, each with a short ring.
+// Sizing: a random 4 KB tile gather streams at 6.6-6.8 TB/s on GB300 only
+// with three or more producers per SM: one producer's per-tile issue chain
+// (wait for the oldest stage, arrive with the byte count, issue the copies)
+// moves ~15 GB/s however deep its ring. So the kernel runs several small CTAs
+// per SM, each with a short ring.
 //
 // Programmatic dependent launch: only ring and barrier set-up come before
 // griddepcontrol.wait; every global access (context lengths, the work list,
 // block tables, q, the KV pool, the output) comes after it, so a launch never
-// touches memory that the kernel before it on the stream still uses.
+// touches memory that the kernel before it on the stream still uses. The
+// merge kernel after it may launch at once (griddepcontrol.launch_dependents
+// right after the wait) and waits for this grid itself.
 #pragma once
 
 #include <atomic>

@@ -47,3 +47,14 @@ def test_kernel_choices_per_workload():
         step = wl.make(name)
         assert bench.kernel_supported(step, "auto")
         assert not any(bench.kernel_supported(step, k) for k in ("mma", "simt", "generic", "tc"))
+
+
+def test_kernel_source_hash_follows_code_not_comments(tmp_path):
+    """The profile guard's hash changes with the kernel code only."""
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* a) {\n    a[0] = 1;   /* one */\n}\n")
+    h0 = bench.kernel_source_hash(str(tmp_path))
+    src.write_text("// another header\n\n__global__ void k(int* a) {\n    a[0] = 1;   // one\n}\n")
+    assert bench.kernel_source_hash(str(tmp_path)) == h0
+    src.write_text("// header\n__global__ void k(int* a) {\n    a[0] = 2;\n}\n")
+    assert bench.kernel_source_hash(str(tmp_path)) != h0
